@@ -1,0 +1,192 @@
+/*
+ * convrot.h -- C ABI of libconvrot, a GB300 (sm_103a) implementation of the
+ * ConvRot INT8 linear layer.
+ *
+ * What the layer computes (MOSS-Image LoRA training guide,
+ * docs/moss_image_train_network.md, section 7.1 "VRAM Usage Optimization",
+ * paragraph "ConvRot INT8"; sd-scripts pull request #2461 "ConvRot INT8",
+ * Summary):
+ *   - frozen base weights W[N,K] are rotated along K by a block-diagonal,
+ *     normalised Sylvester-Hadamard matrix R = I (x) H_b / sqrt(b) and
+ *     quantized to int8 one output row (channel) at a time, with one fp32
+ *     scale per row;
+ *   - at run time each activation row is rotated by the same R and quantized
+ *     per row to int8 with a dynamic absmax scale;
+ *   - an int8 x int8 GEMM accumulates exactly and a dequantization epilogue
+ *     multiplies by scale_x[m] * scale_w[n] and writes bf16.  Because R is
+ *     orthogonal, (x R)(W R)^T = x W^T;
+ *   - for a frozen base only the input gradient is needed;
+ *   - the token embedding table is stored the same way, so a lookup
+ *     dequantizes the row and applies the inverse rotation (R is symmetric
+ *     and orthogonal, hence its own inverse).
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is a DEVICE pointer, 16-byte aligned, row-major and
+ *     contiguous unless a leading dimension is given.  bf16 and fp16 tensors
+ *     are passed as uint16_t bit patterns.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  All work is
+ *     enqueued on it; no entry point synchronises except convrot_get_error.
+ *   - The caller owns every buffer; the library allocates no device memory.
+ *   - Fixed dtypes: bf16 activations/weights/outputs, int8 codes, fp32 scales.
+ *     No dtype is inferred from another tensor.
+ *   - Block sizes: block in {8, 16, 32, 64, 128, 256}; the rotated length must
+ *     be a multiple of block and of 16, and at most CONVROT_MAX_ROW.
+ *   - Argument errors are returned synchronously and nothing is enqueued.
+ *     CONVROT_ERR_CUDA means a launch failed.  Errors found on the device (an
+ *     out-of-range token id, a pipeline wait that exceeded its time limit) set
+ *     a sticky device word that convrot_get_error() reports and clears.
+ *   - Inputs must be finite.  Empty problems (M, N or n equal to 0) are valid
+ *     and enqueue nothing.
+ */
+#ifndef CONVROT_H
+#define CONVROT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CONVROT_API __attribute__((visibility("default")))
+#else
+#define CONVROT_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CONVROT_OK = 0,
+    CONVROT_ERR_INVALID_ARG = 1,   /* bad size, block, alignment or null pointer */
+    CONVROT_ERR_UNSUPPORTED = 2,   /* no sm_100-family GPU, or size beyond a limit */
+    CONVROT_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+    CONVROT_ERR_TIMEOUT = 4,       /* a device-side pipeline wait hit its limit */
+    CONVROT_ERR_INDEX = 5          /* an embedding id was outside [0, V) */
+} convrot_status;
+
+/* Longest row the rotate-and-quantize kernels accept (elements). */
+#define CONVROT_MAX_ROW 32768
+
+typedef void *convrot_stream_t; /* a cudaStream_t */
+
+/* Human-readable name of a status code (static string). */
+CONVROT_API const char *convrot_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+CONVROT_API int convrot_version(void);
+
+/* Synchronises `stream`, then reports and clears the device error word:
+ * CONVROT_ERR_INDEX / CONVROT_ERR_TIMEOUT if a kernel recorded one since the
+ * last call, CONVROT_ERR_CUDA if the stream itself failed, else CONVROT_OK. */
+CONVROT_API int convrot_get_error(convrot_stream_t stream);
+
+/* ---------------------------------------------------------------- weights -- */
+
+/* Load-time weight quantization (guide 7.1: int8 per output channel; PR #2461
+ * Summary: the base is quantized while loading, after any LoRA has been merged
+ * into it; voxprint-model-forge MOSS page: the merge is W + scale*(alpha/rank)*B@A).
+ *   W        bf16 [N, K], row stride ldw (elements, >= K, multiple of 8).
+ *   lora_A   fp32 [rank, K] or NULL; lora_B fp32 [N, rank] or NULL (both or neither).
+ *            When given, W' = bf16_rne(W + c * B@A) with c = fp32(scale*alpha/rank),
+ *            evaluated in fp32 with sequential fused multiply-adds over the rank.
+ *   Wq       out int8 [N, K] contiguous: codes of the rows of W' R.
+ *   scale_w  out fp32 [N]: max|row of W' R| / 127 (0 for an all-zero row).
+ * Row slabs (the row-chunked quantization of a large embedding table) are the
+ * same call on W + row0*ldw with N = rows of the slab and lora_B + row0*rank.
+ * 1 <= rank <= 64 when the LoRA pair is given. */
+CONVROT_API int convrot_quantize_weight(const uint16_t *W, int64_t N, int64_t K, int64_t ldw, int block,
+                            const float *lora_A, const float *lora_B, int rank, float alpha,
+                            float scale, int8_t *Wq, float *scale_w, convrot_stream_t stream);
+
+/* ------------------------------------------------------------ activations -- */
+
+/* Online activation rotation + dynamic per-row quantization (guide 7.1; PR
+ * #2461 Summary on convrot_int8_kernels.py).
+ *   x        bf16 [M, K], row stride ldx (elements, >= K, multiple of 8).
+ *   xq       out [M, K] contiguous: the int8 codes of x R stored as fp16 values
+ *            (every code in [-127, 127] is exact in fp16; this is the operand
+ *            format of the GEMM below, whose tensor-core path reads fp16).
+ *   scale_x  out fp32 [M]. */
+CONVROT_API int convrot_quantize_activation(const uint16_t *x, int64_t M, int64_t K, int64_t ldx, int block,
+                                uint16_t *xq, float *scale_x, convrot_stream_t stream);
+
+/* The fused int8 GEMM + dequantization epilogue on quantized operands:
+ *   y[m,n] = bf16_rne( float(acc[m,n]) * (scale_x[m] * scale_w[n]) + bias[n] ),
+ *   acc[m,n] = sum_k xq[m,k] * Wq[n,k]   (exact integer sum, as int32)
+ *   xq       [M, K] fp16-held codes (from convrot_quantize_activation).
+ *   Wq       int8 [N, K]; scale_w fp32 [N]; bias bf16 [N] or NULL.
+ *   y        out bf16 [M, N] contiguous.
+ * K multiple of 16 and <= 2^20; N multiple of 16. */
+CONVROT_API int convrot_gemm_dequant(const uint16_t *xq, const float *scale_x, int64_t M, int64_t K,
+                         const int8_t *Wq, const float *scale_w, int64_t N, const uint16_t *bias,
+                         uint16_t *y, convrot_stream_t stream);
+
+/* Bytes of workspace convrot_linear_fwd / convrot_linear_bwd_x need for M rows
+ * of length K (the fp16-held codes and the fp32 scales). */
+CONVROT_API size_t convrot_act_workspace_bytes(int64_t M, int64_t K);
+
+/* Forward of the ConvRot INT8 linear layer: convrot_quantize_activation into
+ * `workspace`, then convrot_gemm_dequant.  x bf16 [M, K] contiguous; y bf16
+ * [M, N]; workspace device memory of at least convrot_act_workspace_bytes(M, K),
+ * 256-byte aligned.  The workspace must not be shared by calls in flight on
+ * other streams. */
+CONVROT_API int convrot_linear_fwd(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq,
+                       const float *scale_w, int64_t N, int block, const uint16_t *bias,
+                       uint16_t *y, void *workspace, size_t ws_bytes, convrot_stream_t stream);
+
+/* -------------------------------------------------------- frozen backward -- */
+
+/* Bytes of workspace convrot_prepare_bwd_weight needs ([K, N] fp64). */
+CONVROT_API size_t convrot_bwd_weight_workspace_bytes(int64_t N, int64_t K);
+
+/* One-off preparation of the int8 backward weight (guide 7.1 and 4.1: the
+ * opt-in int8 backward computes the input gradient with the same fused int8
+ * GEMM as the forward; PR #2461 Summary: the base is frozen, so only grad_x).  The GEMM is reused
+ * unchanged, so its weight operand must be a ConvRot quantization along the
+ * new contraction dimension N:
+ *   W_eff    = (scale_w (.) Wq) R      (the dequantized base in the original basis, fp64)
+ *   WtQ      out int8 [K, N]: codes of the rows of W_eff^T rotated along N
+ *   scale_wt out fp32 [K]
+ * N and K multiples of block and of 16; workspace >= convrot_bwd_weight_workspace_bytes. */
+CONVROT_API int convrot_prepare_bwd_weight(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K,
+                               int block, int8_t *WtQ, float *scale_wt, void *workspace,
+                               size_t ws_bytes, convrot_stream_t stream);
+
+/* Input gradient of the frozen layer through the int8 GEMM:
+ *   dX = bf16( acc * scale_dy[m] * scale_wt[k] ),  acc = quant(dY R_N) . WtQ^T
+ *   dY bf16 [M, N]; WtQ int8 [K, N]; scale_wt fp32 [K]; dX out bf16 [M, K];
+ *   workspace >= convrot_act_workspace_bytes(M, N). */
+CONVROT_API int convrot_linear_bwd_x(const uint16_t *dY, int64_t M, int64_t N, const int8_t *WtQ,
+                         const float *scale_wt, int64_t K, int block, uint16_t *dX,
+                         void *workspace, size_t ws_bytes, convrot_stream_t stream);
+
+/* -------------------------------------------------------------- embedding -- */
+
+/* Quantized token-embedding lookup (PR #2461 Summary: the int8 text encoder
+ * quantizes embed_tokens in the rotated basis, so the lookup dequantizes the
+ * rows and applies the inverse rotation).
+ *   ids      int64 [n]; Eq int8 [V, D]; scale_e fp32 [V]
+ *   out      bf16 [n, D]: bf16_rne((scale_e[id] * Eq[id,:]) R)
+ * An id outside [0, V) produces a zero row and sets CONVROT_ERR_INDEX in the
+ * device error word (no out-of-bounds read). */
+CONVROT_API int convrot_embedding_lookup(const int64_t *ids, int64_t n, const int8_t *Eq, const float *scale_e,
+                             int64_t V, int64_t D, int block, uint16_t *out,
+                             convrot_stream_t stream);
+
+/* ------------------------------------------------------------- test entry -- */
+
+/* Bytes of workspace convrot_gemm_s32 needs (A widened to fp16 codes). */
+CONVROT_API size_t convrot_gemm_s32_workspace_bytes(int64_t M, int64_t K);
+
+/* The GEMM's exact integer accumulator, for bit-exact checks:
+ *   C[m,n] = sum_k A[m,k] * B[n,k] as int32, A int8 [M, K], B int8 [N, K].
+ * Runs the same tensor-core kernel as convrot_gemm_dequant with an int32
+ * epilogue.  Entries of A and B must lie in [-127, 127] (the codes the
+ * quantizers produce).  K multiple of 16 and <= 2^17 (so |C| < 2^31). */
+CONVROT_API int convrot_gemm_s32(const int8_t *A, const int8_t *B, int64_t M, int64_t N, int64_t K,
+                     int32_t *C, void *workspace, size_t ws_bytes, convrot_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONVROT_H */

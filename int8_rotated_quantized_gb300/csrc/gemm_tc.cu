@@ -1,0 +1,526 @@
+// Fused int8 GEMM + dequantization epilogue for sm_103a (tcgen05 + TMA + TMEM).
+//
+// Computes acc[m,n] = sum_k A[m,k] * B[n,k] exactly, then either writes acc as
+// int32 or y = bf16(float(acc) * (sa[m] * sb[n]) + bias[n])
+// (sd-scripts PR #2461, ConvRot INT8, Summary: the int8 GEMM is fused with
+// the activation rotation/quantization and a dequantization epilogue;
+// MOSS-Image LoRA training guide, section 7.1).
+//
+// Integer arithmetic on the tensor cores of sm_103a.  The int8 MMA kind of
+// tcgen05 is not available on this target, so the integer codes enter the
+// kind::f16 MMA as fp16 values: every code in [-127, 127] is exact in fp16,
+// every product (|p| <= 16129) is exact in fp32, and a sum of integers stays
+// exact in the fp32 accumulator while every partial sum is below 2^24.  The K
+// loop is therefore cut into chunks of 1024 (1024 * 16129 < 2^24): each chunk
+// accumulates into its own TMEM buffer, and the epilogue warps convert the
+// chunk to int32 and add it to an int32 accumulator held in registers.  The
+// result is the exact int32 dot product for any codes in [-127, 127].
+//
+// Operands.  A holds the activation codes already widened to fp16 by the
+// rotate-and-quantize kernel; B holds the int8 weight codes as stored.  TMA
+// brings A tiles (128B swizzle, the layout the MMA reads) and raw int8 B tiles
+// into shared memory; a converter warpgroup widens each B tile to fp16 into a
+// 128B-swizzled K-major buffer.
+//
+// CTA roles (512 threads, one persistent CTA per SM, 128x256 output tiles):
+//   warp 0        TMA producer (one lane)
+//   warp 1        TMEM allocator and MMA issuer (one lane)
+//   warps 2-3     idle (complete warpgroup 0 for setmaxnreg)
+//   warps 4-7     int8 -> fp16 converters of the B tiles
+//   warps 8-15    epilogue: TMEM -> registers, int32 accumulation, output
+// Pipelines: a 4-stage TMA ring (A fp16 16 KB + B int8 16 KB), a 2-stage
+// converted-B ring (32 KB), and two 128x256 fp32 TMEM accumulators (512
+// columns) alternating per K chunk so the epilogue drains one while the MMA
+// fills the other.  Every wait is bounded: on expiry the kernel records
+// DEVERR_TIMEOUT, lets in-flight copies and MMAs finish, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace convrot {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int STAGES = 4, CSTAGES = 2;
+constexpr int CHUNK_KB = 16;  // K blocks per exact fp32 chunk: 16 * 64 = 1024
+constexpr int NUM_THREADS = 512;
+constexpr int A_STAGE = BM * BK * 2;    // 16 KB
+constexpr int BI8_STAGE = BN * BK;      // 16 KB
+constexpr int BH_STAGE = BN * BK * 2;   // 32 KB
+constexpr int OFF_A = 0;
+constexpr int OFF_BI8 = OFF_A + STAGES * A_STAGE;
+constexpr int OFF_BH = OFF_BI8 + STAGES * BI8_STAGE;
+constexpr int OFF_BAR = OFF_BH + CSTAGES * BH_STAGE;
+constexpr int NUM_BARS = 17;
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
+constexpr int TMEM_COLS = 512;
+constexpr int REGS_WG0 = 48, REGS_CONV = 72, REGS_EPI = 192;
+static_assert(128 * REGS_WG0 + 128 * REGS_CONV + 256 * REGS_EPI <= 65536, "register split exceeds the launch pool");
+
+// Barrier indices.
+constexpr int BAR_TMA_FULL = 0, BAR_TMA_EMPTY = 4, BAR_CONV_FULL = 8, BAR_CONV_EMPTY = 10, BAR_ACC_FULL = 12,
+              BAR_ACC_EMPTY = 14, BAR_DRAIN = 16;
+
+// kind::f16 instruction descriptor: D fp32, A and B fp16, both K-major,
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+struct GemmArgs {
+    int M, N, K;
+    const float *sa, *sb;
+    const uint16_t *bias;
+    void *out;
+    unsigned *err;
+};
+
+// ------------------------------------------------------------- PTX wrappers --
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on the phase with the given parity.  Returns false if another
+// role aborted or the wall-clock limit expired (then the abort flag is set and
+// the error word records a timeout).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(err, DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag: used while draining in-flight work.
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) return;
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            dst),
+        "l"(map), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
+        "[%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major operand tile stored in 128-byte
+// swizzle atoms (8 rows x 128 bytes, atoms 1024 bytes apart along M/N):
+// start address >> 4 (bits 0-13), leading byte offset >> 4 (bits 16-29, not
+// used by swizzled K-major layouts), stride byte offset >> 4 (bits 32-45),
+// descriptor version 1 (bit 46), swizzle mode 2 = 128B (bits 61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// All 512 threads meet here at the end; each role reaches it from its own
+// branch, so no code runs after a join of regions with different register
+// budgets.
+__device__ __forceinline__ void end_barrier() {
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"n"(NUM_THREADS) : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Grouped raster: 8 M-blocks per group so the CTAs in flight share A and B
+// tiles in L2.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int &mb, int &nb) {
+    constexpr int GM = 8;
+    const int group_size = GM * num_n;
+    const int group = tile / group_size;
+    const int first_m = group * GM;
+    const int gm = min(num_m - first_m, GM);
+    const int in_group = tile - group * group_size;
+    mb = first_m + in_group % gm;
+    nb = in_group / gm;
+}
+
+// int8 x 4 -> two fp16x2 words holding the same integers: bias each byte by
+// 128 (xor 0x80), splice it under the fp16 exponent of 1024 (0x64), and
+// subtract 1152 = 1024 + 128 exactly.
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t x = w ^ 0x80808080u;
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(x), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(x), "r"(0x64646464u));
+    const __half2 k = __half2half2(__ushort_as_half((unsigned short)0x6480));
+    __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), k);
+    __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), k);
+    lo = *reinterpret_cast<uint32_t *>(&ha);
+    hi = *reinterpret_cast<uint32_t *>(&hb);
+}
+
+// ------------------------------------------------------------------ kernel --
+
+template <bool OUT_S32>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_s8_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    const uint32_t sA = base + OFF_A, sBi8 = base + OFF_BI8, sBh = base + OFF_BH, sBar = base + OFF_BAR;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+    auto bar = [&](int i) -> uint32_t { return sBar + 8u * (uint32_t)i; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(bar(BAR_TMA_FULL + i), 1);
+            mbar_init(bar(BAR_TMA_EMPTY + i), 1 + 4);  // MMA commit + 4 converter warps
+        }
+        for (int i = 0; i < CSTAGES; ++i) {
+            mbar_init(bar(BAR_CONV_FULL + i), 4);
+            mbar_init(bar(BAR_CONV_EMPTY + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(BAR_ACC_FULL + i), 1);
+            mbar_init(bar(BAR_ACC_EMPTY + i), 8);
+        }
+        mbar_init(bar(BAR_DRAIN), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int num_m = (p.M + BM - 1) / BM;
+    const int num_n = (p.N + BN - 1) / BN;
+    const int num_tiles = num_m * num_n;
+    const int num_kb = (p.K + BK - 1) / BK;
+
+    if (warp < 4) {
+        regs_dec<REGS_WG0>();
+        if (warp == 0 && lane == 0) {
+            // ---------------------------------------------------- producer
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                int mb, nb;
+                tile_coords(tile, num_m, num_n, mb, nb);
+                for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    if (!mbar_wait(bar(BAR_TMA_EMPTY + s), ((it / STAGES) & 1) ^ 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(bar(BAR_TMA_FULL + s), A_STAGE + BI8_STAGE);
+                    tma_load_2d(sA + s * A_STAGE, &tmA, bar(BAR_TMA_FULL + s), kb * BK, mb * BM);
+                    tma_load_2d(sBi8 + s * BI8_STAGE, &tmB, bar(BAR_TMA_FULL + s), kb * BK, nb * BN);
+                }
+            }
+            if (!ok) {  // let the copies already issued land before the CTA exits
+                for (int j = it - 1; j >= 0 && j >= it - STAGES; --j)
+                    mbar_wait_drain(bar(BAR_TMA_FULL + j % STAGES), (j / STAGES) & 1);
+            }
+        } else if (warp == 1 && lane == 0) {
+            // --------------------------------------------------------- MMA
+            int it = 0, g = 0;
+            bool ok = true;
+            uint32_t dcol = 0;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                    const int kc = kb % CHUNK_KB;
+                    if (kc == 0) {
+                        const int buf = g & 1;
+                        if (!mbar_wait(bar(BAR_ACC_EMPTY + buf), ((g >> 1) & 1) ^ 1, abort_flag, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        dcol = (uint32_t)(buf * BN);
+                    }
+                    const int s = it % STAGES;
+                    const int c = it % CSTAGES;
+                    if (!mbar_wait(bar(BAR_TMA_FULL + s), (it / STAGES) & 1, abort_flag, p.err) ||
+                        !mbar_wait(bar(BAR_CONV_FULL + c), (it / CSTAGES) & 1, abort_flag, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = sw128_desc(sA + s * A_STAGE + kk * 32);
+                        const uint64_t bd = sw128_desc(sBh + c * BH_STAGE + kk * 32);
+                        umma_f16(tmem + dcol, ad, bd, (kc > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(bar(BAR_TMA_EMPTY + s));
+                    umma_commit(bar(BAR_CONV_EMPTY + c));
+                    if (kc == CHUNK_KB - 1 || kb == num_kb - 1) {
+                        umma_commit(bar(BAR_ACC_FULL + (g & 1)));
+                        ++g;
+                    }
+                }
+            }
+            // All MMAs issued by this thread have completed once this fires.
+            umma_commit(bar(BAR_DRAIN));
+            mbar_wait_drain(bar(BAR_DRAIN), 0);
+        }
+        __syncwarp();
+        end_barrier();
+        if (warp == 1) {
+            tc_fence_after();
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+        }
+    } else if (warp < 8) {
+        // ----------------------------------------------------------- converters
+        regs_dec<REGS_CONV>();
+        const int ct = threadIdx.x - 128;
+        int it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                const int s = it % STAGES;
+                const int c = it % CSTAGES;
+                const bool got = mbar_wait(bar(BAR_TMA_FULL + s), (it / STAGES) & 1, abort_flag, p.err) &&
+                                 mbar_wait(bar(BAR_CONV_EMPTY + c), ((it / CSTAGES) & 1) ^ 1, abort_flag, p.err);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t *src = smem + OFF_BI8 + s * BI8_STAGE;
+                uint8_t *dst = smem + OFF_BH + c * BH_STAGE;
+#pragma unroll
+                for (int j = 0; j < (BN * BK / 16) / 128; ++j) {
+                    const int L = j * 128 + ct;
+                    const int row = L >> 2;
+                    const int c4 = L & 3;
+                    const uint4 v = *reinterpret_cast<const uint4 *>(src + row * BK + c4 * 16);
+                    uint32_t w[8];
+                    widen4(v.x, w[0], w[1]);
+                    widen4(v.y, w[2], w[3]);
+                    widen4(v.z, w[4], w[5]);
+                    widen4(v.w, w[6], w[7]);
+                    uint8_t *atom = dst + (row >> 3) * 1024 + (row & 7) * 128;
+                    const int sw = row & 7;
+                    *reinterpret_cast<uint4 *>(atom + (((2 * c4) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4 *>(atom + (((2 * c4 + 1) ^ sw) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(bar(BAR_TMA_EMPTY + s));
+                    mbar_arrive(bar(BAR_CONV_FULL + c));
+                }
+            }
+        }
+        end_barrier();
+    } else {
+        // ------------------------------------------------------------- epilogue
+        regs_inc<REGS_EPI>();
+        const int q = warp & 3;          // TMEM lane quarter = rows 32q .. 32q+31
+        const int h = (warp - 8) >> 2;   // column half of the 256-wide tile
+        int g = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            int mb, nb;
+            tile_coords(tile, num_m, num_n, mb, nb);
+            int acc[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i) acc[i] = 0;
+            const int nchunks = (num_kb + CHUNK_KB - 1) / CHUNK_KB;
+            for (int ch = 0; ch < nchunks; ++ch, ++g) {
+                const int buf = g & 1;
+                const bool got = mbar_wait(bar(BAR_ACC_FULL + buf), (g >> 1) & 1, abort_flag, p.err);
+                if (!__all_sync(0xffffffffu, got)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN + h * 128);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t r[16];
+                    tmem_ld16(taddr + 16 * j, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[16 * j + i] += __float2int_rn(__uint_as_float(r[i]));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(BAR_ACC_EMPTY + buf));
+            }
+            if (!ok) break;
+            const int row = mb * BM + 32 * q + lane;
+            const int col0 = nb * BN + h * 128;
+            if (row < p.M) {
+                if constexpr (OUT_S32) {
+                    int32_t *out = static_cast<int32_t *>(p.out) + (int64_t)row * p.N + col0;
+#pragma unroll
+                    for (int i = 0; i < 128; i += 4)
+                        if (col0 + i < p.N)
+                            *reinterpret_cast<int4 *>(out + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+                } else {
+                    uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)row * p.N + col0;
+                    const float sx = __ldg(p.sa + row);
+#pragma unroll
+                    for (int i = 0; i < 128; i += 8) {
+                        if (col0 + i >= p.N) continue;
+                        const float4 w0 = __ldg(reinterpret_cast<const float4 *>(p.sb + col0 + i));
+                        const float4 w1 = __ldg(reinterpret_cast<const float4 *>(p.sb + col0 + i + 4));
+                        const float sw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+                        float y[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) y[k] = __fmul_rn(__int2float_rn(acc[i + k]), __fmul_rn(sx, sw[k]));
+                        if (p.bias != nullptr) {
+                            const uint4 bv = __ldg(reinterpret_cast<const uint4 *>(p.bias + col0 + i));
+                            const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                y[2 * k] = __fadd_rn(y[2 * k], bf16_bits_to_float(bw[k] & 0xffffu));
+                                y[2 * k + 1] = __fadd_rn(y[2 * k + 1], bf16_bits_to_float(bw[k] >> 16));
+                            }
+                        }
+                        *reinterpret_cast<uint4 *>(out + i) = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                                                         pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+                    }
+                }
+            }
+        }
+        end_barrier();
+    }
+}
+
+// ------------------------------------------------------------------- host --
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+cudaError_t get_encoder() {
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode ? cudaSuccess : cudaErrorNotSupported;
+}
+
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, size_t esize, const void *ptr, uint64_t inner, uint64_t outer,
+               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * esize};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    return g_encode(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count_of_current_device() {
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const uint16_t *A, const float *sa, const int8_t *B, const float *sb, const uint16_t *bias,
+                        int64_t M, int64_t N, int64_t K, void *out, bool out_s32, unsigned *err, cudaStream_t st) {
+    if (M == 0 || N == 0) return cudaSuccess;
+    cudaError_t e = get_encoder();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tmA, tmB;
+    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, (uint64_t)K, (uint64_t)M, BK, BM,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, (uint64_t)K, (uint64_t)N, BK, BN,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    GemmArgs p{(int)M, (int)N, (int)K, sa, sb, bias, out, err};
+    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int sms = sm_count_of_current_device();
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    if (out_s32) {
+        e = cudaFuncSetAttribute(gemm_s8_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        gemm_s8_tc_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, p);
+    } else {
+        e = cudaFuncSetAttribute(gemm_s8_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        gemm_s8_tc_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace convrot

@@ -1,0 +1,30 @@
+// Host-side launchers shared between the translation units of libconvrot.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace convrot {
+
+cudaError_t launch_rotq_bf16(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx, int block,
+                             const float *lora_A, const float *lora_B, int rank, float coef, bool out_f16,
+                             void *q, float *scale, cudaStream_t st);
+
+cudaError_t launch_rotq_f64(const double *x, int64_t rows, int64_t K, int block, int8_t *q, float *scale,
+                            cudaStream_t st);
+
+cudaError_t launch_emb_lookup(const int64_t *ids, int64_t n, const int8_t *Eq, const float *scale_e, int64_t V,
+                              int64_t D, int block, uint16_t *out, unsigned *err, cudaStream_t st);
+
+cudaError_t launch_bwd_prep_transpose(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K, int block,
+                                      double *T, cudaStream_t st);
+
+cudaError_t launch_widen_i8(const int8_t *A, int64_t count, uint16_t *out, cudaStream_t st);
+
+// C[M,N] = A[M,K] . B[N,K]^T with A fp16-held integer codes and B int8 codes.
+// out_s32: write the exact int32 accumulator to `out`; otherwise write
+// bf16(float(acc) * (sa[m] * sb[n]) + bias[n]).
+cudaError_t launch_gemm(const uint16_t *A, const float *sa, const int8_t *B, const float *sb, const uint16_t *bias,
+                        int64_t M, int64_t N, int64_t K, void *out, bool out_s32, unsigned *err, cudaStream_t st);
+
+}  // namespace convrot

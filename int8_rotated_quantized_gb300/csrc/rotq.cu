@@ -1,0 +1,477 @@
+// Row-wise kernels of libconvrot: rotate + quantize (weights, activations,
+// gradients, embedding table), quantized embedding lookup, and the one-off
+// preparation of the int8 backward weight.
+//
+// The rotation is the block-diagonal normalised Sylvester-Hadamard matrix
+// R = I (x) H_b / sqrt(b) (MOSS-Image LoRA training guide, section 7.1,
+// ConvRot INT8: the rotation spreads activation outliers over each block
+// before quantization).  It is applied as a fast Walsh-Hadamard transform: every thread
+// holds 8 consecutive elements of a row (one 16-byte load of bf16), does the
+// three in-register butterfly stages, and the remaining log2(b/8) stages run
+// across the b/8 consecutive lanes of a warp with __shfl_xor_sync.  The
+// butterfly (a, c) -> (a + c, a - c) on indices k and k ^ h reproduces the
+// Sylvester ordering H[i][j] = (-1)^popcount(i & j).
+//
+// Quantization is symmetric and per row (sd-scripts PR #2461, ConvRot INT8,
+// Summary: weights and, at run time, activations get one absmax scale per row):
+// with u = H_b x the unnormalised transform, amax_u = max |u| over the row,
+//   scale = amax_u / (127 sqrt(b))   (= max |x R| / 127),
+//   code  = clamp(rne(u * (127 / amax_u)), -127, 127)   (= rne(v / scale)).
+// An all-zero row gets scale 0 and codes 0.
+#include "common.cuh"
+#include "internal.h"
+
+namespace convrot {
+namespace {
+
+constexpr int kMaxThreads = 512;
+
+// ------------------------------------------------------------------ loads --
+
+__device__ __forceinline__ void load8(const uint16_t *p, float (&e)[8]) {
+    uint4 v = __ldcs(reinterpret_cast<const uint4 *>(p));
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        e[2 * i] = __uint_as_float(w[i] << 16);
+        e[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ void load8(const double *p, double (&e)[8]) {
+    const double2 *q = reinterpret_cast<const double2 *>(p);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        double2 v = __ldcs(q + i);
+        e[2 * i] = v.x;
+        e[2 * i + 1] = v.y;
+    }
+}
+
+__device__ __forceinline__ float absv(float v) { return fabsf(v); }
+__device__ __forceinline__ double absv(double v) { return fabs(v); }
+__device__ __forceinline__ float maxv(float a, float b) { return fmaxf(a, b); }
+__device__ __forceinline__ double maxv(double a, double b) { return fmax(a, b); }
+
+template <typename CT>
+__device__ __forceinline__ void zero8(CT (&e)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) e[i] = CT(0);
+}
+
+// ------------------------------------------------------------------- FWHT --
+
+// In-register stages h = 1, 2, 4 on the 8 elements of one lane.
+template <typename CT>
+__device__ __forceinline__ void fwht8(CT (&e)[8]) {
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            if ((i & h) == 0) {
+                CT a = e[i], c = e[i + h];
+                e[i] = a + c;
+                e[i + h] = a - c;
+            }
+        }
+    }
+}
+
+// Cross-lane stages h = 8, 16, ..., b/2 (lane xor masks 1 .. lanes/2).  Every
+// lane of the warp must call this with the same `lanes`.
+template <typename CT>
+__device__ __forceinline__ void fwht_lanes(CT (&e)[8], int lanes, int lane) {
+    for (int m = 1; m < lanes; m <<= 1) {
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            CT p = __shfl_xor_sync(0xffffffffu, e[i], m);
+            e[i] = upper ? (p - e[i]) : (e[i] + p);
+        }
+    }
+}
+
+// ----------------------------------------------------------- code stores --
+
+__device__ __forceinline__ int quant_code(float u, float inv) {
+    int q = __float2int_rn(__fmul_rn(u, inv));
+    return max(-127, min(127, q));
+}
+
+__device__ __forceinline__ void store_codes(int8_t *dst, const int (&q)[8]) {
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        lo |= (uint32_t)(q[i] & 0xff) << (8 * i);
+        hi |= (uint32_t)(q[i + 4] & 0xff) << (8 * i);
+    }
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(lo, hi);
+}
+
+__device__ __forceinline__ void store_codes(__half *dst, const int (&q)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 h = __halves2half2(__int2half_rn(q[2 * i]), __int2half_rn(q[2 * i + 1]));
+        w[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// ------------------------------------------------------ rotate + quantize --
+
+struct RotqArgs {
+    const void *x;
+    int64_t rows, K, ldx;
+    int lanes;          // b / 8
+    int G;              // threads per row group (multiple of 32, <= 512)
+    double scale_coef;  // 1 / (127 sqrt(b))
+    void *q;            // codes, row stride K
+    float *scale;
+    const float *lora_A;  // [rank, K]
+    const float *lora_B;  // [rows, rank]
+    int rank;
+    float coef;  // scale * alpha / rank
+};
+
+// InT: element type of x (uint16_t = bf16 bits, or double).  CT: arithmetic
+// type of the transform.  OutT: int8_t codes or __half-held codes.  S: 8-element
+// slots per thread.  RPT: rows held per thread group at once.  LORA: merge
+// W + coef * B@A (fp32, sequential fma over the rank, rounded to bf16) first.
+template <typename InT, typename CT, typename OutT, int S, int RPT, bool LORA>
+__global__ void __launch_bounds__(kMaxThreads) rotq_rows_kernel(const RotqArgs a) {
+    __shared__ CT red[RPT][kMaxThreads / 32];
+    const int G = a.G;
+    const int g = threadIdx.x / G;
+    const int t = threadIdx.x - g * G;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int groups = blockDim.x / G;
+    const int64_t row0 = ((int64_t)blockIdx.x * groups + g) * RPT;
+    const int64_t chunks = a.K >> 3;
+    const InT *x = static_cast<const InT *>(a.x);
+
+    CT e[RPT][S][8];
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            const int64_t c = (int64_t)s * G + t;
+            const int64_t row = row0 + r;
+            if (c < chunks && row < a.rows)
+                load8(x + row * a.ldx + 8 * c, e[r][s]);
+            else
+                zero8(e[r][s]);
+        }
+    }
+
+    if constexpr (LORA) {
+        // W' = bf16(W + coef * sum_j B[n,j] A[j,k]) with d accumulated by
+        // fused multiply-adds in j order (voxprint-model-forge MOSS page:
+        // merge W + scale * (alpha / rank) * B @ A before quantizing).
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            const int64_t c = (int64_t)s * G + t;
+            if (c >= chunks) continue;
+            float d[RPT][8];
+#pragma unroll
+            for (int r = 0; r < RPT; ++r)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) d[r][i] = 0.f;
+            for (int j = 0; j < a.rank; ++j) {
+                const float4 *ap = reinterpret_cast<const float4 *>(a.lora_A + (int64_t)j * a.K + 8 * c);
+                float4 a0 = __ldg(ap), a1 = __ldg(ap + 1);
+                float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    const int64_t row = min(row0 + r, a.rows - 1);
+                    const float bj = __ldg(a.lora_B + row * a.rank + j);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) d[r][i] = __fmaf_rn(bj, av[i], d[r][i]);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < RPT; ++r)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    e[r][s][i] = __bfloat162float(__float2bfloat16_rn(__fmaf_rn(a.coef, d[r][i], (float)e[r][s][i])));
+        }
+    }
+
+    CT amax[RPT];
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        amax[r] = CT(0);
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            fwht8(e[r][s]);
+            fwht_lanes(e[r][s], a.lanes, lane);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax[r] = maxv(amax[r], absv(e[r][s][i]));
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) amax[r] = maxv(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], m));
+        if (lane == 0) red[r][warp] = amax[r];
+    }
+    __syncthreads();
+    const int wpg = G >> 5;
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        CT m = CT(0);
+        for (int w = 0; w < wpg; ++w) m = maxv(m, red[r][g * wpg + w]);
+        amax[r] = m;
+    }
+
+#pragma unroll
+    for (int r = 0; r < RPT; ++r) {
+        const int64_t row = row0 + r;
+        if (row >= a.rows) continue;
+        // The code decision is taken in fp32 on the fp32-rounded transform.
+        const float amax_f = (float)amax[r];
+        const float inv = amax_f > 0.f ? __fdiv_rn(127.f, amax_f) : 0.f;
+        if (t == 0) a.scale[row] = (float)((double)amax[r] * a.scale_coef);
+        OutT *qrow = static_cast<OutT *>(a.q) + row * a.K;
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            const int64_t c = (int64_t)s * G + t;
+            if (c >= chunks) continue;
+            int q[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) q[i] = quant_code((float)e[r][s][i], inv);
+            store_codes(qrow + 8 * c, q);
+        }
+    }
+}
+
+template <typename InT, typename CT, typename OutT, bool LORA>
+cudaError_t launch_rotq_t(const RotqArgs &base, int64_t rows, int64_t K, cudaStream_t st) {
+    RotqArgs a = base;
+    const int64_t chunks = K / 8;
+    int G, S;
+    if (chunks <= kMaxThreads) {
+        G = (int)((chunks + 31) / 32 * 32);
+        S = 1;
+    } else {
+        G = kMaxThreads;
+        const int64_t need = (chunks + kMaxThreads - 1) / kMaxThreads;
+        S = need <= 2 ? 2 : need <= 4 ? 4 : 8;
+    }
+    a.G = G;
+    const int groups = G >= 256 ? 1 : 256 / G;
+    const int threads = groups * G;
+    auto go = [&](auto kernel, int rpt) -> cudaError_t {
+        const int64_t per_cta = (int64_t)groups * rpt;
+        const int64_t grid = (rows + per_cta - 1) / per_cta;
+        kernel<<<(unsigned)grid, threads, 0, st>>>(a);
+        return cudaGetLastError();
+    };
+    // Rows held per thread group: enough independent 16-byte loads in flight
+    // per SM for HBM, within the register budget of 512-thread CTAs.
+    constexpr bool dbl = sizeof(CT) == 8;
+    constexpr int R1 = LORA ? 4 : (dbl ? 1 : 2);
+    constexpr int R2 = LORA ? 2 : (dbl ? 1 : 2);
+    switch (S) {
+        case 1: return go(rotq_rows_kernel<InT, CT, OutT, 1, R1, LORA>, R1);
+        case 2: return go(rotq_rows_kernel<InT, CT, OutT, 2, R2, LORA>, R2);
+        case 4: return go(rotq_rows_kernel<InT, CT, OutT, 4, 1, LORA>, 1);
+        default: return go(rotq_rows_kernel<InT, CT, OutT, 8, 1, LORA>, 1);
+    }
+}
+
+// ------------------------------------------------------- embedding lookup --
+
+// out[t] = bf16( (scale[id] * Eq[id,:]) R ).  The transform runs on the integer
+// codes (exact in fp32: |sums| <= 127 * 256), then one scaling.
+template <int S>
+__global__ void __launch_bounds__(kMaxThreads) emb_lookup_kernel(const int64_t *ids, int64_t n, const int8_t *Eq,
+                                                                 const float *scale_e, int64_t V, int64_t D,
+                                                                 int lanes, int G, float inv_sqrt_b, uint16_t *out,
+                                                                 unsigned *err) {
+    const int g = threadIdx.x / G;
+    const int t = threadIdx.x - g * G;
+    const int lane = threadIdx.x & 31;
+    const int groups = blockDim.x / G;
+    const int64_t tok = (int64_t)blockIdx.x * groups + g;
+    const int64_t chunks = D >> 3;
+    int64_t id = -1;
+    if (tok < n) id = __ldg(ids + tok);
+    const bool ok = tok < n && id >= 0 && id < V;
+    if (tok < n && !ok && t == 0) atomicOr(err, DEVERR_INDEX);
+    const float s = ok ? __ldg(scale_e + id) : 0.f;
+    float e[S][8];
+#pragma unroll
+    for (int sl = 0; sl < S; ++sl) {
+        const int64_t c = (int64_t)sl * G + t;
+        if (ok && c < chunks) {
+            uint2 v = __ldcs(reinterpret_cast<const uint2 *>(Eq + id * D + 8 * c));
+            uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) e[sl][i] = (float)(int8_t)((w[i >> 2] >> (8 * (i & 3))) & 0xff);
+        } else {
+            zero8(e[sl]);
+        }
+        fwht8(e[sl]);
+        fwht_lanes(e[sl], lanes, lane);
+    }
+    if (tok >= n) return;
+#pragma unroll
+    for (int sl = 0; sl < S; ++sl) {
+        const int64_t c = (int64_t)sl * G + t;
+        if (c >= chunks) continue;
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            w[i] = pack_bf16x2(__fmul_rn(__fmul_rn(e[sl][2 * i], s), inv_sqrt_b),
+                               __fmul_rn(__fmul_rn(e[sl][2 * i + 1], s), inv_sqrt_b));
+        *reinterpret_cast<uint4 *>(out + tok * D + 8 * c) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// ------------------------------------------------------ int8 bwd weight prep --
+
+// T[k][n] = (scale_w[n] * (H_b q_n)[k]) / sqrt(b) in fp64: the dequantized base
+// rotated back to the original basis, written transposed.  A CTA covers 16
+// weight rows and one Hadamard block of b columns.
+constexpr int kPrepRows = 16;
+
+__global__ void __launch_bounds__(256) bwd_prep_transpose_kernel(const int8_t *Wq, const float *scale_w, int64_t N,
+                                                                 int64_t K, int b, double rsqrt_b, double *T) {
+    extern __shared__ double tile[];  // [b][kPrepRows]
+    const int lanes = b >> 3;
+    const int64_t n0 = (int64_t)blockIdx.x * kPrepRows;
+    const int64_t k0 = (int64_t)blockIdx.y * b;
+    const int total = kPrepRows * lanes;
+    const int lane = threadIdx.x & 31;
+    for (int j0 = 0; j0 < total; j0 += blockDim.x) {
+        const int j = j0 + threadIdx.x;
+        if (j0 + (threadIdx.x & ~31) >= total) break;  // warp-uniform
+        const bool valid = j < total;
+        const int rl = valid ? j / lanes : 0;
+        const int cb = valid ? j - rl * lanes : 0;
+        const int64_t n = n0 + rl;
+        double e[8];
+        if (valid && n < N) {
+            uint2 v = __ldg(reinterpret_cast<const uint2 *>(Wq + n * K + k0 + 8 * cb));
+            uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) e[i] = (double)(int8_t)((w[i >> 2] >> (8 * (i & 3))) & 0xff);
+        } else {
+            zero8(e);
+        }
+        fwht8(e);
+        fwht_lanes(e, lanes, lane);
+        const double s = (valid && n < N) ? (double)__ldg(scale_w + n) : 0.0;
+        if (valid) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) tile[(8 * cb + i) * kPrepRows + rl] = (s * e[i]) * rsqrt_b;
+        }
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < b * kPrepRows; idx += blockDim.x) {
+        const int kl = idx / kPrepRows;
+        const int rl = idx - kl * kPrepRows;
+        if (n0 + rl < N) T[(k0 + kl) * N + n0 + rl] = tile[idx];
+    }
+}
+
+__global__ void widen_i8_kernel(const int8_t *A, int64_t count8, __half *out) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count8; i += (int64_t)gridDim.x * blockDim.x) {
+        uint2 v = __ldg(reinterpret_cast<const uint2 *>(A) + i);
+        uint32_t w[2] = {v.x, v.y};
+        int q[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) q[k] = (int8_t)((w[k >> 2] >> (8 * (k & 3))) & 0xff);
+        store_codes(out + 8 * i, q);
+    }
+}
+
+int lanes_of(int block) { return block / 8; }
+
+}  // namespace
+
+cudaError_t launch_rotq_bf16(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx, int block, const float *lora_A,
+                             const float *lora_B, int rank, float coef, bool out_f16, void *q, float *scale,
+                             cudaStream_t st) {
+    if (rows == 0) return cudaSuccess;
+    RotqArgs a{};
+    a.x = x;
+    a.rows = rows;
+    a.K = K;
+    a.ldx = ldx;
+    a.lanes = lanes_of(block);
+    a.scale_coef = 1.0 / (127.0 * sqrt((double)block));
+    a.q = q;
+    a.scale = scale;
+    a.lora_A = lora_A;
+    a.lora_B = lora_B;
+    a.rank = rank;
+    a.coef = coef;
+    if (lora_A != nullptr) return launch_rotq_t<uint16_t, float, int8_t, true>(a, rows, K, st);
+    if (out_f16) return launch_rotq_t<uint16_t, float, __half, false>(a, rows, K, st);
+    return launch_rotq_t<uint16_t, float, int8_t, false>(a, rows, K, st);
+}
+
+cudaError_t launch_rotq_f64(const double *x, int64_t rows, int64_t K, int block, int8_t *q, float *scale,
+                            cudaStream_t st) {
+    if (rows == 0) return cudaSuccess;
+    RotqArgs a{};
+    a.x = x;
+    a.rows = rows;
+    a.K = K;
+    a.ldx = K;
+    a.lanes = lanes_of(block);
+    a.scale_coef = 1.0 / (127.0 * sqrt((double)block));
+    a.q = q;
+    a.scale = scale;
+    return launch_rotq_t<double, double, int8_t, false>(a, rows, K, st);
+}
+
+cudaError_t launch_emb_lookup(const int64_t *ids, int64_t n, const int8_t *Eq, const float *scale_e, int64_t V,
+                              int64_t D, int block, uint16_t *out, unsigned *err, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const int64_t chunks = D / 8;
+    int G, S;
+    if (chunks <= kMaxThreads) {
+        G = (int)((chunks + 31) / 32 * 32);
+        S = 1;
+    } else {
+        G = kMaxThreads;
+        const int64_t need = (chunks + kMaxThreads - 1) / kMaxThreads;
+        S = need <= 2 ? 2 : need <= 4 ? 4 : 8;
+    }
+    const int groups = G >= 256 ? 1 : 256 / G;
+    const int threads = groups * G;
+    const unsigned grid = (unsigned)((n + groups - 1) / groups);
+    const float inv_sqrt_b = (float)(1.0 / sqrt((double)block));
+    const int lanes = lanes_of(block);
+    switch (S) {
+        case 1: emb_lookup_kernel<1><<<grid, threads, 0, st>>>(ids, n, Eq, scale_e, V, D, lanes, G, inv_sqrt_b, out, err); break;
+        case 2: emb_lookup_kernel<2><<<grid, threads, 0, st>>>(ids, n, Eq, scale_e, V, D, lanes, G, inv_sqrt_b, out, err); break;
+        case 4: emb_lookup_kernel<4><<<grid, threads, 0, st>>>(ids, n, Eq, scale_e, V, D, lanes, G, inv_sqrt_b, out, err); break;
+        default: emb_lookup_kernel<8><<<grid, threads, 0, st>>>(ids, n, Eq, scale_e, V, D, lanes, G, inv_sqrt_b, out, err); break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_prep_transpose(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K, int block,
+                                      double *T, cudaStream_t st) {
+    if (N == 0 || K == 0) return cudaSuccess;
+    const size_t smem = sizeof(double) * (size_t)block * kPrepRows;
+    cudaError_t e = cudaFuncSetAttribute(bwd_prep_transpose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(sizeof(double) * 256 * kPrepRows));
+    if (e != cudaSuccess) return e;
+    dim3 grid((unsigned)((N + kPrepRows - 1) / kPrepRows), (unsigned)(K / block));
+    bwd_prep_transpose_kernel<<<grid, 256, smem, st>>>(Wq, scale_w, N, K, block, 1.0 / sqrt((double)block), T);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_widen_i8(const int8_t *A, int64_t count, uint16_t *out, cudaStream_t st) {
+    if (count == 0) return cudaSuccess;
+    const int64_t count8 = count / 8;
+    const int64_t blocks = (count8 + 255) / 256;
+    widen_i8_kernel<<<(unsigned)(blocks < 65535 ? blocks : 65535), 256, 0, st>>>(A, count8,
+                                                                                 reinterpret_cast<__half *>(out));
+    return cudaGetLastError();
+}
+
+}  // namespace convrot

@@ -1,0 +1,98 @@
+"""The C-ABI library builds, loads and exports every declared entry point, and
+host-side argument validation answers without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import int8_rotated_quantized_gb300 as cr
+from int8_rotated_quantized_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "convrot.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return cr.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"CONVROT_API\s+[\w\s\*]+?\b(convrot_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for must in ["convrot_quantize_weight", "convrot_linear_fwd", "convrot_linear_bwd_x", "convrot_embedding_lookup",
+                 "convrot_prepare_bwd_weight", "convrot_gemm_s32", "convrot_get_error", "convrot_status_string"]:
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+
+
+def test_status_strings_and_version(L):
+    assert cr.status_string(0) == "CONVROT_OK"
+    assert cr.status_string(1) == "CONVROT_ERR_INVALID_ARG"
+    assert cr.status_string(4) == "CONVROT_ERR_TIMEOUT"
+    assert cr.status_string(5) == "CONVROT_ERR_INDEX"
+    assert cr.status_string(99) == "CONVROT_ERR_UNKNOWN"
+    assert L.convrot_version() >= 100
+
+
+def test_workspace_sizes(L):
+    assert L.convrot_act_workspace_bytes(4096, 4096) == 4096 * 4096 * 2 + 4096 * 4
+    assert L.convrot_act_workspace_bytes(3, 16) % 256 == 0
+    assert L.convrot_act_workspace_bytes(3, 16) >= 3 * 16 * 2 + 3 * 4
+    assert L.convrot_bwd_weight_workspace_bytes(16384, 4096) == 16384 * 4096 * 8
+    assert L.convrot_gemm_s32_workspace_bytes(64, 256) == 64 * 256 * 2
+    assert L.convrot_act_workspace_bytes(-1, 4) == 0
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # an aligned non-null address; never dereferenced on invalid input
+
+
+@pytest.mark.parametrize("block", [0, 3, 12, 512, 1024])
+def test_bad_block_is_rejected(L, block):
+    rc = L.convrot_quantize_weight(FAKE, 4, 256, 256, block, None, None, 0, 1.0, 1.0, FAKE, FAKE, None)
+    assert rc == cr.ERR_INVALID_ARG
+
+
+def test_bad_shapes_are_rejected(L):
+    # K not a multiple of the block, K not a multiple of 16, ldw < K, row too long
+    assert L.convrot_quantize_weight(FAKE, 4, 96, 96, 64, None, None, 0, 1.0, 1.0, FAKE, FAKE, None) == 1
+    assert L.convrot_quantize_weight(FAKE, 4, 40, 40, 8, None, None, 0, 1.0, 1.0, FAKE, FAKE, None) == 1
+    assert L.convrot_quantize_weight(FAKE, 4, 256, 128, 32, None, None, 0, 1.0, 1.0, FAKE, FAKE, None) == 1
+    assert L.convrot_quantize_weight(FAKE, 4, 65536, 65536, 128, None, None, 0, 1.0, 1.0, FAKE, FAKE, None) == 1
+    # LoRA pair incomplete, rank out of range
+    assert L.convrot_quantize_weight(FAKE, 4, 256, 256, 32, FAKE, None, 4, 1.0, 1.0, FAKE, FAKE, None) == 1
+    assert L.convrot_quantize_weight(FAKE, 4, 256, 256, 32, FAKE, FAKE, 0, 1.0, 1.0, FAKE, FAKE, None) == 1
+    # GEMM: N not a multiple of 16, K not a multiple of 16
+    assert L.convrot_gemm_dequant(FAKE, FAKE, 8, 256, FAKE, FAKE, 24, None, FAKE, None) == 1
+    assert L.convrot_gemm_dequant(FAKE, FAKE, 8, 200, FAKE, FAKE, 32, None, FAKE, None) == 1
+    # forward: workspace too small or misaligned
+    need = L.convrot_act_workspace_bytes(8, 256)
+    assert L.convrot_linear_fwd(FAKE, 8, 256, FAKE, FAKE, 32, 32, None, FAKE, FAKE, need - 1, None) == 1
+    assert L.convrot_linear_fwd(FAKE, 8, 256, FAKE, FAKE, 32, 32, None, FAKE, ctypes.c_void_p((1 << 20) + 16),
+                                need, None) == 1
+    # s32 entry: K beyond the int32-safe limit
+    assert L.convrot_gemm_s32(FAKE, FAKE, 1, 16, 1 << 18, FAKE, FAKE, 1 << 30, None) == 1
+
+
+def test_null_and_misaligned_pointers_are_rejected(L):
+    assert L.convrot_quantize_activation(None, 4, 256, 256, 32, FAKE, FAKE, None) == 1
+    assert L.convrot_quantize_activation(ctypes.c_void_p((1 << 20) + 2), 4, 256, 256, 32, FAKE, FAKE, None) == 1
+    assert L.convrot_embedding_lookup(None, 4, FAKE, FAKE, 10, 256, 128, FAKE, None) == 1
+    assert L.convrot_prepare_bwd_weight(FAKE, FAKE, 256, 256, 32, FAKE, FAKE, None, 1 << 30, None) == 1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(cr, "_lib", None)
+    monkeypatch.setattr(cr, "library_path", lambda: str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        cr.lib()

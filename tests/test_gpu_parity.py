@@ -1,0 +1,270 @@
+"""GPU parity: the CUDA library (called through its C ABI binding) against the
+CPU oracle on the same seeded inputs.  Sizes span several 128x256 GEMM tiles,
+K chunks of 1024 and ragged tails in M, N and K."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import (REL_FRO_BF16, REL_FRO_ORACLE, bits_of, check_codes, check_scales, codes_of, f64, rel_fro,
+                     torch_bf16)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import int8_rotated_quantized_gb300 as cr  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    cr._build.build()
+    cr.lib()
+    assert cr.convrot_get_error() == cr.OK
+
+
+def _i8(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int8)).cuda()
+
+
+def _f32(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+
+def _rand_codes(rng, shape):
+    return rng.integers(-127, 128, size=shape, dtype=np.int8)
+
+
+# ------------------------------------------------------------------ GEMM (int32)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 16, 16), (128, 256, 64), (129, 272, 1040), (300, 528, 2064), (64, 128, 256),
+                                   (17, 48, 4096)])
+def test_gemm_s32_bit_exact(M, N, K):
+    rng = np.random.default_rng(M * 7 + N * 3 + K)
+    A = _rand_codes(rng, (M, K))
+    B = _rand_codes(rng, (N, K))
+    C = cr.convrot_gemm_s32(_i8(A), _i8(B))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(C.cpu().numpy(), oracle.gemm_s32(A, B))
+    assert cr.convrot_get_error() == cr.OK
+
+
+@pytest.mark.parametrize("K", [1024, 4096, 16384])
+def test_gemm_s32_extremes_cross_the_fp32_exact_range(K):
+    """All-127 operands drive every partial sum past 2^24 for K > 1040."""
+    M, N = 130, 272
+    A = np.full((M, K), 127, dtype=np.int8)
+    B = np.full((N, K), 127, dtype=np.int8)
+    A[1::2] = -127
+    B[:, ::3] *= -1
+    C = cr.convrot_gemm_s32(_i8(A), _i8(B)).cpu().numpy()
+    np.testing.assert_array_equal(C, oracle.gemm_s32(A, B))
+    assert abs(int(C[0, 1])) > 1 << 24 or K <= 1040
+
+
+def test_gemm_s32_random_signs_long_k():
+    rng = np.random.default_rng(5)
+    M, N, K = 140, 260 - 4, 16384 + 64
+    A = (rng.integers(0, 2, size=(M, K)) * 254 - 127).astype(np.int8)
+    B = (rng.integers(0, 2, size=(N, K)) * 254 - 127).astype(np.int8)
+    C = cr.convrot_gemm_s32(_i8(A), _i8(B)).cpu().numpy()
+    np.testing.assert_array_equal(C, oracle.gemm_s32(A, B))
+
+
+# ------------------------------------------------------------------ quantizers
+
+
+@pytest.mark.parametrize("block", [8, 16, 32, 64, 128, 256])
+@pytest.mark.parametrize("K", [512, 4096])
+def test_quantize_weight_parity(block, K):
+    N = 70
+    W = synth.normal_bf16(1, synth.STREAM_W, N, K, 0.02)
+    W[5] = 0  # an all-zero row
+    q_ref, s_ref = oracle.quantize_weight(W, block)
+    Wq, sw = cr.convrot_quantize_weight(torch_bf16(W), block)
+    check_codes(codes_of(Wq), q_ref, f64(W), block)
+    check_scales(sw.cpu().numpy(), s_ref)
+    assert float(sw[5]) == 0.0 and int(Wq[5].abs().max()) == 0
+
+
+@pytest.mark.parametrize("K", [12288, 16384, 32768])
+def test_quantize_long_rows_parity(K):
+    """Rows longer than one CTA pass (several 8-element slots per thread, partly masked)."""
+    M = 9
+    x = synth.activations_bf16(2, M, K, 41, 30.0)
+    q_ref, s_ref = oracle.quantize_rows_bf16(x, 128)
+    xq, sx = cr.convrot_quantize_activation(torch_bf16(x), 128)
+    check_codes(codes_of(xq), q_ref, f64(x), 128)
+    check_scales(sx.cpu().numpy(), s_ref)
+
+
+@pytest.mark.parametrize("block", [32, 128])
+def test_quantize_activation_parity(block):
+    M, K = 333, 1024
+    x = synth.activations_bf16(3, M, K, 10, 30.0)
+    q_ref, s_ref = oracle.quantize_rows_bf16(x, block)
+    xq, sx = cr.convrot_quantize_activation(torch_bf16(x), block)
+    assert xq.dtype == torch.float16
+    check_codes(codes_of(xq), q_ref, f64(x), block)
+    check_scales(sx.cpu().numpy(), s_ref)
+
+
+def test_quantize_weight_with_row_stride():
+    N, K, ld = 40, 256, 384
+    Wfull = synth.normal_bf16(4, synth.STREAM_W, N, ld, 0.02)
+    q_ref, s_ref = oracle.quantize_weight(np.ascontiguousarray(Wfull[:, :K]), 32)
+    t = torch_bf16(Wfull)
+    Wq = torch.empty((N, K), dtype=torch.int8, device="cuda")
+    sw = torch.empty((N,), dtype=torch.float32, device="cuda")
+    rc = cr.lib().convrot_quantize_weight(cr._ptr(t), N, K, ld, 32, None, None, 0, 1.0, 1.0, cr._ptr(Wq), cr._ptr(sw),
+                                          cr._stream(None))
+    assert rc == cr.OK
+    check_codes(codes_of(Wq), q_ref, f64(Wfull[:, :K]), 32)
+    check_scales(sw.cpu().numpy(), s_ref)
+
+
+@pytest.mark.parametrize("N,K,rank", [(96, 512, 16), (50, 4096, 16), (33, 1024, 3)])
+def test_quantize_weight_lora_merge_parity(N, K, rank):
+    W = synth.normal_bf16(6, synth.STREAM_W, N, K, 0.02)
+    A, B = synth.lora_pair(6, N, K, rank, 0.01)
+    q_ref, s_ref = oracle.quantize_weight(W, 128 if K % 128 == 0 else 32, A, B, 16.0, 1.0)
+    block = 128 if K % 128 == 0 else 32
+    Wq, sw = cr.convrot_quantize_weight(torch_bf16(W), block, _f32(A), _f32(B), 16.0, 1.0)
+    merged = oracle.lora_merge(W, A, B, 16.0, 1.0)
+    check_codes(codes_of(Wq), q_ref, f64(merged), block)
+    check_scales(sw.cpu().numpy(), s_ref)
+    # scale = 0 reproduces the unmerged path bit for bit
+    Wq0, sw0 = cr.convrot_quantize_weight(torch_bf16(W), block, _f32(A), _f32(B), 16.0, 0.0)
+    Wqp, swp = cr.convrot_quantize_weight(torch_bf16(W), block)
+    assert torch.equal(Wq0, Wqp) and torch.equal(sw0, swp)
+
+
+# ------------------------------------------------------------------ fused GEMM + epilogue
+
+
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_gemm_dequant_on_oracle_codes(with_bias):
+    M, K, N, b = 300, 2048, 528, 128
+    x = synth.activations_bf16(7, M, K, 20, 30.0)
+    W = synth.normal_bf16(7, synth.STREAM_W, N, K, 0.02)
+    wq, sw = oracle.quantize_weight(W, b)
+    xq, sx = oracle.quantize_rows_bf16(x, b)
+    bias = synth.normal_bf16(7, 9, 1, N, 0.5)[0] if with_bias else None
+    y_ref = oracle.dequant(oracle.gemm_s32(xq, wq), sx, sw, bias)
+    y = cr.convrot_gemm_dequant(torch.from_numpy(xq.astype(np.float16)).cuda(), _f32(sx), _i8(wq), _f32(sw),
+                                None if bias is None else torch_bf16(bias))
+    yb = bits_of(y)
+    assert rel_fro(f64(yb), f64(y_ref)) <= REL_FRO_ORACLE
+    # the epilogue differs from the fp64 oracle by at most one bf16 rounding step
+    ulps = np.abs(yb.astype(np.int32) - y_ref.astype(np.int32))
+    same_sign = (yb >> 15) == (y_ref >> 15)
+    assert np.all(ulps[same_sign] <= 1)
+    assert np.mean(yb == y_ref) > 0.99
+
+
+def test_linear_fwd_tiny_workload():
+    wl = synth.WORKLOADS["tiny"]
+    M, K, N, b = wl["M"], wl["K"], wl["N"], wl["block"]
+    x = synth.activations_bf16(0, M, K, wl["x_outliers"], wl["x_factor"])
+    W = synth.normal_bf16(0, synth.STREAM_W, N, K, wl["w_sigma"])
+    wq_ref, sw_ref = oracle.quantize_weight(W, b)
+    y_ref, xq_ref, sx_ref = oracle.linear_fwd(x, wq_ref, sw_ref, b)
+    Wq, sw = cr.convrot_quantize_weight(torch_bf16(W), b)
+    check_codes(codes_of(Wq), wq_ref, f64(W), b)
+    y = cr.convrot_linear_fwd(torch_bf16(x), Wq, sw, b)
+    yb = f64(bits_of(y))
+    assert rel_fro(yb, f64(y_ref)) <= REL_FRO_ORACLE
+    assert rel_fro(yb, f64(x) @ f64(W).T) <= REL_FRO_BF16
+    assert cr.convrot_get_error() == cr.OK
+
+
+def test_linear_fwd_ragged_multi_tile():
+    M, K, N, b = 259, 1152, 400, 64
+    x = synth.activations_bf16(8, M, K, 12, 30.0)
+    W = synth.normal_bf16(8, synth.STREAM_W, N, K, 0.02)
+    bias = synth.normal_bf16(8, 9, 1, N, 0.1)[0]
+    wq_ref, sw_ref = oracle.quantize_weight(W, b)
+    y_ref, _, _ = oracle.linear_fwd(x, wq_ref, sw_ref, b, bias)
+    Wq, sw = cr.convrot_quantize_weight(torch_bf16(W), b)
+    y = cr.convrot_linear_fwd(torch_bf16(x), Wq, sw, b, bias=torch_bf16(bias))
+    yb = f64(bits_of(y))
+    assert rel_fro(yb, f64(y_ref)) <= REL_FRO_ORACLE
+    assert rel_fro(yb, f64(x) @ f64(W).T + f64(bias)) <= REL_FRO_BF16
+
+
+# ------------------------------------------------------------------ backward
+
+
+@pytest.mark.parametrize("block", [32, 128])
+def test_bwd_prep_and_grad_x_parity(block):
+    M, K, N = 150, 256, 768
+    W = synth.normal_bf16(9, synth.STREAM_W, N, K, 0.02)
+    wq, sw = oracle.quantize_weight(W, block)
+    wtq_ref, swt_ref = oracle.prepare_bwd_weight(wq, sw, block)
+    WtQ, swt = cr.convrot_prepare_bwd_weight(_i8(wq), _f32(sw), block)
+    w_eff_t = ((sw[:, None].astype(np.float64) * wq) @ np.kron(np.eye(K // block), oracle.hadamard(block) /
+                                                               math.sqrt(block))).T
+    check_codes(codes_of(WtQ), wtq_ref, w_eff_t, block, "bwd weight codes")
+    check_scales(swt.cpu().numpy(), swt_ref, "bwd weight scales")
+    dY = synth.normal_bf16(9, synth.STREAM_DY, M, N, 1e-3)
+    dX_ref, _, _ = oracle.linear_bwd_x(dY, wtq_ref, swt_ref, block)
+    dX = cr.convrot_linear_bwd_x(torch_bf16(dY), WtQ, swt, block)
+    d = f64(bits_of(dX))
+    assert rel_fro(d, f64(dX_ref)) <= REL_FRO_ORACLE
+    assert rel_fro(d, f64(dY) @ f64(W)) <= REL_FRO_BF16
+
+
+# ------------------------------------------------------------------ embedding
+
+
+def test_embedding_lookup_parity_and_bad_ids():
+    V, D, b = 1000, 512, 128
+    table = synth.normal_bf16(10, synth.STREAM_TABLE, V, D, 0.02)
+    eq_ref, se_ref = oracle.quantize_rows_bf16(table, b)
+    Eq, se = cr.convrot_quantize_weight(torch_bf16(table), b)
+    check_codes(codes_of(Eq), eq_ref, f64(table), b)
+    ids = synth.token_ids(10, 300, V)
+    out = cr.convrot_embedding_lookup(torch.from_numpy(ids).cuda(), _i8(eq_ref), _f32(se_ref), b)
+    out_ref, bad = oracle.embedding_lookup(ids, eq_ref, se_ref, b)
+    assert bad == 0
+    ob = bits_of(out)
+    assert rel_fro(f64(ob), f64(out_ref)) <= REL_FRO_ORACLE
+    assert np.mean(ob == out_ref) > 0.99
+    assert rel_fro(f64(ob), f64(table[ids])) < 2e-2
+    assert cr.convrot_get_error() == cr.OK
+    ids[[4, 9]] = [V, -3]
+    out = cr.convrot_embedding_lookup(torch.from_numpy(ids).cuda(), _i8(eq_ref), _f32(se_ref), b)
+    assert cr.convrot_get_error() == cr.ERR_INDEX
+    assert cr.convrot_get_error() == cr.OK  # cleared
+    ob = bits_of(out)
+    assert np.all(ob[4] == 0) and np.all(ob[9] == 0)
+    good = [i for i in range(300) if i not in (4, 9)]
+    assert rel_fro(f64(ob[good]), f64(out_ref[good])) <= REL_FRO_ORACLE
+
+
+# ------------------------------------------------------------------ edge cases
+
+
+def test_empty_problems_are_no_ops():
+    W = torch.zeros((0, 256), dtype=torch.bfloat16, device="cuda")
+    Wq, sw = cr.convrot_quantize_weight(W, 32)
+    assert Wq.shape == (0, 256)
+    x = torch.zeros((0, 256), dtype=torch.bfloat16, device="cuda")
+    Wq2, sw2 = cr.convrot_quantize_weight(torch.ones((32, 256), dtype=torch.bfloat16, device="cuda"), 32)
+    y = cr.convrot_linear_fwd(x, Wq2, sw2, 32)
+    assert y.shape == (0, 32)
+    out = cr.convrot_embedding_lookup(torch.zeros((0,), dtype=torch.int64, device="cuda"), Wq2, sw2, 32)
+    assert out.shape == (0, 256)
+    assert cr.convrot_get_error() == cr.OK
+
+
+def test_argument_errors_raise():
+    x = torch.ones((4, 96), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(cr.ConvRotError):
+        cr.convrot_quantize_activation(x, 64)  # 96 is not a multiple of 64
+    with pytest.raises(TypeError):
+        cr.convrot_quantize_activation(x.float(), 32)
