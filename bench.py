@@ -1,0 +1,469 @@
+#!/usr/bin/env python
+"""Benchmark of the ConvRot INT8 layer on GB300.
+
+One step = the per-step hot path of a packed 20k-token training step of one
+frozen ConvRot INT8 linear layer (x bf16 [20480, 4096], W [16384, 4096],
+block 128): online rotation + per-row quantization of x, the fused int8 GEMM
+with dequantization epilogue, rotation + quantization of dY along N, and the
+int8 grad_x GEMM.  Weight quantization (with and without a LoRA merge), the
+int8 backward weight preparation, the embedding-table quantization and the
+quantized embedding lookup are load-time or separate kernels; each is timed
+on its own workload and reported under "rows".
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "ConvRot int8 linear TOPS & quantizer GB/s (1×GB300, % of roofline)"
+WORKLOAD = ("train20k: packed 20k-token training step of one ConvRot INT8 linear layer, x bf16 [20480,4096] "
+            "N(0,1) with 41 outlier channels x30, W bf16 [16384,4096] N(0,0.02), dY bf16 [20480,16384] N(0,1e-3), "
+            "Hadamard block 128; per step: rotate+quantize x, int8 GEMM + dequant -> y, rotate+quantize dY, "
+            "int8 grad_x GEMM -> dX")
+L2_FLUSH_BYTES = 256 << 20
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+# ---------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.file = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [ln.strip().split(",") for ln in self.file.read().splitlines() if ln.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = max(mx, float(r[2]))
+                for name, val in zip(names, r[5:9]):
+                    if val.strip().lower() in ("active", "0x1", "1"):
+                        reasons.add(name)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ our kernels ----
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import int8_rotated_quantized_gb300 as cr
+    import synth
+    import synth.gpu as sg
+    from int8_rotated_quantized_gb300 import _build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    if rank == 0:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    cr.lib()
+    pk = peaks()
+
+    wl = synth.WORKLOADS["train20k"]
+    M, K, N, b = wl["M"], wl["K"], wl["N"], wl["block"]
+    # weak scaling: every rank owns its own 20480-token batch (rows row0 .. row0+M of one tall batch)
+    row0 = rank * M
+    x = sg.activations_bf16(0, M, K, wl["x_outliers"], wl["x_factor"], dev, row0=row0)
+    W = sg.normal_bf16(0, synth.STREAM_W, N, K, wl["w_sigma"], dev)
+    dY = sg.normal_bf16(0, synth.STREAM_DY, M, N, wl["dy_sigma"], dev, row0=row0)
+    stream = torch.cuda.current_stream()
+
+    # load-time work (not in the step): quantize W, prepare the int8 backward weight
+    Wq, sw = cr.convrot_quantize_weight(W, b)
+    WtQ, swt = cr.convrot_prepare_bwd_weight(Wq, sw, b)
+    xq = torch.empty((M, K), dtype=torch.float16, device=dev)
+    sx = torch.empty((M,), dtype=torch.float32, device=dev)
+    dyq = torch.empty((M, N), dtype=torch.float16, device=dev)
+    sdy = torch.empty((M,), dtype=torch.float32, device=dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    dX = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+    assert cr.convrot_get_error() == cr.OK
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        cr.convrot_quantize_activation(x, b, xq, sx)
+        if ev:
+            ev[1].record(stream)
+        cr.convrot_gemm_dequant(xq, sx, Wq, sw, None, y)
+        if ev:
+            ev[2].record(stream)
+        cr.convrot_quantize_activation(dY, b, dyq, sdy)
+        if ev:
+            ev[3].record(stream)
+        cr.convrot_gemm_dequant(dyq, sdy, WtQ, swt, None, dX)
+        if ev:
+            ev[4].record(stream)
+
+    launches_per_step = 4
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert cr.convrot_get_error() == cr.OK
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(local) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()  # L2 flush between steps, outside the events
+        step(evs[i])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop() if sampler else None
+
+    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
+    k1x = [e[0].elapsed_time(e[1]) for e in evs]
+    gf = [e[1].elapsed_time(e[2]) for e in evs]
+    k1d = [e[2].elapsed_time(e[3]) for e in evs]
+    gb = [e[3].elapsed_time(e[4]) for e in evs]
+    total_ms = sum(step_ms)
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    assert cr.convrot_get_error() == cr.OK
+
+    ops_step = 2.0 * 2.0 * M * N * K           # fwd + grad_x GEMMs
+    value = world * ops_step * args.steps / (total_ms * 1e-3) / 1e12
+    gemm_ms = statistics.mean(gf + gb)
+    gemm_tflops = 2.0 * M * N * K / (gemm_ms * 1e-3) / 1e12
+
+    result = None
+    if rank == 0:
+        rows = measure_rows(cr, synth, sg, torch, dev, flush, pk) if not args.no_rows else {}
+        rows["a3_x_rotate_quant"] = _hbm_row(M * K * 2 + M * K * 2 + M * 4, statistics.median(k1x), pk,
+                                             "C4 x [20480,4096] bf16 -> fp16-held codes + fp32 scales")
+        rows["a6_dy_rotate_quant"] = _hbm_row(M * N * 2 + M * N * 2 + M * 4, statistics.median(k1d), pk,
+                                              "C4 dY [20480,16384] bf16 -> fp16-held codes + fp32 scales")
+        rows["a4a5_fwd_gemm"] = _tc_row(2.0 * M * N * K, statistics.median(gf), pk, "C4 20480x16384x4096")
+        rows["a6_bwd_gemm"] = _tc_row(2.0 * M * N * K, statistics.median(gb), pk, "C4 20480x4096x16384")
+        e2e = measure_e2e(cr, torch, dev, x, dY, Wq, sw, WtQ, swt, b, ops_step)
+        cpu = None
+        if world == 1 and not args.no_cpu:
+            cpu = cpu_baseline(args.cpu_rows, M, K, N, b, wl)
+        result = {
+            "metric": METRIC,
+            "value": round(value, 3),
+            "unit": "TOPS",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(total_ms / args.steps, 4),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "s8",
+            "data": "synthetic (seeded splitmix64 + Box-Muller, generated on the device)",
+            "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "block": b,
+                       "tokens_per_gpu": M, "l2": "flushed between steps (256 MiB write, outside the events)",
+                       "parallelism": f"replicas x{world} (rows sharded, no collective)"},
+            "roofline": {
+                "kernel": "gemm_s8_tc_kernel (fwd and grad_x launches)",
+                "bound": "tensor",
+                "achieved": round(gemm_tflops, 1),
+                "peak": pk["bf16"],
+                "unit": "TFLOP/s",
+                "frac": round(gemm_tflops / pk["bf16"], 4),
+                "peak_note": f"{pk['source']} dense bf16 burst (the kind::f16 MMA that carries the int8 codes runs at the "
+                             "bf16/fp16 rate; tcgen05 kind::i8 does not exist on sm_103a)",
+                "traffic": None,
+            },
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "wall_s_timed_region": round(t_wall, 4),
+            "rows": rows,
+        }
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+def _hbm_row(nbytes, ms, pk, what):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"what": what, "ms": round(ms, 4), "algorithmic_bytes": int(nbytes), "GB/s": round(gbs, 1),
+            "peak_GB/s": pk["hbm"], "frac": round(gbs / pk["hbm"], 4)}
+
+
+def _tc_row(ops, ms, pk, what):
+    tops = ops / (ms * 1e-3) / 1e12
+    return {"what": what, "ms": round(ms, 4), "ops": ops, "TOPS": round(tops, 1), "peak_TFLOP/s": pk["bf16"],
+            "frac": round(tops / pk["bf16"], 4)}
+
+
+def _time(torch, fn, flush, reps, pre=None):
+    """Median device time (ms) of fn() over reps, each after an L2 flush."""
+    stream = torch.cuda.current_stream()
+    out = []
+    for i in range(reps + 2):
+        flush.zero_()
+        if pre:
+            pre(i)
+        a = torch.cuda.Event(enable_timing=True)
+        z = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn(i)
+        z.record(stream)
+        torch.cuda.synchronize()
+        if i >= 2:
+            out.append(a.elapsed_time(z))
+    return statistics.median(out)
+
+
+def measure_rows(cr, synth, sg, torch, dev, flush, pk):
+    rows = {}
+    reps = 10
+    # a2: weight rotate + quantize, C4 weight
+    wl = synth.WORKLOADS["train20k"]
+    N, K, b = wl["N"], wl["K"], wl["block"]
+    W = sg.normal_bf16(0, synth.STREAM_W, N, K, wl["w_sigma"], dev)
+    Wq = torch.empty((N, K), dtype=torch.int8, device=dev)
+    sw = torch.empty((N,), dtype=torch.float32, device=dev)
+    ms = _time(torch, lambda i: cr.convrot_quantize_weight(W, b, Wq=Wq, scale_w=sw), flush, reps)
+    rows["a2_weight_rotate_quant"] = _hbm_row(N * K * 2 + N * K + N * 4, ms, pk, "C4 W [16384,4096] bf16 -> int8")
+    # a6 prep (one-off): int8 backward weight
+    WtQ = torch.empty((K, N), dtype=torch.int8, device=dev)
+    swt = torch.empty((K,), dtype=torch.float32, device=dev)
+    ws = torch.empty(cr.convrot_bwd_weight_workspace_bytes(N, K), dtype=torch.uint8, device=dev)
+    ms = _time(torch, lambda i: cr.convrot_prepare_bwd_weight(Wq, sw, b, WtQ, swt, ws), flush, 3)
+    rows["a6_prep_bwd_weight"] = _hbm_row(N * K + N * 4 + K * N + K * 4, ms, pk,
+                                          "C4 Wq [16384,4096] -> WtQ [4096,16384] (one-off, via an fp64 workspace)")
+    del W, Wq, WtQ, ws
+    # a1 + a2: LoRA merge fused into the weight quantizer, C3 qkv weight
+    wl3 = synth.WORKLOADS["qkv_lora"]
+    N3, K3, r = wl3["N"], wl3["K"], wl3["lora_rank"]
+    W3 = sg.normal_bf16(0, synth.STREAM_W, N3, K3, wl3["w_sigma"], dev)
+    A, B = sg.lora_pair(0, N3, K3, r, wl3["lora_sigma"], dev)
+    Wq3 = torch.empty((N3, K3), dtype=torch.int8, device=dev)
+    sw3 = torch.empty((N3,), dtype=torch.float32, device=dev)
+    ms = _time(torch, lambda i: cr.convrot_quantize_weight(W3, b, A, B, wl3["lora_alpha"], wl3["lora_scale"], Wq3,
+                                                           sw3), flush, reps)
+    rows["a1a2_lora_merge_quant"] = _hbm_row(N3 * K3 * 2 + N3 * K3 + N3 * 4 + r * K3 * 4 + N3 * r * 4, ms, pk,
+                                             "C3 W [12288,4096] + LoRA r16 -> int8")
+    del W3, Wq3, A, B
+    # a7: embedding table quantization (row-chunked: 8 slabs of 31000 rows)
+    wl5 = synth.WORKLOADS["embed"]
+    V, D = wl5["V"], wl5["D"]
+    T = sg.normal_bf16(0, synth.STREAM_TABLE, V, D, wl5["table_sigma"], dev)
+    Eq = torch.empty((V, D), dtype=torch.int8, device=dev)
+    se = torch.empty((V,), dtype=torch.float32, device=dev)
+    slab = 31000
+
+    def quant_table(i):
+        for r0 in range(0, V, slab):
+            r1 = min(V, r0 + slab)
+            cr.convrot_quantize_weight(T[r0:r1], b, Wq=Eq[r0:r1], scale_w=se[r0:r1])
+
+    ms = _time(torch, quant_table, flush, 5)
+    rows["a7_table_rotate_quant"] = _hbm_row(V * D * 2 + V * D + V * 4, ms, pk,
+                                             "C5 table [248000,4096] bf16 -> int8, 8 row slabs")
+    del T
+    # a8: lookup of 8192 ids, rotating over 8 id sets
+    n_ids = wl5["n_ids"]
+    id_sets = [sg.token_ids(0, n_ids, V, dev, set_index=s) for s in range(wl5["id_sets"])]
+    out = torch.empty((n_ids, D), dtype=torch.bfloat16, device=dev)
+    ms = _time(torch, lambda i: cr.convrot_embedding_lookup(id_sets[i % len(id_sets)], Eq, se, b, out), flush, 16)
+    rows["a8_embedding_lookup"] = _hbm_row(n_ids * 8 + n_ids * D + n_ids * 4 + n_ids * D * 2, ms, pk,
+                                           "C5 8192 ids -> bf16 [8192,4096]")
+    assert cr.convrot_get_error() == cr.OK
+    return rows
+
+
+def measure_e2e(cr, torch, dev, x, dY, Wq, sw, WtQ, swt, b, ops_step, steps=3):
+    """The step through the public calls with host buffers: H2D of x and dY from
+    pinned memory, forward and grad_x, D2H of y and dX, all inside the timed region."""
+    M, K = x.shape
+    N = dY.shape[1]
+    xh = x.cpu().pin_memory()
+    dyh = dY.cpu().pin_memory()
+    yh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    dxh = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(x)
+    dyd = torch.empty_like(dY)
+    yd = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    dxd = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(cr.convrot_act_workspace_bytes(M, K), cr.convrot_act_workspace_bytes(M, N)),
+                     dtype=torch.uint8, device=dev)
+
+    def one():
+        xd.copy_(xh, non_blocking=True)
+        dyd.copy_(dyh, non_blocking=True)
+        cr.convrot_linear_fwd(xd, Wq, sw, b, y=yd, workspace=ws)
+        cr.convrot_linear_bwd_x(dyd, WtQ, swt, b, dX=dxd, workspace=ws)
+        yh.copy_(yd, non_blocking=True)
+        dxh.copy_(dxd, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": round(ops_step / dt / 1e12, 3), "unit": "TOPS", "ms_per_step": round(dt * 1e3, 3),
+            "h2d_bytes_per_step": int(x.numel() * 2 + dY.numel() * 2),
+            "d2h_bytes_per_step": int(M * N * 2 + M * K * 2)}
+
+
+# ---------------------------------------------------------------- oracle ----
+
+def _oracle_setup(M, K, N, b, wl, rows):
+    import numpy as np  # noqa: F401
+
+    import oracle
+    import synth
+    oracle.build()
+    W = synth.normal_bf16(0, synth.STREAM_W, N, K, wl["w_sigma"])
+    wq, sw = oracle.quantize_weight(W, b)
+    wtq, swt = oracle.prepare_bwd_weight(wq, sw, b)
+    x = synth.activations_bf16(0, rows, K, wl["x_outliers"], wl["x_factor"])
+    dy = synth.normal_bf16(0, synth.STREAM_DY, rows, N, wl["dy_sigma"])
+    return oracle, (wq, sw, wtq, swt, x, dy)
+
+
+def _oracle_step(oracle, data, b):
+    wq, sw, wtq, swt, x, dy = data
+    oracle.linear_fwd(x, wq, sw, b)
+    oracle.linear_bwd_x(dy, wtq, swt, b)
+
+
+def cpu_baseline(rows, M, K, N, b, wl):
+    oracle, data = _oracle_setup(M, K, N, b, wl, rows)
+    t0 = time.perf_counter()
+    _oracle_step(oracle, data, b)
+    dt = time.perf_counter() - t0
+    return {"value": round(2.0 * 2.0 * rows * N * K / dt / 1e12, 6), "unit": "TOPS", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"{rows} of the {M} token rows of one step (fwd + grad_x), weights prepared outside the timing; "
+                      f"{dt:.2f} s"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import synth
+    wl = synth.WORKLOADS["train20k"]
+    M, K, N, b = wl["M"], wl["K"], wl["N"], wl["block"]
+    oracle, data = _oracle_setup(M, K, N, b, wl, args.ref_rows)
+    for _ in range(args.warmup):
+        _oracle_step(oracle, data, b)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(oracle, data, b)
+    dt = time.perf_counter() - t0
+    value = 2.0 * 2.0 * args.ref_rows * N * K * args.steps / dt / 1e12
+    cores = oracle.num_threads()
+    sample = (f"each step: {args.ref_rows} of the {M} token rows of the training step (fwd + grad_x through the "
+              f"oracle), weights prepared once outside the timing")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "s8",
+        "data": "synthetic (seeded splitmix64 + Box-Muller)",
+        "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "block": b, "rows_per_step": args.ref_rows},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TOPS", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["convrot", "reference"], default="convrot")
+    ap.add_argument("--cpu-rows", type=int, default=512, help="token rows in the CPU-oracle sample")
+    ap.add_argument("--ref-rows", type=int, default=64, help="token rows per step of --impl reference")
+    ap.add_argument("--no-rows", action="store_true", help="skip the per-kernel rows")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    res = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()
