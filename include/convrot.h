@@ -133,6 +133,35 @@ CONVROT_API int convrot_linear_fwd(const uint16_t *x, int64_t M, int64_t K, cons
                        const float *scale_w, int64_t N, int block, const uint16_t *bias,
                        uint16_t *y, void *workspace, size_t ws_bytes, convrot_stream_t stream);
 
+/* Forward without a workspace, for callers that cannot allocate device
+ * memory on this path: a host framework or plugin that only passes in
+ * pointers to memory it owns, a latency-critical loop where cudaMalloc (which
+ * synchronises the device) is not allowed, or a process held to a fixed
+ * device-memory budget.  The pages have no counterpart of this entry point;
+ * it computes exactly what convrot_linear_fwd computes, with the activation
+ * codes and scales kept in one fixed device array inside the library instead
+ * of a caller workspace.
+ *   - The array is convrot_linear_fwd_noalloc_max_bytes() bytes (64 MiB) on
+ *     every GPU that loads the library, held until the process exits.
+ *     Problems needing more (M*K*2 + M*4 bytes, each part rounded up to 256)
+ *     return CONVROT_ERR_UNSUPPORTED and enqueue nothing.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls share the array: calls whose kernels can overlap on the GPU
+ *     (other streams, other host threads) race and must be serialised by the
+ *     caller.  Nothing needs clearing between calls: each call rewrites all
+ *     it reads.
+ *   - No allocation of any kind happens inside the call.
+ * Arguments, layouts and errors are those of convrot_linear_fwd without the
+ * workspace. */
+CONVROT_API int convrot_linear_fwd_noalloc(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq,
+                               const float *scale_w, int64_t N, int block, const uint16_t *bias,
+                               uint16_t *y, convrot_stream_t stream);
+
+/* Size in bytes of the fixed device array used by convrot_linear_fwd_noalloc. */
+CONVROT_API size_t convrot_linear_fwd_noalloc_max_bytes(void);
+
 /* -------------------------------------------------------- frozen backward -- */
 
 /* Bytes of workspace convrot_prepare_bwd_weight needs ([K, N] fp64). */

@@ -58,6 +58,8 @@ def lib():
                 "convrot_embedding_lookup": ([P, I64, P, P, I64, I64, I, P, P], I),
                 "convrot_gemm_s32_workspace_bytes": ([I64, I64], S),
                 "convrot_gemm_s32": ([P, P, I64, I64, I64, P, P, S, P], I),
+                "convrot_linear_fwd_noalloc": ([P, I64, I64, P, P, I64, I, P, P, P], I),
+                "convrot_linear_fwd_noalloc_max_bytes": ([], S),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
@@ -265,3 +267,29 @@ def convrot_gemm_s32(A, B, C=None, workspace=None, stream=None):
     _check(lib().convrot_gemm_s32(_ptr(A), _ptr(B), M, N, K, _ptr(C), _ptr(ws), nbytes, _stream(stream)),
            "convrot_gemm_s32")
     return C
+
+
+def convrot_linear_fwd_noalloc_max_bytes() -> int:
+    return lib().convrot_linear_fwd_noalloc_max_bytes()
+
+
+def convrot_linear_fwd_noalloc(x, Wq, scale_w, block, bias=None, y=None, stream=None):
+    """Forward without a caller workspace, for callers that cannot allocate on
+    this path (the library keeps the activation codes in a fixed 64 MiB device
+    array; calls that overlap on the GPU must be serialised by the caller).
+    `y` must be given by such callers; it is allocated here only for
+    convenience when omitted."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(Wq, torch.int8, "Wq", 2)
+    _need(scale_w, torch.float32, "scale_w", 1)
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias", 1)
+    M, K = x.shape
+    N = Wq.shape[0]
+    if Wq.shape[1] != K or scale_w.shape[0] != N:
+        raise ValueError("shape mismatch")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(lib().convrot_linear_fwd_noalloc(_ptr(x), M, K, _ptr(Wq), _ptr(scale_w), N, block, _ptr(bias), _ptr(y),
+                                            _stream(stream)), "convrot_linear_fwd_noalloc")
+    return y

@@ -15,7 +15,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libconvrot.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["rotq.cu", "gemm_tc.cu", "convrot_api.cu"]
+SOURCES = ["rotq.cu", "gemm_tc.cu", "convrot_api.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "internal.h"]
 
 NVCC_FLAGS = [
