@@ -6,7 +6,7 @@
 
 #include <mutex>
 
-#include "../../include/convrot.h"
+#include "convrot.h"
 #include "common.cuh"
 #include "internal.h"
 

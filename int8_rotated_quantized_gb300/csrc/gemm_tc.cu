@@ -16,23 +16,28 @@
 // chunk to int32 and add it to an int32 accumulator held in registers.  The
 // result is the exact int32 dot product for any codes in [-127, 127].
 //
-// Operands.  A holds the activation codes already widened to fp16 by the
-// rotate-and-quantize kernel; B holds the int8 weight codes as stored.  TMA
-// brings A tiles (128B swizzle, the layout the MMA reads) and raw int8 B tiles
-// into shared memory; a converter warpgroup widens each B tile to fp16 into a
-// 128B-swizzled K-major buffer.
+// Operands.  The MMA's M side (128 rows, the operand that must be widened)
+// is the WEIGHT: its int8 codes arrive by TMA and a converter warpgroup widens
+// each 128x64 tile to fp16 into a 128B-swizzled K-major buffer.  The N side
+// (256 rows) is the ACTIVATION, whose codes the rotate-and-quantize kernel
+// already stored as fp16: TMA brings them in the 128B-swizzled layout the MMA
+// reads.  Putting the weight on the 128-row side halves the conversion work
+// per MMA compared with the opposite assignment.  The accumulator is therefore
+// the transposed tile (TMEM lane = weight row n, column = token m).
 //
-// CTA roles (512 threads, one persistent CTA per SM, 128x256 output tiles):
+// CTA roles (512 threads, one persistent CTA per SM, 128 weight rows x 256
+// tokens per tile):
 //   warp 0        TMA producer (one lane)
 //   warp 1        TMEM allocator and MMA issuer (one lane)
 //   warps 2-3     idle (complete warpgroup 0 for setmaxnreg)
-//   warps 4-7     int8 -> fp16 converters of the B tiles
+//   warps 4-7     int8 -> fp16 converters of the weight tiles
 //   warps 8-15    epilogue: TMEM -> registers, int32 accumulation, output
-// Pipelines: a 4-stage TMA ring (A fp16 16 KB + B int8 16 KB), a 2-stage
-// converted-B ring (32 KB), and two 128x256 fp32 TMEM accumulators (512
-// columns) alternating per K chunk so the epilogue drains one while the MMA
-// fills the other.  Every wait is bounded: on expiry the kernel records
-// DEVERR_TIMEOUT, lets in-flight copies and MMAs finish, frees TMEM and exits.
+// Pipelines: a 4-stage TMA ring (weight int8 8 KB + activation fp16 32 KB), a
+// 3-stage converted-weight ring (16 KB), and two 128x256 fp32 TMEM
+// accumulators (512 columns) alternating per K chunk so the epilogue drains
+// one while the MMA fills the other.
+// Every wait is bounded: on expiry the kernel records DEVERR_TIMEOUT, lets
+// in-flight copies and MMAs finish, frees TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -44,31 +49,31 @@
 namespace convrot {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int STAGES = 4, CSTAGES = 2;
+constexpr int TW = 128, TT = 256, BK = 64;  // weight rows (MMA M), tokens (MMA N), K per stage
+constexpr int STAGES = 4, CSTAGES = 3;
 constexpr int CHUNK_KB = 16;  // K blocks per exact fp32 chunk: 16 * 64 = 1024
 constexpr int NUM_THREADS = 512;
-constexpr int A_STAGE = BM * BK * 2;    // 16 KB
-constexpr int BI8_STAGE = BN * BK;      // 16 KB
-constexpr int BH_STAGE = BN * BK * 2;   // 32 KB
-constexpr int OFF_A = 0;
-constexpr int OFF_BI8 = OFF_A + STAGES * A_STAGE;
-constexpr int OFF_BH = OFF_BI8 + STAGES * BI8_STAGE;
-constexpr int OFF_BAR = OFF_BH + CSTAGES * BH_STAGE;
-constexpr int NUM_BARS = 17;
+constexpr int W8_STAGE = TW * BK;      // 8 KB int8 weight tile (TMA)
+constexpr int X_STAGE = TT * BK * 2;   // 32 KB fp16 activation tile (TMA)
+constexpr int WH_STAGE = TW * BK * 2;  // 16 KB widened weight tile
+constexpr int OFF_X = 0;
+constexpr int OFF_W8 = OFF_X + STAGES * X_STAGE;
+constexpr int OFF_WH = OFF_W8 + STAGES * W8_STAGE;
+constexpr int OFF_BAR = OFF_WH + CSTAGES * WH_STAGE;
+// Barrier indices.
+constexpr int BAR_TMA_FULL = 0, BAR_TMA_EMPTY = STAGES, BAR_CONV_FULL = 2 * STAGES,
+              BAR_CONV_EMPTY = 2 * STAGES + CSTAGES, BAR_ACC_FULL = 2 * STAGES + 2 * CSTAGES,
+              BAR_ACC_EMPTY = BAR_ACC_FULL + 2, BAR_DRAIN = BAR_ACC_EMPTY + 2, NUM_BARS = BAR_DRAIN + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 constexpr int TMEM_COLS = 512;
 constexpr int REGS_WG0 = 48, REGS_CONV = 72, REGS_EPI = 192;
 static_assert(128 * REGS_WG0 + 128 * REGS_CONV + 256 * REGS_EPI <= 65536, "register split exceeds the launch pool");
 
-// Barrier indices.
-constexpr int BAR_TMA_FULL = 0, BAR_TMA_EMPTY = 4, BAR_CONV_FULL = 8, BAR_CONV_EMPTY = 10, BAR_ACC_FULL = 12,
-              BAR_ACC_EMPTY = 14, BAR_DRAIN = 16;
-
 // kind::f16 instruction descriptor: D fp32, A and B fp16, both K-major,
 // N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(TT >> 3) << 17) | ((uint32_t)(TW >> 4) << 24);
 
 struct GemmArgs {
     int M, N, K;
@@ -213,14 +218,24 @@ __device__ __forceinline__ void widen4(uint32_t w, uint32_t &lo, uint32_t &hi) {
 
 // ------------------------------------------------------------------ kernel --
 
+// Every lane of the warp polls the barrier (a single polling lane with the
+// rest parked in __syncwarp measured 2x slower); the result is made
+// warp-uniform so no lane runs ahead on an abort.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *err,
+                                          int lane) {
+    (void)lane;
+    const bool got = mbar_wait(bar, parity, abort_flag, err);
+    return __all_sync(0xffffffffu, got);
+}
+
 template <bool OUT_S32>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_s8_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs p) {
+    gemm_s8_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const GemmArgs p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base - raw);
-    const uint32_t sA = base + OFF_A, sBi8 = base + OFF_BI8, sBh = base + OFF_BH, sBar = base + OFF_BAR;
+    const uint32_t sX = base + OFF_X, sW8 = base + OFF_W8, sWh = base + OFF_WH, sBar = base + OFF_BAR;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
     auto bar = [&](int i) -> uint32_t { return sBar + 8u * (uint32_t)i; };
@@ -256,31 +271,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int num_m = (p.M + BM - 1) / BM;
-    const int num_n = (p.N + BN - 1) / BN;
-    const int num_tiles = num_m * num_n;
+    // p.M = tokens (activation rows), p.N = weight rows, p.K = contraction.
+    const int num_t = (p.M + TT - 1) / TT;
+    const int num_w = (p.N + TW - 1) / TW;
+    const int num_tiles = num_t * num_w;
     const int num_kb = (p.K + BK - 1) / BK;
 
     if (warp < 4) {
         regs_dec<REGS_WG0>();
         if (warp == 0 && lane == 0) {
             // ---------------------------------------------------- producer
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmA) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmB) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                int mb, nb;
-                tile_coords(tile, num_m, num_n, mb, nb);
+                int tb, wb;
+                tile_coords(tile, num_t, num_w, tb, wb);
                 for (int kb = 0; kb < num_kb; ++kb, ++it) {
                     const int s = it % STAGES;
                     if (!mbar_wait(bar(BAR_TMA_EMPTY + s), ((it / STAGES) & 1) ^ 1, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(bar(BAR_TMA_FULL + s), A_STAGE + BI8_STAGE);
-                    tma_load_2d(sA + s * A_STAGE, &tmA, bar(BAR_TMA_FULL + s), kb * BK, mb * BM);
-                    tma_load_2d(sBi8 + s * BI8_STAGE, &tmB, bar(BAR_TMA_FULL + s), kb * BK, nb * BN);
+                    mbar_expect_tx(bar(BAR_TMA_FULL + s), X_STAGE + W8_STAGE);
+                    tma_load_2d(sX + s * X_STAGE, &tmX, bar(BAR_TMA_FULL + s), kb * BK, tb * TT);
+                    tma_load_2d(sW8 + s * W8_STAGE, &tmW, bar(BAR_TMA_FULL + s), kb * BK, wb * TW);
                 }
             }
             if (!ok) {  // let the copies already issued land before the CTA exits
@@ -302,7 +318,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             break;
                         }
                         tc_fence_after();
-                        dcol = (uint32_t)(buf * BN);
+                        dcol = (uint32_t)(buf * TT);
                     }
                     const int s = it % STAGES;
                     const int c = it % CSTAGES;
@@ -314,8 +330,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = sw128_desc(sA + s * A_STAGE + kk * 32);
-                        const uint64_t bd = sw128_desc(sBh + c * BH_STAGE + kk * 32);
+                        const uint64_t ad = sw128_desc(sWh + c * WH_STAGE + kk * 32);
+                        const uint64_t bd = sw128_desc(sX + s * X_STAGE + kk * 32);
                         umma_f16(tmem + dcol, ad, bd, (kc > 0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(bar(BAR_TMA_EMPTY + s));
@@ -346,25 +362,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int kb = 0; kb < num_kb; ++kb, ++it) {
                 const int s = it % STAGES;
                 const int c = it % CSTAGES;
-                const bool got = mbar_wait(bar(BAR_TMA_FULL + s), (it / STAGES) & 1, abort_flag, p.err) &&
-                                 mbar_wait(bar(BAR_CONV_EMPTY + c), ((it / CSTAGES) & 1) ^ 1, abort_flag, p.err);
-                if (!__all_sync(0xffffffffu, got)) {
+                if (!warp_wait(bar(BAR_TMA_FULL + s), (it / STAGES) & 1, abort_flag, p.err, lane) ||
+                    !warp_wait(bar(BAR_CONV_EMPTY + c), ((it / CSTAGES) & 1) ^ 1, abort_flag, p.err, lane)) {
                     ok = false;
                     break;
                 }
-                const uint8_t *src = smem + OFF_BI8 + s * BI8_STAGE;
-                uint8_t *dst = smem + OFF_BH + c * BH_STAGE;
+                const uint8_t *src = smem + OFF_W8 + s * W8_STAGE;
+                uint8_t *dst = smem + OFF_WH + c * WH_STAGE;
+                // 128 rows x 64 int8 (rows of 64 bytes, no swizzle) -> 128 rows x 64 fp16
+                // in 128B-swizzle atoms (8 rows x 128 bytes, 16-byte chunk j of row r at j ^ (r & 7)).
+                uint4 v[(TW * BK / 16) / 128];
 #pragma unroll
-                for (int j = 0; j < (BN * BK / 16) / 128; ++j) {
+                for (int j = 0; j < (TW * BK / 16) / 128; ++j) {
+                    const int L = j * 128 + ct;
+                    v[j] = *reinterpret_cast<const uint4 *>(src + (L >> 2) * BK + (L & 3) * 16);
+                }
+#pragma unroll
+                for (int j = 0; j < (TW * BK / 16) / 128; ++j) {
                     const int L = j * 128 + ct;
                     const int row = L >> 2;
                     const int c4 = L & 3;
-                    const uint4 v = *reinterpret_cast<const uint4 *>(src + row * BK + c4 * 16);
                     uint32_t w[8];
-                    widen4(v.x, w[0], w[1]);
-                    widen4(v.y, w[2], w[3]);
-                    widen4(v.z, w[4], w[5]);
-                    widen4(v.w, w[6], w[7]);
+                    widen4(v[j].x, w[0], w[1]);
+                    widen4(v[j].y, w[2], w[3]);
+                    widen4(v[j].z, w[4], w[5]);
+                    widen4(v[j].w, w[6], w[7]);
                     uint8_t *atom = dst + (row >> 3) * 1024 + (row & 7) * 128;
                     const int sw = row & 7;
                     *reinterpret_cast<uint4 *>(atom + (((2 * c4) ^ sw) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
@@ -382,26 +404,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else {
         // ------------------------------------------------------------- epilogue
         regs_inc<REGS_EPI>();
-        const int q = warp & 3;          // TMEM lane quarter = rows 32q .. 32q+31
-        const int h = (warp - 8) >> 2;   // column half of the 256-wide tile
+        const int q = warp & 3;          // TMEM lane quarter = weight rows 32q .. 32q+31
+        const int h = (warp - 8) >> 2;   // token half of the 256-wide tile
         int g = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            int mb, nb;
-            tile_coords(tile, num_m, num_n, mb, nb);
+            int tb, wb;
+            tile_coords(tile, num_t, num_w, tb, wb);
             int acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0;
             const int nchunks = (num_kb + CHUNK_KB - 1) / CHUNK_KB;
             for (int ch = 0; ch < nchunks; ++ch, ++g) {
                 const int buf = g & 1;
-                const bool got = mbar_wait(bar(BAR_ACC_FULL + buf), (g >> 1) & 1, abort_flag, p.err);
-                if (!__all_sync(0xffffffffu, got)) {
+                if (!warp_wait(bar(BAR_ACC_FULL + buf), (g >> 1) & 1, abort_flag, p.err, lane)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * BN + h * 128);
+                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * TT + h * 128);
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     uint32_t r[16];
@@ -415,38 +436,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (lane == 0) mbar_arrive(bar(BAR_ACC_EMPTY + buf));
             }
             if (!ok) break;
-            const int row = mb * BM + 32 * q + lane;
-            const int col0 = nb * BN + h * 128;
-            if (row < p.M) {
+            // Thread = weight row n, registers = 128 consecutive tokens m: each
+            // store instruction of the warp writes 32 consecutive n of one row m.
+            const int n = wb * TW + 32 * q + lane;
+            const int m0 = tb * TT + h * 128;
+            if (n < p.N) {
                 if constexpr (OUT_S32) {
-                    int32_t *out = static_cast<int32_t *>(p.out) + (int64_t)row * p.N + col0;
+                    int32_t *out = static_cast<int32_t *>(p.out) + n;
 #pragma unroll
-                    for (int i = 0; i < 128; i += 4)
-                        if (col0 + i < p.N)
-                            *reinterpret_cast<int4 *>(out + i) = make_int4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+                    for (int i = 0; i < 128; ++i)
+                        if (m0 + i < p.M) out[(int64_t)(m0 + i) * p.N] = acc[i];
                 } else {
-                    uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)row * p.N + col0;
-                    const float sx = __ldg(p.sa + row);
+                    uint16_t *out = static_cast<uint16_t *>(p.out) + n;
+                    const float swn = __ldg(p.sb + n);
+                    const float bn = p.bias != nullptr ? bf16_bits_to_float(__ldg(p.bias + n)) : 0.f;
 #pragma unroll
-                    for (int i = 0; i < 128; i += 8) {
-                        if (col0 + i >= p.N) continue;
-                        const float4 w0 = __ldg(reinterpret_cast<const float4 *>(p.sb + col0 + i));
-                        const float4 w1 = __ldg(reinterpret_cast<const float4 *>(p.sb + col0 + i + 4));
-                        const float sw[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-                        float y[8];
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) y[k] = __fmul_rn(__int2float_rn(acc[i + k]), __fmul_rn(sx, sw[k]));
-                        if (p.bias != nullptr) {
-                            const uint4 bv = __ldg(reinterpret_cast<const uint4 *>(p.bias + col0 + i));
-                            const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                y[2 * k] = __fadd_rn(y[2 * k], bf16_bits_to_float(bw[k] & 0xffffu));
-                                y[2 * k + 1] = __fadd_rn(y[2 * k + 1], bf16_bits_to_float(bw[k] >> 16));
-                            }
+                    for (int i = 0; i < 128; ++i) {
+                        const int m = m0 + i;
+                        if (m < p.M) {
+                            float y = __fmul_rn(__int2float_rn(acc[i]), __fmul_rn(__ldg(p.sa + m), swn));
+                            if (p.bias != nullptr) y = __fadd_rn(y, bn);
+                            out[(int64_t)m * p.N] = (uint16_t)float_to_bf16_bits(y);
                         }
-                        *reinterpret_cast<uint4 *>(out + i) = make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                                                                         pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
                     }
                 }
             }
@@ -501,24 +512,24 @@ cudaError_t launch_gemm(const uint16_t *A, const float *sa, const int8_t *B, con
     if (M == 0 || N == 0) return cudaSuccess;
     cudaError_t e = get_encoder();
     if (e != cudaSuccess) return e;
-    CUtensorMap tmA, tmB;
-    if (!encode_2d(&tmA, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, (uint64_t)K, (uint64_t)M, BK, BM,
+    CUtensorMap tmX, tmW;
+    if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, (uint64_t)K, (uint64_t)M, BK, TT,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, (uint64_t)K, (uint64_t)N, BK, BN,
+        !encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, (uint64_t)K, (uint64_t)N, BK, TW,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     GemmArgs p{(int)M, (int)N, (int)K, sa, sb, bias, out, err};
-    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    const int64_t tiles = ((M + TT - 1) / TT) * ((N + TW - 1) / TW);
     const int sms = sm_count_of_current_device();
     const int grid = (int)(tiles < sms ? tiles : sms);
     if (out_s32) {
         e = cudaFuncSetAttribute(gemm_s8_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        gemm_s8_tc_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, p);
+        gemm_s8_tc_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmX, tmW, p);
     } else {
         e = cudaFuncSetAttribute(gemm_s8_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        gemm_s8_tc_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmA, tmB, p);
+        gemm_s8_tc_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmX, tmW, p);
     }
     return cudaGetLastError();
 }

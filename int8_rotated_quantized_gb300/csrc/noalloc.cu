@@ -16,7 +16,7 @@
 // them), so nothing has to be cleared between calls.
 #include <mutex>
 
-#include "../../include/convrot.h"
+#include "convrot.h"
 #include "common.cuh"
 #include "internal.h"
 

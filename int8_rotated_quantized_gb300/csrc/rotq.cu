@@ -91,8 +91,121 @@ __device__ __forceinline__ void fwht_lanes(CT (&e)[8], int lanes, int lane) {
     }
 }
 
-// ----------------------------------------------------------- code stores --
+// ------------------------------------------- fp32 path (packed f32x2 ops) --
+//
+// The same butterflies with two lanes of fp32 per instruction (f32x2, round
+// to nearest per lane, so every value equals the scalar computation).
 
+// (a, c) -> (a + c, a - c) on the pairs (a0, a1) and (c0, c1).
+__device__ __forceinline__ void addsub2(float &a0, float &a1, float &c0, float &c1) {
+    asm("{\n .reg .b64 ra, rc, rs, rd;\n mov.b64 ra, {%0, %1};\n mov.b64 rc, {%2, %3};\n"
+        " add.rn.f32x2 rs, ra, rc;\n sub.rn.f32x2 rd, ra, rc;\n mov.b64 {%0, %1}, rs;\n mov.b64 {%2, %3}, rd;\n}"
+        : "+f"(a0), "+f"(a1), "+f"(c0), "+f"(c1));
+}
+
+// (e0, e1) <- (s * e0 + p0, s * e1 + p1) with s = +-1: one rounding, equal to e + p or p - e.
+__device__ __forceinline__ void sfma2(float s, float &e0, float &e1, float p0, float p1) {
+    asm("{\n .reg .b64 rs, re, rp;\n mov.b64 rs, {%2, %2};\n mov.b64 re, {%0, %1};\n mov.b64 rp, {%3, %4};\n"
+        " fma.rn.f32x2 re, rs, re, rp;\n mov.b64 {%0, %1}, re;\n}"
+        : "+f"(e0), "+f"(e1)
+        : "f"(s), "f"(p0), "f"(p1));
+}
+
+// (e0, e1) <- (e0 * k + c, e1 * k + c): one rounding per lane.
+__device__ __forceinline__ void fma2c(float &e0, float &e1, float k, float c) {
+    asm("{\n .reg .b64 rk, re, rc;\n mov.b64 rk, {%2, %2};\n mov.b64 re, {%0, %1};\n mov.b64 rc, {%3, %3};\n"
+        " fma.rn.f32x2 re, re, rk, rc;\n mov.b64 {%0, %1}, re;\n}"
+        : "+f"(e0), "+f"(e1)
+        : "f"(k), "f"(c));
+}
+
+__device__ __forceinline__ void mul2c(float &e0, float &e1, float k) {
+    asm("{\n .reg .b64 rk, re;\n mov.b64 rk, {%2, %2};\n mov.b64 re, {%0, %1};\n"
+        " mul.rn.f32x2 re, re, rk;\n mov.b64 {%0, %1}, re;\n}"
+        : "+f"(e0), "+f"(e1)
+        : "f"(k));
+}
+
+__device__ __forceinline__ void add2c(float &e0, float &e1, float c) {
+    asm("{\n .reg .b64 rc, re;\n mov.b64 rc, {%2, %2};\n mov.b64 re, {%0, %1};\n"
+        " add.rn.f32x2 re, re, rc;\n mov.b64 {%0, %1}, re;\n}"
+        : "+f"(e0), "+f"(e1)
+        : "f"(c));
+}
+
+template <>
+__device__ __forceinline__ void fwht8<float>(float (&e)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {  // h = 1 lies inside a pair: scalar
+        const float a = e[i], c = e[i + 1];
+        e[i] = a + c;
+        e[i + 1] = a - c;
+    }
+    addsub2(e[0], e[1], e[2], e[3]);  // h = 2
+    addsub2(e[4], e[5], e[6], e[7]);
+    addsub2(e[0], e[1], e[4], e[5]);  // h = 4
+    addsub2(e[2], e[3], e[6], e[7]);
+}
+
+template <>
+__device__ __forceinline__ void fwht_lanes<float>(float (&e)[8], int lanes, int lane) {
+    for (int m = 1; m < lanes; m <<= 1) {
+        const float sg = (lane & m) ? -1.f : 1.f;
+        float p[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) p[i] = __shfl_xor_sync(0xffffffffu, e[i], m);
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) sfma2(sg, e[i], e[i + 1], p[i], p[i + 1]);
+    }
+}
+
+// ----------------------------------------------------------- code stores --
+//
+// Codes are rne(u * inv) with |u * inv| < 127.5 (|u| <= amax_u and
+// inv = fp32(127 / amax_u)), so the result already lies in [-127, 127].  The
+// rounding is done by adding 1.5 * 2^23 (+ an offset): in [2^23, 2^24) the
+// fp32 spacing is 1, so the sum is u * inv rounded to the nearest integer,
+// ties to even, and the integer sits in the low mantissa bits.
+
+constexpr float kMagicI8 = 12582912.0f;   // 1.5 * 2^23: low byte = two's-complement code
+constexpr float kMagicF16 = 12608640.0f;  // 1.5 * 2^23 + 0x6480: low 16 bits = fp16 bits of 1152 + code
+
+__device__ __forceinline__ void quant_store(float (&e)[8], float inv, int8_t *dst) {
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) mul2c(e[i], e[i + 1], inv);
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) add2c(e[i], e[i + 1], kMagicI8);
+    uint32_t b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) b[i] = __float_as_uint(e[i]);
+    uint32_t w[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const uint32_t lo = __byte_perm(b[4 * k], b[4 * k + 1], 0x0040);
+        const uint32_t hi = __byte_perm(b[4 * k + 2], b[4 * k + 3], 0x0040);
+        w[k] = __byte_perm(lo, hi, 0x5410);
+    }
+    *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
+}
+
+__device__ __forceinline__ void quant_store(float (&e)[8], float inv, __half *dst) {
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) mul2c(e[i], e[i + 1], inv);
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) add2c(e[i], e[i + 1], kMagicF16);
+    const __half2 k1152 = __half2half2(__ushort_as_half((unsigned short)0x6480));
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t v = __byte_perm(__float_as_uint(e[2 * i]), __float_as_uint(e[2 * i + 1]), 0x5410);
+        __half2 h = __hsub2(*reinterpret_cast<__half2 *>(&v), k1152);
+        w[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// fp64 path (the one-off backward-weight preparation): round in fp32 after
+// converting the transform, with an explicit clamp.
 __device__ __forceinline__ int quant_code(float u, float inv) {
     int q = __float2int_rn(__fmul_rn(u, inv));
     return max(-127, min(127, q));
@@ -178,6 +291,7 @@ __global__ void __launch_bounds__(kMaxThreads) rotq_rows_kernel(const RotqArgs a
             for (int r = 0; r < RPT; ++r)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) d[r][i] = 0.f;
+#pragma unroll 4
             for (int j = 0; j < a.rank; ++j) {
                 const float4 *ap = reinterpret_cast<const float4 *>(a.lora_A + (int64_t)j * a.K + 8 * c);
                 float4 a0 = __ldg(ap), a1 = __ldg(ap + 1);
@@ -235,10 +349,14 @@ __global__ void __launch_bounds__(kMaxThreads) rotq_rows_kernel(const RotqArgs a
         for (int s = 0; s < S; ++s) {
             const int64_t c = (int64_t)s * G + t;
             if (c >= chunks) continue;
-            int q[8];
+            if constexpr (sizeof(CT) == 4) {
+                quant_store(e[r][s], inv, qrow + 8 * c);
+            } else {
+                int q[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) q[i] = quant_code((float)e[r][s][i], inv);
-            store_codes(qrow + 8 * c, q);
+                for (int i = 0; i < 8; ++i) q[i] = quant_code((float)e[r][s][i], inv);
+                store_codes(qrow + 8 * c, q);
+            }
         }
     }
 }
