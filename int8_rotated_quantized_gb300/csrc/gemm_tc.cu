@@ -97,21 +97,26 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, 1000;\n selp.u32 %0, 1, 0, "
+        "p;\n}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
 }
 
-// Bounded wait on the phase with the given parity.  Returns false if another
-// role aborted or the wall-clock limit expired (then the abort flag is set and
-// the error word records a timeout).
+// Bounded wait on the phase with the given parity.  Each poll may suspend the
+// thread in hardware for up to 1 us (it wakes when the phase completes), so
+// waiting warps leave the issue slots and the shared-memory pipe to the
+// working ones; the abort flag and the clock are read every 64 polls.
+// Returns false if another role aborted or the wall-clock limit expired (then
+// the abort flag is set and the error word records a timeout).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *err) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    while (true) {
+    for (uint32_t spin = 1;; ++spin) {
         if (mbar_try_wait(bar, parity)) return true;
+        if ((spin & 63) != 0) continue;
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             *abort_flag = 1;

@@ -10,6 +10,15 @@ cudaError_t launch_rotq_bf16(const uint16_t *x, int64_t rows, int64_t K, int64_t
                              const float *lora_A, const float *lora_B, int rank, float coef, bool out_f16,
                              void *q, float *scale, cudaStream_t st);
 
+// 32-elements-per-thread variants (rotq_wide.cu): usable when the row length
+// is a multiple of 32 and pointers/strides allow 32-byte accesses.
+bool rotq_wide_ok(const void *x, int64_t K, int64_t ldx, const void *q);
+cudaError_t launch_rotq_wide(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx, int block, bool out_f16, void *q,
+                             float *scale, cudaStream_t st);
+bool lookup_wide_ok(const void *Eq, int64_t D, const void *out);
+cudaError_t launch_lookup_wide(const int64_t *ids, int64_t n, const int8_t *Eq, const float *scale_e, int64_t V,
+                               int64_t D, int block, uint16_t *out, unsigned *err, cudaStream_t st);
+
 cudaError_t launch_rotq_f64(const double *x, int64_t rows, int64_t K, int block, int8_t *q, float *scale,
                             cudaStream_t st);
 

@@ -19,6 +19,7 @@
 //   code  = clamp(rne(u * (127 / amax_u)), -127, 127)   (= rne(v / scale)).
 // An all-zero row gets scale 0 and codes 0.
 #include "common.cuh"
+#include "fwht.cuh"
 #include "internal.h"
 
 namespace convrot {
@@ -91,48 +92,6 @@ __device__ __forceinline__ void fwht_lanes(CT (&e)[8], int lanes, int lane) {
     }
 }
 
-// ------------------------------------------- fp32 path (packed f32x2 ops) --
-//
-// The same butterflies with two lanes of fp32 per instruction (f32x2, round
-// to nearest per lane, so every value equals the scalar computation).
-
-// (a, c) -> (a + c, a - c) on the pairs (a0, a1) and (c0, c1).
-__device__ __forceinline__ void addsub2(float &a0, float &a1, float &c0, float &c1) {
-    asm("{\n .reg .b64 ra, rc, rs, rd;\n mov.b64 ra, {%0, %1};\n mov.b64 rc, {%2, %3};\n"
-        " add.rn.f32x2 rs, ra, rc;\n sub.rn.f32x2 rd, ra, rc;\n mov.b64 {%0, %1}, rs;\n mov.b64 {%2, %3}, rd;\n}"
-        : "+f"(a0), "+f"(a1), "+f"(c0), "+f"(c1));
-}
-
-// (e0, e1) <- (s * e0 + p0, s * e1 + p1) with s = +-1: one rounding, equal to e + p or p - e.
-__device__ __forceinline__ void sfma2(float s, float &e0, float &e1, float p0, float p1) {
-    asm("{\n .reg .b64 rs, re, rp;\n mov.b64 rs, {%2, %2};\n mov.b64 re, {%0, %1};\n mov.b64 rp, {%3, %4};\n"
-        " fma.rn.f32x2 re, rs, re, rp;\n mov.b64 {%0, %1}, re;\n}"
-        : "+f"(e0), "+f"(e1)
-        : "f"(s), "f"(p0), "f"(p1));
-}
-
-// (e0, e1) <- (e0 * k + c, e1 * k + c): one rounding per lane.
-__device__ __forceinline__ void fma2c(float &e0, float &e1, float k, float c) {
-    asm("{\n .reg .b64 rk, re, rc;\n mov.b64 rk, {%2, %2};\n mov.b64 re, {%0, %1};\n mov.b64 rc, {%3, %3};\n"
-        " fma.rn.f32x2 re, re, rk, rc;\n mov.b64 {%0, %1}, re;\n}"
-        : "+f"(e0), "+f"(e1)
-        : "f"(k), "f"(c));
-}
-
-__device__ __forceinline__ void mul2c(float &e0, float &e1, float k) {
-    asm("{\n .reg .b64 rk, re;\n mov.b64 rk, {%2, %2};\n mov.b64 re, {%0, %1};\n"
-        " mul.rn.f32x2 re, re, rk;\n mov.b64 {%0, %1}, re;\n}"
-        : "+f"(e0), "+f"(e1)
-        : "f"(k));
-}
-
-__device__ __forceinline__ void add2c(float &e0, float &e1, float c) {
-    asm("{\n .reg .b64 rc, re;\n mov.b64 rc, {%2, %2};\n mov.b64 re, {%0, %1};\n"
-        " add.rn.f32x2 re, re, rc;\n mov.b64 {%0, %1}, re;\n}"
-        : "+f"(e0), "+f"(e1)
-        : "f"(c));
-}
-
 template <>
 __device__ __forceinline__ void fwht8<float>(float (&e)[8]) {
 #pragma unroll
@@ -161,15 +120,6 @@ __device__ __forceinline__ void fwht_lanes<float>(float (&e)[8], int lanes, int 
 
 // ----------------------------------------------------------- code stores --
 //
-// Codes are rne(u * inv) with |u * inv| < 127.5 (|u| <= amax_u and
-// inv = fp32(127 / amax_u)), so the result already lies in [-127, 127].  The
-// rounding is done by adding 1.5 * 2^23 (+ an offset): in [2^23, 2^24) the
-// fp32 spacing is 1, so the sum is u * inv rounded to the nearest integer,
-// ties to even, and the integer sits in the low mantissa bits.
-
-constexpr float kMagicI8 = 12582912.0f;   // 1.5 * 2^23: low byte = two's-complement code
-constexpr float kMagicF16 = 12608640.0f;  // 1.5 * 2^23 + 0x6480: low 16 bits = fp16 bits of 1152 + code
-
 __device__ __forceinline__ void quant_store(float (&e)[8], float inv, int8_t *dst) {
 #pragma unroll
     for (int i = 0; i < 8; i += 2) mul2c(e[i], e[i + 1], inv);
@@ -239,6 +189,7 @@ struct RotqArgs {
     int lanes;          // b / 8
     int G;              // threads per row group (multiple of 32, <= 512)
     double scale_coef;  // 1 / (127 sqrt(b))
+    float scale_denom;  // fp32(127 sqrt(b))
     void *q;            // codes, row stride K
     float *scale;
     const float *lora_A;  // [rank, K]
@@ -247,115 +198,189 @@ struct RotqArgs {
     float coef;  // scale * alpha / rank
 };
 
+// Raw storage of one 8-element slot as loaded (bf16: one 16-byte vector;
+// fp64: four 16-byte vectors), so the next rows can be prefetched into
+// registers while the current ones are transformed.
+template <typename InT>
+struct Raw8;
+template <>
+struct Raw8<uint16_t> {
+    uint4 v;
+    __device__ __forceinline__ void load(const uint16_t *p) { v = __ldcs(reinterpret_cast<const uint4 *>(p)); }
+    __device__ __forceinline__ void zero() { v = make_uint4(0, 0, 0, 0); }
+    __device__ __forceinline__ void unpack(float (&e)[8]) const {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            e[2 * i] = __uint_as_float(w[i] << 16);
+            e[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+template <>
+struct Raw8<double> {
+    double v[8];
+    __device__ __forceinline__ void load(const double *p) {
+        const double2 *q = reinterpret_cast<const double2 *>(p);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const double2 d = __ldcs(q + i);
+            v[2 * i] = d.x;
+            v[2 * i + 1] = d.y;
+        }
+    }
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = 0.0;
+    }
+    __device__ __forceinline__ void unpack(double (&e)[8]) const {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) e[i] = v[i];
+    }
+};
+
 // InT: element type of x (uint16_t = bf16 bits, or double).  CT: arithmetic
 // type of the transform.  OutT: int8_t codes or __half-held codes.  S: 8-element
 // slots per thread.  RPT: rows held per thread group at once.  LORA: merge
 // W + coef * B@A (fp32, sequential fma over the rank, rounded to bf16) first.
+//
+// Persistent: each CTA walks row blocks (groups * RPT rows) with a grid
+// stride; the raw data of the next block is loaded before the current one is
+// transformed, so HBM reads overlap the arithmetic.
 template <typename InT, typename CT, typename OutT, int S, int RPT, bool LORA>
 __global__ void __launch_bounds__(kMaxThreads) rotq_rows_kernel(const RotqArgs a) {
-    __shared__ CT red[RPT][kMaxThreads / 32];
+    __shared__ CT red[2][RPT][kMaxThreads / 32];
     const int G = a.G;
     const int g = threadIdx.x / G;
     const int t = threadIdx.x - g * G;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int groups = blockDim.x / G;
-    const int64_t row0 = ((int64_t)blockIdx.x * groups + g) * RPT;
     const int64_t chunks = a.K >> 3;
+    const int64_t rows_per_block = (int64_t)groups * RPT;
+    const int64_t nblocks = (a.rows + rows_per_block - 1) / rows_per_block;
     const InT *x = static_cast<const InT *>(a.x);
+    const int wpg = G >> 5;
 
-    CT e[RPT][S][8];
+    Raw8<InT> raw[RPT][S];
+    auto fetch = [&](int64_t blk) {
+        const int64_t row0 = (blk * groups + g) * RPT;
 #pragma unroll
-    for (int r = 0; r < RPT; ++r) {
+        for (int r = 0; r < RPT; ++r) {
 #pragma unroll
-        for (int s = 0; s < S; ++s) {
-            const int64_t c = (int64_t)s * G + t;
-            const int64_t row = row0 + r;
-            if (c < chunks && row < a.rows)
-                load8(x + row * a.ldx + 8 * c, e[r][s]);
-            else
-                zero8(e[r][s]);
+            for (int s = 0; s < S; ++s) {
+                const int64_t c = (int64_t)s * G + t;
+                const int64_t row = row0 + r;
+                if (c < chunks && row < a.rows)
+                    raw[r][s].load(x + row * a.ldx + 8 * c);
+                else
+                    raw[r][s].zero();
+            }
         }
-    }
+    };
 
-    if constexpr (LORA) {
-        // W' = bf16(W + coef * sum_j B[n,j] A[j,k]) with d accumulated by
-        // fused multiply-adds in j order (voxprint-model-forge MOSS page:
-        // merge W + scale * (alpha / rank) * B @ A before quantizing).
+    // The fp64 variant (one-off backward-weight preparation) has no register
+    // room for a second copy: it loads at the top of each block instead.
+    constexpr bool kPrefetch = sizeof(InT) == 2;
+    int par = 0;
+    int64_t blk = blockIdx.x;
+    if (kPrefetch && blk < nblocks) fetch(blk);
+    for (; blk < nblocks; blk += gridDim.x, par ^= 1) {
+        const int64_t row0 = (blk * groups + g) * RPT;
+        if (!kPrefetch) fetch(blk);
+        CT e[RPT][S][8];
 #pragma unroll
-        for (int s = 0; s < S; ++s) {
-            const int64_t c = (int64_t)s * G + t;
-            if (c >= chunks) continue;
-            float d[RPT][8];
+        for (int r = 0; r < RPT; ++r)
 #pragma unroll
-            for (int r = 0; r < RPT; ++r)
+            for (int s = 0; s < S; ++s) raw[r][s].unpack(e[r][s]);
+        if (kPrefetch && blk + gridDim.x < nblocks) fetch(blk + gridDim.x);
+
+        if constexpr (LORA) {
+            // W' = bf16(W + coef * sum_j B[n,j] A[j,k]) with d accumulated by
+            // fused multiply-adds in j order (voxprint-model-forge MOSS page:
+            // merge W + scale * (alpha / rank) * B @ A before quantizing).
 #pragma unroll
-                for (int i = 0; i < 8; ++i) d[r][i] = 0.f;
+            for (int s = 0; s < S; ++s) {
+                const int64_t c = (int64_t)s * G + t;
+                if (c >= chunks) continue;
+                float d[RPT][8];
+#pragma unroll
+                for (int r = 0; r < RPT; ++r)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) d[r][i] = 0.f;
 #pragma unroll 4
-            for (int j = 0; j < a.rank; ++j) {
-                const float4 *ap = reinterpret_cast<const float4 *>(a.lora_A + (int64_t)j * a.K + 8 * c);
-                float4 a0 = __ldg(ap), a1 = __ldg(ap + 1);
-                float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                for (int j = 0; j < a.rank; ++j) {
+                    const float4 *ap = reinterpret_cast<const float4 *>(a.lora_A + (int64_t)j * a.K + 8 * c);
+                    float4 a0 = __ldg(ap), a1 = __ldg(ap + 1);
+                    float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
-                for (int r = 0; r < RPT; ++r) {
-                    const int64_t row = min(row0 + r, a.rows - 1);
-                    const float bj = __ldg(a.lora_B + row * a.rank + j);
+                    for (int r = 0; r < RPT; ++r) {
+                        const int64_t row = min(row0 + r, a.rows - 1);
+                        const float bj = __ldg(a.lora_B + row * a.rank + j);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) d[r][i] = __fmaf_rn(bj, av[i], d[r][i]);
+                        for (int i = 0; i < 8; ++i) d[r][i] = __fmaf_rn(bj, av[i], d[r][i]);
+                    }
                 }
+#pragma unroll
+                for (int r = 0; r < RPT; ++r)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        e[r][s][i] =
+                            __bfloat162float(__float2bfloat16_rn(__fmaf_rn(a.coef, d[r][i], (float)e[r][s][i])));
+            }
+        }
+
+        CT amax[RPT];
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            amax[r] = CT(0);
+#pragma unroll
+            for (int s = 0; s < S; ++s) {
+                fwht8(e[r][s]);
+                fwht_lanes(e[r][s], a.lanes, lane);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) amax[r] = maxv(amax[r], absv(e[r][s][i]));
             }
 #pragma unroll
-            for (int r = 0; r < RPT; ++r)
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    e[r][s][i] = __bfloat162float(__float2bfloat16_rn(__fmaf_rn(a.coef, d[r][i], (float)e[r][s][i])));
+            for (int m = 16; m >= 1; m >>= 1) amax[r] = maxv(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], m));
+            if (lane == 0) red[par][r][warp] = amax[r];
         }
-    }
-
-    CT amax[RPT];
+        __syncthreads();
 #pragma unroll
-    for (int r = 0; r < RPT; ++r) {
-        amax[r] = CT(0);
-#pragma unroll
-        for (int s = 0; s < S; ++s) {
-            fwht8(e[r][s]);
-            fwht_lanes(e[r][s], a.lanes, lane);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) amax[r] = maxv(amax[r], absv(e[r][s][i]));
+        for (int r = 0; r < RPT; ++r) {
+            CT m = CT(0);
+            for (int w = 0; w < wpg; ++w) m = maxv(m, red[par][r][g * wpg + w]);
+            amax[r] = m;
         }
-#pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) amax[r] = maxv(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], m));
-        if (lane == 0) red[r][warp] = amax[r];
-    }
-    __syncthreads();
-    const int wpg = G >> 5;
-#pragma unroll
-    for (int r = 0; r < RPT; ++r) {
-        CT m = CT(0);
-        for (int w = 0; w < wpg; ++w) m = maxv(m, red[r][g * wpg + w]);
-        amax[r] = m;
-    }
 
 #pragma unroll
-    for (int r = 0; r < RPT; ++r) {
-        const int64_t row = row0 + r;
-        if (row >= a.rows) continue;
-        // The code decision is taken in fp32 on the fp32-rounded transform.
-        const float amax_f = (float)amax[r];
-        const float inv = amax_f > 0.f ? __fdiv_rn(127.f, amax_f) : 0.f;
-        if (t == 0) a.scale[row] = (float)((double)amax[r] * a.scale_coef);
-        OutT *qrow = static_cast<OutT *>(a.q) + row * a.K;
+        for (int r = 0; r < RPT; ++r) {
+            const int64_t row = row0 + r;
+            if (row >= a.rows) continue;
+            // The code decision is taken in fp32 on the fp32-rounded transform.
+            const float amax_f = (float)amax[r];
+            const float inv = amax_f > 0.f ? __fdiv_rn(127.f, amax_f) : 0.f;
+            // scale = amax_u / (127 sqrt(b)); fp32 on the hot path (fp64 issue
+            // is scarce on this GPU), fp64 in the fp64 variant.
+            if (t == 0) {
+                if constexpr (sizeof(CT) == 4)
+                    a.scale[row] = __fdiv_rn(amax_f, a.scale_denom);
+                else
+                    a.scale[row] = (float)((double)amax[r] * a.scale_coef);
+            }
+            OutT *qrow = static_cast<OutT *>(a.q) + row * a.K;
 #pragma unroll
-        for (int s = 0; s < S; ++s) {
-            const int64_t c = (int64_t)s * G + t;
-            if (c >= chunks) continue;
-            if constexpr (sizeof(CT) == 4) {
-                quant_store(e[r][s], inv, qrow + 8 * c);
-            } else {
-                int q[8];
+            for (int s = 0; s < S; ++s) {
+                const int64_t c = (int64_t)s * G + t;
+                if (c >= chunks) continue;
+                if constexpr (sizeof(CT) == 4) {
+                    quant_store(e[r][s], inv, qrow + 8 * c);
+                } else {
+                    int q[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) q[i] = quant_code((float)e[r][s][i], inv);
-                store_codes(qrow + 8 * c, q);
+                    for (int i = 0; i < 8; ++i) q[i] = quant_code((float)e[r][s][i], inv);
+                    store_codes(qrow + 8 * c, q);
+                }
             }
         }
     }
@@ -379,7 +404,14 @@ cudaError_t launch_rotq_t(const RotqArgs &base, int64_t rows, int64_t K, cudaStr
     const int threads = groups * G;
     auto go = [&](auto kernel, int rpt) -> cudaError_t {
         const int64_t per_cta = (int64_t)groups * rpt;
-        const int64_t grid = (rows + per_cta - 1) / per_cta;
+        const int64_t nblocks = (rows + per_cta - 1) / per_cta;
+        int dev = 0, sms = 0, per_sm = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+        if (e != cudaSuccess) return e;
+        const int64_t resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+        const int64_t grid = nblocks < resident ? nblocks : resident;
         kernel<<<(unsigned)grid, threads, 0, st>>>(a);
         return cudaGetLastError();
     };
@@ -399,8 +431,10 @@ cudaError_t launch_rotq_t(const RotqArgs &base, int64_t rows, int64_t K, cudaStr
 // ------------------------------------------------------- embedding lookup --
 
 // out[t] = bf16( (scale[id] * Eq[id,:]) R ).  The transform runs on the integer
-// codes (exact in fp32: |sums| <= 127 * 256), then one scaling.
-template <int S>
+// codes (exact in fp32: |sums| <= 127 * 256), then one scaling.  Persistent
+// like the quantizer: each CTA walks blocks of groups * RPT tokens and
+// prefetches the next block's codes while it transforms the current ones.
+template <int S, int RPT>
 __global__ void __launch_bounds__(kMaxThreads) emb_lookup_kernel(const int64_t *ids, int64_t n, const int8_t *Eq,
                                                                  const float *scale_e, int64_t V, int64_t D,
                                                                  int lanes, int G, float inv_sqrt_b, uint16_t *out,
@@ -409,39 +443,72 @@ __global__ void __launch_bounds__(kMaxThreads) emb_lookup_kernel(const int64_t *
     const int t = threadIdx.x - g * G;
     const int lane = threadIdx.x & 31;
     const int groups = blockDim.x / G;
-    const int64_t tok = (int64_t)blockIdx.x * groups + g;
     const int64_t chunks = D >> 3;
-    int64_t id = -1;
-    if (tok < n) id = __ldg(ids + tok);
-    const bool ok = tok < n && id >= 0 && id < V;
-    if (tok < n && !ok && t == 0) atomicOr(err, DEVERR_INDEX);
-    const float s = ok ? __ldg(scale_e + id) : 0.f;
-    float e[S][8];
+    const int64_t per_block = (int64_t)groups * RPT;
+    const int64_t nblocks = (n + per_block - 1) / per_block;
+
+    uint2 raw[RPT][S];
+    float sc[RPT];
+    int64_t idv[RPT];
+    auto fetch = [&](int64_t blk) {
 #pragma unroll
-    for (int sl = 0; sl < S; ++sl) {
-        const int64_t c = (int64_t)sl * G + t;
-        if (ok && c < chunks) {
-            uint2 v = __ldcs(reinterpret_cast<const uint2 *>(Eq + id * D + 8 * c));
-            uint32_t w[2] = {v.x, v.y};
+        for (int r = 0; r < RPT; ++r) {
+            const int64_t tok = (blk * groups + g) * RPT + r;
+            int64_t id = -1;
+            if (tok < n) id = __ldg(ids + tok);
+            const bool ok = tok < n && id >= 0 && id < V;
+            if (tok < n && !ok && t == 0) atomicOr(err, DEVERR_INDEX);
+            idv[r] = ok ? id : -1;
+            sc[r] = ok ? __ldg(scale_e + id) : 0.f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) e[sl][i] = (float)(int8_t)((w[i >> 2] >> (8 * (i & 3))) & 0xff);
-        } else {
-            zero8(e[sl]);
+            for (int sl = 0; sl < S; ++sl) {
+                const int64_t c = (int64_t)sl * G + t;
+                raw[r][sl] = (ok && c < chunks) ? __ldcs(reinterpret_cast<const uint2 *>(Eq + id * D + 8 * c))
+                                                : make_uint2(0, 0);
+            }
         }
-        fwht8(e[sl]);
-        fwht_lanes(e[sl], lanes, lane);
-    }
-    if (tok >= n) return;
+    };
+
+    int64_t blk = blockIdx.x;
+    if (blk < nblocks) fetch(blk);
+    for (; blk < nblocks; blk += gridDim.x) {
+        float e[RPT][S][8];
+        float s_cur[RPT];
 #pragma unroll
-    for (int sl = 0; sl < S; ++sl) {
-        const int64_t c = (int64_t)sl * G + t;
-        if (c >= chunks) continue;
-        uint32_t w[4];
+        for (int r = 0; r < RPT; ++r) {
+            s_cur[r] = sc[r];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            w[i] = pack_bf16x2(__fmul_rn(__fmul_rn(e[sl][2 * i], s), inv_sqrt_b),
-                               __fmul_rn(__fmul_rn(e[sl][2 * i + 1], s), inv_sqrt_b));
-        *reinterpret_cast<uint4 *>(out + tok * D + 8 * c) = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int sl = 0; sl < S; ++sl) {
+                const uint32_t w[2] = {raw[r][sl].x, raw[r][sl].y};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) e[r][sl][i] = (float)(int8_t)((w[i >> 2] >> (8 * (i & 3))) & 0xff);
+            }
+        }
+        if (blk + gridDim.x < nblocks) fetch(blk + gridDim.x);
+#pragma unroll
+        for (int r = 0; r < RPT; ++r) {
+            const int64_t tok = (blk * groups + g) * RPT + r;
+#pragma unroll
+            for (int sl = 0; sl < S; ++sl) {
+                fwht8(e[r][sl]);
+                fwht_lanes(e[r][sl], lanes, lane);
+            }
+            if (tok >= n) continue;
+#pragma unroll
+            for (int sl = 0; sl < S; ++sl) {
+                const int64_t c = (int64_t)sl * G + t;
+                if (c >= chunks) continue;
+                uint32_t w[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float y0 = __fmul_rn(__fmul_rn(e[r][sl][2 * i], s_cur[r]), inv_sqrt_b);
+                    const float y1 = __fmul_rn(__fmul_rn(e[r][sl][2 * i + 1], s_cur[r]), inv_sqrt_b);
+                    __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
+                    w[i] = *reinterpret_cast<uint32_t *>(&h);
+                }
+                __stcs(reinterpret_cast<uint4 *>(out + tok * D + 8 * c), make_uint4(w[0], w[1], w[2], w[3]));
+            }
+        }
     }
 }
 
@@ -511,6 +578,8 @@ cudaError_t launch_rotq_bf16(const uint16_t *x, int64_t rows, int64_t K, int64_t
                              const float *lora_B, int rank, float coef, bool out_f16, void *q, float *scale,
                              cudaStream_t st) {
     if (rows == 0) return cudaSuccess;
+    if (lora_A == nullptr && rotq_wide_ok(x, K, ldx, q))
+        return launch_rotq_wide(x, rows, K, ldx, block, out_f16, q, scale, st);
     RotqArgs a{};
     a.x = x;
     a.rows = rows;
@@ -518,6 +587,7 @@ cudaError_t launch_rotq_bf16(const uint16_t *x, int64_t rows, int64_t K, int64_t
     a.ldx = ldx;
     a.lanes = lanes_of(block);
     a.scale_coef = 1.0 / (127.0 * sqrt((double)block));
+    a.scale_denom = (float)(127.0 * sqrt((double)block));
     a.q = q;
     a.scale = scale;
     a.lora_A = lora_A;
@@ -547,6 +617,7 @@ cudaError_t launch_rotq_f64(const double *x, int64_t rows, int64_t K, int block,
 cudaError_t launch_emb_lookup(const int64_t *ids, int64_t n, const int8_t *Eq, const float *scale_e, int64_t V,
                               int64_t D, int block, uint16_t *out, unsigned *err, cudaStream_t st) {
     if (n == 0) return cudaSuccess;
+    if (lookup_wide_ok(Eq, D, out)) return launch_lookup_wide(ids, n, Eq, scale_e, V, D, block, out, err, st);
     const int64_t chunks = D / 8;
     int G, S;
     if (chunks <= kMaxThreads) {
@@ -559,16 +630,27 @@ cudaError_t launch_emb_lookup(const int64_t *ids, int64_t n, const int8_t *Eq, c
     }
     const int groups = G >= 256 ? 1 : 256 / G;
     const int threads = groups * G;
-    const unsigned grid = (unsigned)((n + groups - 1) / groups);
     const float inv_sqrt_b = (float)(1.0 / sqrt((double)block));
     const int lanes = lanes_of(block);
+    auto go = [&](auto kernel, int rpt) -> cudaError_t {
+        const int64_t per_cta = (int64_t)groups * rpt;
+        const int64_t nblocks = (n + per_cta - 1) / per_cta;
+        int dev = 0, sms = 0, per_sm = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+        if (e != cudaSuccess) return e;
+        const int64_t resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+        const int64_t grid = nblocks < resident ? nblocks : resident;
+        kernel<<<(unsigned)grid, threads, 0, st>>>(ids, n, Eq, scale_e, V, D, lanes, G, inv_sqrt_b, out, err);
+        return cudaGetLastError();
+    };
     switch (S) {
-        case 1: emb_lookup_kernel<1><<<grid, threads, 0, st>>>(ids, n, Eq, scale_e, V, D, lanes, G, inv_sqrt_b, out, err); break;
-        case 2: emb_lookup_kernel<2><<<grid, threads, 0, st>>>(ids, n, Eq, scale_e, V, D, lanes, G, inv_sqrt_b, out, err); break;
-        case 4: emb_lookup_kernel<4><<<grid, threads, 0, st>>>(ids, n, Eq, scale_e, V, D, lanes, G, inv_sqrt_b, out, err); break;
-        default: emb_lookup_kernel<8><<<grid, threads, 0, st>>>(ids, n, Eq, scale_e, V, D, lanes, G, inv_sqrt_b, out, err); break;
+        case 1: return go(emb_lookup_kernel<1, 4>, 4);
+        case 2: return go(emb_lookup_kernel<2, 2>, 2);
+        case 4: return go(emb_lookup_kernel<4, 1>, 1);
+        default: return go(emb_lookup_kernel<8, 1>, 1);
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_prep_transpose(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K, int block,

@@ -1,0 +1,379 @@
+// Row-wise kernels with 32 consecutive elements per thread: rotate + quantize
+// of bf16 rows (activations, gradients, weights, the embedding table) and the
+// quantized embedding lookup.
+//
+// Same arithmetic as the 8-element kernels in rotq.cu (the block-diagonal
+// normalised Sylvester-Hadamard rotation as a fast Walsh-Hadamard transform,
+// per-row absmax scale, codes by round-to-nearest-even; MOSS-Image LoRA
+// training guide, section 7.1, ConvRot INT8; sd-scripts PR #2461, Summary),
+// laid out for fewer instructions per element:
+//   - each thread loads its 32 elements with two coalesced 256-bit loads (a
+//     warp reads 2 KB of a row per pair of instructions);
+//   - butterfly stages h < min(b, 32) run inside the thread on packed fp32
+//     pairs, and only log2(b / 32) stages cross lanes (2 for b = 128, instead
+//     of 4 with 8 elements per thread), with the stage count fixed at compile
+//     time;
+//   - codes leave with one or two 256-bit stores per thread.
+// The kernels are persistent and prefetch the next rows' raw data while the
+// current ones are transformed.  Callers use them when the row length is a
+// multiple of 32 and the pointers and row strides allow 32-byte accesses;
+// rotq.cu covers the other cases.
+#include "common.cuh"
+#include "fwht.cuh"
+#include "internal.h"
+
+namespace convrot {
+namespace {
+
+constexpr int kThreads = 512;
+
+__device__ __forceinline__ void ld256(const void *p, uint32_t *r) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "l"(p));
+}
+
+__device__ __forceinline__ void st256(void *p, const uint32_t *r) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]),
+                 "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+// Walsh-Hadamard butterflies on blocks of 2^LOGB elements, 32 consecutive
+// elements per thread, blocks wider than 32 spread over 2^LOGB / 32
+// consecutive lanes.  (a, c) -> (a + c, a - c) on indices k and k ^ h gives the
+// Sylvester order H[i][j] = (-1)^popcount(i & j).
+template <int LOGB>
+__device__ __forceinline__ void fwht32(float (&e)[32], int lane) {
+    constexpr int B = 1 << LOGB;
+    constexpr int HMAX = B < 32 ? B : 32;
+    if constexpr (HMAX > 1) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            const float a = e[i], c = e[i + 1];
+            e[i] = a + c;
+            e[i + 1] = a - c;
+        }
+    }
+#pragma unroll
+    for (int h = 2; h < HMAX; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2)
+            if ((i & h) == 0) addsub2(e[i], e[i + 1], e[i + h], e[i + h + 1]);
+    }
+    constexpr int L = B / 32;
+#pragma unroll
+    for (int m = 1; m < L; m <<= 1) {
+        const float sg = (lane & m) ? -1.f : 1.f;
+#pragma unroll
+        for (int i0 = 0; i0 < 32; i0 += 8) {
+            float p[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) p[i] = __shfl_xor_sync(0xffffffffu, e[i0 + i], m);
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) sfma2(sg, e[i0 + i], e[i0 + i + 1], p[i], p[i + 1]);
+        }
+    }
+}
+
+__device__ __forceinline__ void unpack_bf16x32(const uint32_t (&w)[16], float (&e)[32]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        e[2 * i] = __uint_as_float(w[i] << 16);
+        e[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// 32 codes rne(e * inv) as fp16 values (64 bytes).
+__device__ __forceinline__ void store_codes32(float (&e)[32], float inv, __half *dst) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) mul2c(e[i], e[i + 1], inv);
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) add2c(e[i], e[i + 1], kMagicF16);
+    const __half2 k1152 = __half2half2(__ushort_as_half((unsigned short)0x6480));
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        uint32_t v = __byte_perm(__float_as_uint(e[2 * i]), __float_as_uint(e[2 * i + 1]), 0x5410);
+        __half2 h = __hsub2(*reinterpret_cast<__half2 *>(&v), k1152);
+        w[i] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    st256(dst, w);
+    st256(dst + 16, w + 8);
+}
+
+// 32 codes rne(e * inv) as int8 (32 bytes).
+__device__ __forceinline__ void store_codes32(float (&e)[32], float inv, int8_t *dst) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) mul2c(e[i], e[i + 1], inv);
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) add2c(e[i], e[i + 1], kMagicI8);
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t lo = __byte_perm(__float_as_uint(e[4 * k]), __float_as_uint(e[4 * k + 1]), 0x0040);
+        const uint32_t hi = __byte_perm(__float_as_uint(e[4 * k + 2]), __float_as_uint(e[4 * k + 3]), 0x0040);
+        w[k] = __byte_perm(lo, hi, 0x5410);
+    }
+    st256(dst, w);
+}
+
+__device__ __forceinline__ float amax32(const float (&e)[32]) {
+    float m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = fmaxf(fabsf(e[i]), fabsf(e[i + 8]));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = fmaxf(m[i], fmaxf(fabsf(e[i + 16]), fabsf(e[i + 24])));
+    return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+}
+
+struct WideArgs {
+    const uint16_t *x;
+    int64_t rows, K, ldx;
+    int G;              // threads per row (multiple of 32, <= 512)
+    float scale_denom;  // fp32(127 sqrt(b))
+    void *q;            // codes, row stride K
+    float *scale;
+};
+
+// One row per group of G threads, S slots of 32 elements per thread.
+template <typename OutT, int S, int LOGB>
+__global__ void __launch_bounds__(kThreads) rotq_wide_kernel(const WideArgs a) {
+    __shared__ float red[2][kThreads / 32];
+    const int G = a.G;
+    const int g = threadIdx.x / G;
+    const int t = threadIdx.x - g * G;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int groups = blockDim.x / G;
+    const int wpg = G >> 5;
+    const int64_t chunks = a.K >> 5;
+    const int64_t nblocks = (a.rows + groups - 1) / groups;
+
+    uint32_t raw[S][16];
+    auto fetch = [&](int64_t blk) {
+        const int64_t row = blk * groups + g;
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            const int64_t c = (int64_t)s * G + t;
+            if (c < chunks && row < a.rows) {
+                const uint16_t *p = a.x + row * a.ldx + 32 * c;
+                ld256(p, raw[s]);
+                ld256(p + 16, raw[s] + 8);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) raw[s][i] = 0u;
+            }
+        }
+    };
+
+    int par = 0;
+    int64_t blk = blockIdx.x;
+    if (blk < nblocks) fetch(blk);
+    for (; blk < nblocks; blk += gridDim.x, par ^= 1) {
+        const int64_t row = blk * groups + g;
+        float e[S][32];
+#pragma unroll
+        for (int s = 0; s < S; ++s) unpack_bf16x32(raw[s], e[s]);
+        if (blk + gridDim.x < nblocks) fetch(blk + gridDim.x);
+        float amax = 0.f;
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            fwht32<LOGB>(e[s], lane);
+            amax = fmaxf(amax, amax32(e[s]));
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
+        if (lane == 0) red[par][warp] = amax;
+        __syncthreads();
+        float m = 0.f;
+        for (int w = 0; w < wpg; ++w) m = fmaxf(m, red[par][g * wpg + w]);
+        if (row < a.rows) {
+            // fp32 decision on the fp32 transform; scale = amax_u / (127 sqrt(b)).
+            const float inv = m > 0.f ? __fdiv_rn(127.f, m) : 0.f;
+            if (t == 0) a.scale[row] = __fdiv_rn(m, a.scale_denom);
+            OutT *qrow = static_cast<OutT *>(a.q) + row * a.K;
+#pragma unroll
+            for (int s = 0; s < S; ++s) {
+                const int64_t c = (int64_t)s * G + t;
+                if (c < chunks) store_codes32(e[s], inv, qrow + 32 * c);
+            }
+        }
+    }
+}
+
+// out[t] = bf16((scale[id] * Eq[id,:]) R): the transform of the integer codes
+// is exact in fp32; one scaling after it.
+template <int S, int LOGB>
+__global__ void __launch_bounds__(kThreads) lookup_wide_kernel(const int64_t *ids, int64_t n, const int8_t *Eq,
+                                                               const float *scale_e, int64_t V, int64_t D, int G,
+                                                               float inv_sqrt_b, uint16_t *out, unsigned *err) {
+    const int g = threadIdx.x / G;
+    const int t = threadIdx.x - g * G;
+    const int lane = threadIdx.x & 31;
+    const int groups = blockDim.x / G;
+    const int64_t chunks = D >> 5;
+    const int64_t nblocks = (n + groups - 1) / groups;
+
+    uint32_t raw[S][8];
+    float sc = 0.f;
+    auto fetch = [&](int64_t blk) {
+        const int64_t tok = blk * groups + g;
+        int64_t id = -1;
+        if (tok < n) id = __ldg(ids + tok);
+        const bool ok = tok < n && id >= 0 && id < V;
+        if (tok < n && !ok && t == 0) atomicOr(err, DEVERR_INDEX);
+        sc = ok ? __ldg(scale_e + id) : 0.f;
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            const int64_t c = (int64_t)s * G + t;
+            if (ok && c < chunks) {
+                ld256(Eq + id * D + 32 * c, raw[s]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) raw[s][i] = 0u;
+            }
+        }
+    };
+
+    int64_t blk = blockIdx.x;
+    if (blk < nblocks) fetch(blk);
+    for (; blk < nblocks; blk += gridDim.x) {
+        const int64_t tok = blk * groups + g;
+        float e[S][32];
+#pragma unroll
+        for (int s = 0; s < S; ++s)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) e[s][i] = (float)(int8_t)((raw[s][i >> 2] >> (8 * (i & 3))) & 0xff);
+        const float s_cur = sc;
+        if (blk + gridDim.x < nblocks) fetch(blk + gridDim.x);
+#pragma unroll
+        for (int s = 0; s < S; ++s) fwht32<LOGB>(e[s], lane);
+        if (tok >= n) continue;
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            const int64_t c = (int64_t)s * G + t;
+            if (c >= chunks) continue;
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float y0 = __fmul_rn(__fmul_rn(e[s][2 * i], s_cur), inv_sqrt_b);
+                const float y1 = __fmul_rn(__fmul_rn(e[s][2 * i + 1], s_cur), inv_sqrt_b);
+                __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
+                w[i] = *reinterpret_cast<uint32_t *>(&h);
+            }
+            uint16_t *dst = out + tok * D + 32 * c;
+            st256(dst, w);
+            st256(dst + 16, w + 8);
+        }
+    }
+}
+
+int log2_of(int b) {
+    int l = 0;
+    while ((1 << l) < b) ++l;
+    return l;
+}
+
+void shape_for(int64_t len, int &G, int &S) {
+    const int64_t chunks = len / 32;
+    if (chunks <= kThreads) {
+        G = (int)((chunks + 31) / 32 * 32);
+        S = 1;
+    } else {
+        G = kThreads;
+        S = 2;
+    }
+}
+
+template <typename Kernel, typename... Args>
+cudaError_t launch_persistent(Kernel kernel, int threads, int64_t nblocks, cudaStream_t st, Args... args) {
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
+    if (e != cudaSuccess) return e;
+    const int64_t resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+    const int64_t grid = nblocks < resident ? nblocks : resident;
+    kernel<<<(unsigned)grid, threads, 0, st>>>(args...);
+    return cudaGetLastError();
+}
+
+template <typename OutT, int S>
+cudaError_t rotq_wide_dispatch(int logb, const WideArgs &a, int threads, int64_t nblocks, cudaStream_t st) {
+    switch (logb) {
+        case 3: return launch_persistent(rotq_wide_kernel<OutT, S, 3>, threads, nblocks, st, a);
+        case 4: return launch_persistent(rotq_wide_kernel<OutT, S, 4>, threads, nblocks, st, a);
+        case 5: return launch_persistent(rotq_wide_kernel<OutT, S, 5>, threads, nblocks, st, a);
+        case 6: return launch_persistent(rotq_wide_kernel<OutT, S, 6>, threads, nblocks, st, a);
+        case 7: return launch_persistent(rotq_wide_kernel<OutT, S, 7>, threads, nblocks, st, a);
+        default: return launch_persistent(rotq_wide_kernel<OutT, S, 8>, threads, nblocks, st, a);
+    }
+}
+
+template <int S>
+cudaError_t lookup_wide_dispatch(int logb, int threads, int64_t nblocks, cudaStream_t st, const int64_t *ids,
+                                 int64_t n, const int8_t *Eq, const float *scale_e, int64_t V, int64_t D, int G,
+                                 float inv_sqrt_b, uint16_t *out, unsigned *err) {
+    switch (logb) {
+        case 3: return launch_persistent(lookup_wide_kernel<S, 3>, threads, nblocks, st, ids, n, Eq, scale_e, V, D, G, inv_sqrt_b, out, err);
+        case 4: return launch_persistent(lookup_wide_kernel<S, 4>, threads, nblocks, st, ids, n, Eq, scale_e, V, D, G, inv_sqrt_b, out, err);
+        case 5: return launch_persistent(lookup_wide_kernel<S, 5>, threads, nblocks, st, ids, n, Eq, scale_e, V, D, G, inv_sqrt_b, out, err);
+        case 6: return launch_persistent(lookup_wide_kernel<S, 6>, threads, nblocks, st, ids, n, Eq, scale_e, V, D, G, inv_sqrt_b, out, err);
+        case 7: return launch_persistent(lookup_wide_kernel<S, 7>, threads, nblocks, st, ids, n, Eq, scale_e, V, D, G, inv_sqrt_b, out, err);
+        default: return launch_persistent(lookup_wide_kernel<S, 8>, threads, nblocks, st, ids, n, Eq, scale_e, V, D, G, inv_sqrt_b, out, err);
+    }
+}
+
+bool a32(const void *p) { return ((uintptr_t)p & 31u) == 0; }
+
+}  // namespace
+
+bool rotq_wide_ok(const void *x, int64_t K, int64_t ldx, const void *q) {
+    return K % 32 == 0 && K <= 32 * 2 * kThreads && ldx % 16 == 0 && a32(x) && a32(q);
+}
+
+cudaError_t launch_rotq_wide(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx, int block, bool out_f16, void *q,
+                             float *scale, cudaStream_t st) {
+    if (rows == 0) return cudaSuccess;
+    WideArgs a{};
+    a.x = x;
+    a.rows = rows;
+    a.K = K;
+    a.ldx = ldx;
+    a.scale_denom = (float)(127.0 * sqrt((double)block));
+    a.q = q;
+    a.scale = scale;
+    int G, S;
+    shape_for(K, G, S);
+    a.G = G;
+    const int groups = G >= kThreads ? 1 : kThreads / G;
+    const int threads = groups * G;
+    const int64_t nblocks = (rows + groups - 1) / groups;
+    const int logb = log2_of(block);
+    if (out_f16)
+        return S == 1 ? rotq_wide_dispatch<__half, 1>(logb, a, threads, nblocks, st)
+                      : rotq_wide_dispatch<__half, 2>(logb, a, threads, nblocks, st);
+    return S == 1 ? rotq_wide_dispatch<int8_t, 1>(logb, a, threads, nblocks, st)
+                  : rotq_wide_dispatch<int8_t, 2>(logb, a, threads, nblocks, st);
+}
+
+bool lookup_wide_ok(const void *Eq, int64_t D, const void *out) {
+    return D % 32 == 0 && D <= 32 * 2 * kThreads && a32(Eq) && a32(out);
+}
+
+cudaError_t launch_lookup_wide(const int64_t *ids, int64_t n, const int8_t *Eq, const float *scale_e, int64_t V,
+                               int64_t D, int block, uint16_t *out, unsigned *err, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    int G, S;
+    shape_for(D, G, S);
+    const int groups = G >= kThreads ? 1 : kThreads / G;
+    const int threads = groups * G;
+    const int64_t nblocks = (n + groups - 1) / groups;
+    const float inv_sqrt_b = (float)(1.0 / sqrt((double)block));
+    const int logb = log2_of(block);
+    return S == 1 ? lookup_wide_dispatch<1>(logb, threads, nblocks, st, ids, n, Eq, scale_e, V, D, G, inv_sqrt_b, out, err)
+                  : lookup_wide_dispatch<2>(logb, threads, nblocks, st, ids, n, Eq, scale_e, V, D, G, inv_sqrt_b, out, err);
+}
+
+}  // namespace convrot

@@ -268,3 +268,50 @@ def test_argument_errors_raise():
         cr.convrot_quantize_activation(x, 64)  # 96 is not a multiple of 64
     with pytest.raises(TypeError):
         cr.convrot_quantize_activation(x.float(), 32)
+
+
+# ------------------------------------------------------------------ both kernel layouts
+
+
+@pytest.mark.parametrize("K,block", [(48, 16), (80, 8), (272, 16)])
+def test_quantize_rows_not_multiple_of_32(K, block):
+    """Row lengths that are not a multiple of 32 take the 8-elements-per-thread kernel."""
+    M = 37
+    x = synth.activations_bf16(31, M, K, 3, 30.0)
+    q_ref, s_ref = oracle.quantize_rows_bf16(x, block)
+    xq, sx = cr.convrot_quantize_activation(torch_bf16(x), block)
+    check_codes(codes_of(xq), q_ref, f64(x), block)
+    check_scales(sx.cpu().numpy(), s_ref)
+    Wq, sw = cr.convrot_quantize_weight(torch_bf16(x), block)
+    check_codes(codes_of(Wq), q_ref, f64(x), block)
+
+
+def test_quantize_16_byte_aligned_input_takes_the_narrow_path():
+    """An input that is 16- but not 32-byte aligned (row stride 264) must give the same codes."""
+    N, K, ld, b = 21, 256, 264, 64
+    full = synth.normal_bf16(32, synth.STREAM_W, N, ld + 8, 0.02)
+    t = torch_bf16(full)
+    q_ref, s_ref = oracle.quantize_weight(np.ascontiguousarray(full[:, 8:8 + K]), b)
+    Wq = torch.empty((N, K), dtype=torch.int8, device="cuda")
+    sw = torch.empty((N,), dtype=torch.float32, device="cuda")
+    base = t.data_ptr() + 16  # column 8: 16-byte aligned, not 32
+    # rows of the view: stride ld + 8 elements
+    rc = cr.lib().convrot_quantize_weight(cr.ctypes.c_void_p(base), N, K, ld + 8, b, None, None, 0, 1.0, 1.0,
+                                          cr._ptr(Wq), cr._ptr(sw), cr._stream(None))
+    assert rc == cr.OK
+    check_codes(codes_of(Wq), q_ref, f64(full[:, 8:8 + K]), b)
+    check_scales(sw.cpu().numpy(), s_ref)
+
+
+@pytest.mark.parametrize("D,block", [(48, 16), (4096, 128), (512, 256)])
+def test_embedding_lookup_layouts(D, block):
+    V = 300
+    table = synth.normal_bf16(33, synth.STREAM_TABLE, V, D, 0.02)
+    eq, se = oracle.quantize_rows_bf16(table, block)
+    ids = synth.token_ids(33, 77, V)
+    ref, bad = oracle.embedding_lookup(ids, eq, se, block)
+    out = cr.convrot_embedding_lookup(torch.from_numpy(ids).cuda(), _i8(eq), _f32(se), block)
+    ob = bits_of(out)
+    assert rel_fro(f64(ob), f64(ref)) <= REL_FRO_ORACLE
+    assert np.mean(ob == ref) > 0.99
+    assert cr.convrot_get_error() == cr.OK
