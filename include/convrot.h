@@ -214,6 +214,13 @@ CONVROT_API size_t convrot_gemm_s32_workspace_bytes(int64_t M, int64_t K);
 CONVROT_API int convrot_gemm_s32(const int8_t *A, const int8_t *B, int64_t M, int64_t N, int64_t K,
                      int32_t *C, void *workspace, size_t ws_bytes, convrot_stream_t stream);
 
+/* Test entry for the failure path: launches one CTA that waits, with the same
+ * bounded mbarrier wait as the GEMM pipeline, on a barrier nothing arrives on.
+ * After `limit_ns` (1 ns .. 10 s) the wait gives up and records a timeout, so
+ * the next convrot_get_error() returns CONVROT_ERR_TIMEOUT and the context
+ * remains usable.  (The GEMM's own waits use a 2 s limit.) */
+CONVROT_API int convrot_selftest_wait_timeout(uint64_t limit_ns, convrot_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -60,6 +60,7 @@ def lib():
                 "convrot_gemm_s32": ([P, P, I64, I64, I64, P, P, S, P], I),
                 "convrot_linear_fwd_noalloc": ([P, I64, I64, P, P, I64, I, P, P, P], I),
                 "convrot_linear_fwd_noalloc_max_bytes": ([], S),
+                "convrot_selftest_wait_timeout": ([ctypes.c_uint64, P], I),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)

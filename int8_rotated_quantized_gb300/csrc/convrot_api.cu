@@ -230,4 +230,12 @@ int convrot_gemm_s32(const int8_t *A, const int8_t *B, int64_t M, int64_t N, int
     return cuda_status(convrot::launch_gemm(a16, nullptr, B, nullptr, nullptr, M, N, K, C, true, err, st));
 }
 
+int convrot_selftest_wait_timeout(uint64_t limit_ns, convrot_stream_t stream) {
+    CHECK(limit_ns > 0 && limit_ns <= 10000000000ull);
+    unsigned *err = nullptr;
+    int rc = device_setup(&err);
+    if (rc != CONVROT_OK) return rc;
+    return cuda_status(convrot::launch_wait_timeout(limit_ns, err, (cudaStream_t)stream));
+}
+
 }  // extern "C"

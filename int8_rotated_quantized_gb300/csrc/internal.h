@@ -36,4 +36,7 @@ cudaError_t launch_widen_i8(const int8_t *A, int64_t count, uint16_t *out, cudaS
 cudaError_t launch_gemm(const uint16_t *A, const float *sa, const int8_t *B, const float *sb, const uint16_t *bias,
                         int64_t M, int64_t N, int64_t K, void *out, bool out_s32, unsigned *err, cudaStream_t st);
 
+// Self-test of the bounded-wait failure path (selftest.cu).
+cudaError_t launch_wait_timeout(uint64_t limit_ns, unsigned *err, cudaStream_t st);
+
 }  // namespace convrot

@@ -1,0 +1,61 @@
+// mbarrier helpers with bounded waits, shared by the tensor-core GEMM and the
+// self-test of its timeout path.
+#pragma once
+
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace convrot {
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, 1000;\n selp.u32 %0, 1, 0, "
+        "p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on the phase with the given parity.  Each poll may suspend the
+// thread in hardware for up to 1 us (it wakes when the phase completes), so
+// waiting warps leave the issue slots and the shared-memory pipe to the
+// working ones; the abort flag and the clock are read every 64 polls.
+// Returns false if another role aborted or the wall-clock limit expired (then
+// the abort flag is set and the error word records a timeout).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *err,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((spin & 63) != 0) continue;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            atomicOr(err, DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Bounded wait that ignores the abort flag: used while draining in-flight work.
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) return;
+    }
+}
+
+}  // namespace convrot

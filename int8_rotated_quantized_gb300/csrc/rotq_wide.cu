@@ -138,7 +138,7 @@ struct WideArgs {
 
 // One row per group of G threads, S slots of 32 elements per thread.
 template <typename OutT, int S, int LOGB>
-__global__ void __launch_bounds__(kThreads) rotq_wide_kernel(const WideArgs a) {
+__global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) rotq_wide_kernel(const WideArgs a) {
     __shared__ float red[2][kThreads / 32];
     const int G = a.G;
     const int g = threadIdx.x / G;
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kThreads) rotq_wide_kernel(const WideArgs a) {
 // out[t] = bf16((scale[id] * Eq[id,:]) R): the transform of the integer codes
 // is exact in fp32; one scaling after it.
 template <int S, int LOGB>
-__global__ void __launch_bounds__(kThreads) lookup_wide_kernel(const int64_t *ids, int64_t n, const int8_t *Eq,
+__global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) lookup_wide_kernel(const int64_t *ids, int64_t n, const int8_t *Eq,
                                                                const float *scale_e, int64_t V, int64_t D, int G,
                                                                float inv_sqrt_b, uint16_t *out, unsigned *err) {
     const int g = threadIdx.x / G;

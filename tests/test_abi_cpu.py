@@ -27,7 +27,8 @@ def declared_symbols():
 def test_header_declares_the_boundary():
     names = declared_symbols()
     for must in ["convrot_quantize_weight", "convrot_linear_fwd", "convrot_linear_bwd_x", "convrot_embedding_lookup",
-                 "convrot_prepare_bwd_weight", "convrot_gemm_s32", "convrot_get_error", "convrot_status_string"]:
+                 "convrot_prepare_bwd_weight", "convrot_gemm_s32", "convrot_get_error", "convrot_status_string",
+                 "convrot_linear_fwd_noalloc", "convrot_selftest_wait_timeout"]:
         assert must in names
 
 
