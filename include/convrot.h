@@ -113,6 +113,7 @@ CONVROT_API int convrot_quantize_activation(const uint16_t *x, int64_t M, int64_
  *   y[m,n] = bf16_rne( float(acc[m,n]) * (scale_x[m] * scale_w[n]) + bias[n] ),
  *   acc[m,n] = sum_k xq[m,k] * Wq[n,k]   (exact integer sum, as int32)
  *   xq       [M, K] fp16-held codes (from convrot_quantize_activation).
+ *   scale_x  fp32 [M], 16-byte aligned.
  *   Wq       int8 [N, K]; scale_w fp32 [N]; bias bf16 [N] or NULL.
  *   y        out bf16 [M, N] contiguous.
  * K multiple of 16 and <= 2^20; N multiple of 16. */

@@ -134,7 +134,7 @@ int convrot_gemm_dequant(const uint16_t *xq, const float *scale_x, int64_t M, in
     CHECK(M <= INT32_MAX && N <= INT32_MAX);
     CHECK(M == 0 || N == 0 ||
           (xq && scale_x && Wq && scale_w && y && aligned16(xq) && aligned16(Wq) && aligned16(y) &&
-           aligned16(scale_w) && (bias == nullptr || aligned16(bias))));
+           aligned16(scale_x) && aligned16(scale_w) && (bias == nullptr || aligned16(bias))));
     unsigned *err = nullptr;
     int rc = device_setup(&err);
     if (rc != CONVROT_OK) return rc;

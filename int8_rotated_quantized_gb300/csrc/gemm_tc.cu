@@ -27,13 +27,16 @@
 //
 // CTA roles (512 threads, one persistent CTA per SM, 128 weight rows x 256
 // tokens per tile):
-//   warp 0        TMA producer (one lane)
+//   warp 0        TMA producer of the activation tiles (one lane)
 //   warp 1        TMEM allocator and MMA issuer (one lane)
-//   warps 2-3     idle (complete warpgroup 0 for setmaxnreg)
+//   warp 2        TMA producer of the weight tiles (one lane)
+//   warp 3        idle (completes warpgroup 0 for setmaxnreg)
 //   warps 4-7     int8 -> fp16 converters of the weight tiles
 //   warps 8-15    epilogue: TMEM -> registers, int32 accumulation, output
-// Pipelines: a 4-stage TMA ring (weight int8 8 KB + activation fp16 32 KB), a
-// 3-stage converted-weight ring (16 KB), and two 128x256 fp32 TMEM
+// Pipelines: a 4-stage activation ring (fp16 32 KB, refilled when the MMA
+// is done with a slot), a 6-stage int8 weight ring (8 KB, refilled when the
+// converters are done, so weight loads and their widening run ahead of the
+// MMA), a 3-stage converted-weight ring (16 KB), and two 128x256 fp32 TMEM
 // accumulators (512 columns) alternating per K chunk so the epilogue drains
 // one while the MMA fills the other.
 // Every wait is bounded: on expiry the kernel records DEVERR_TIMEOUT, lets
@@ -51,20 +54,21 @@ namespace convrot {
 namespace {
 
 constexpr int TW = 128, TT = 256, BK = 64;  // weight rows (MMA M), tokens (MMA N), K per stage
-constexpr int STAGES = 4, CSTAGES = 3;
+constexpr int XSTAGES = 4, WSTAGES = 6, CSTAGES = 3;
 constexpr int CHUNK_KB = 16;  // K blocks per exact fp32 chunk: 16 * 64 = 1024
 constexpr int NUM_THREADS = 512;
 constexpr int W8_STAGE = TW * BK;      // 8 KB int8 weight tile (TMA)
 constexpr int X_STAGE = TT * BK * 2;   // 32 KB fp16 activation tile (TMA)
 constexpr int WH_STAGE = TW * BK * 2;  // 16 KB widened weight tile
 constexpr int OFF_X = 0;
-constexpr int OFF_W8 = OFF_X + STAGES * X_STAGE;
-constexpr int OFF_WH = OFF_W8 + STAGES * W8_STAGE;
+constexpr int OFF_W8 = OFF_X + XSTAGES * X_STAGE;
+constexpr int OFF_WH = OFF_W8 + WSTAGES * W8_STAGE;
 constexpr int OFF_BAR = OFF_WH + CSTAGES * WH_STAGE;
 // Barrier indices.
-constexpr int BAR_TMA_FULL = 0, BAR_TMA_EMPTY = STAGES, BAR_CONV_FULL = 2 * STAGES,
-              BAR_CONV_EMPTY = 2 * STAGES + CSTAGES, BAR_ACC_FULL = 2 * STAGES + 2 * CSTAGES,
-              BAR_ACC_EMPTY = BAR_ACC_FULL + 2, BAR_DRAIN = BAR_ACC_EMPTY + 2, NUM_BARS = BAR_DRAIN + 1;
+constexpr int BAR_X_FULL = 0, BAR_X_EMPTY = XSTAGES, BAR_W_FULL = 2 * XSTAGES, BAR_W_EMPTY = BAR_W_FULL + WSTAGES,
+              BAR_CONV_FULL = BAR_W_EMPTY + WSTAGES, BAR_CONV_EMPTY = BAR_CONV_FULL + CSTAGES,
+              BAR_ACC_FULL = BAR_CONV_EMPTY + CSTAGES, BAR_ACC_EMPTY = BAR_ACC_FULL + 2, BAR_DRAIN = BAR_ACC_EMPTY + 2,
+              NUM_BARS = BAR_DRAIN + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -201,9 +205,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < STAGES; ++i) {
-            mbar_init(bar(BAR_TMA_FULL + i), 1);
-            mbar_init(bar(BAR_TMA_EMPTY + i), 1 + 4);  // MMA commit + 4 converter warps
+        for (int i = 0; i < XSTAGES; ++i) {
+            mbar_init(bar(BAR_X_FULL + i), 1);
+            mbar_init(bar(BAR_X_EMPTY + i), 1);  // MMA commit
+        }
+        for (int i = 0; i < WSTAGES; ++i) {
+            mbar_init(bar(BAR_W_FULL + i), 1);
+            mbar_init(bar(BAR_W_EMPTY + i), 4);  // 4 converter warps
         }
         for (int i = 0; i < CSTAGES; ++i) {
             mbar_init(bar(BAR_CONV_FULL + i), 4);
@@ -236,29 +244,39 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (warp < 4) {
         regs_dec<REGS_WG0>();
-        if (warp == 0 && lane == 0) {
-            // ---------------------------------------------------- producer
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmX) : "memory");
-            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
+        if ((warp == 0 || warp == 2) && lane == 0) {
+            // ---------------------------------------------------- producers
+            // warp 0 streams activation tiles (freed by the MMA), warp 2 the
+            // int8 weight tiles (freed by the converters), each in its own ring.
+            const bool is_x = warp == 0;
+            const int nst = is_x ? XSTAGES : WSTAGES;
+            const int full0 = is_x ? BAR_X_FULL : BAR_W_FULL;
+            const int empty0 = is_x ? BAR_X_EMPTY : BAR_W_EMPTY;
+            const CUtensorMap *map = is_x ? &tmX : &tmW;
+            asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
             int it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
                 int tb, wb;
                 tile_coords(tile, num_t, num_w, tb, wb);
                 for (int kb = 0; kb < num_kb; ++kb, ++it) {
-                    const int s = it % STAGES;
-                    if (!mbar_wait(bar(BAR_TMA_EMPTY + s), ((it / STAGES) & 1) ^ 1, abort_flag, p.err)) {
+                    const int s = it % nst;
+                    if (!mbar_wait(bar(empty0 + s), ((it / nst) & 1) ^ 1, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
-                    mbar_expect_tx(bar(BAR_TMA_FULL + s), X_STAGE + W8_STAGE);
-                    tma_load_2d(sX + s * X_STAGE, &tmX, bar(BAR_TMA_FULL + s), kb * BK, tb * TT);
-                    tma_load_2d(sW8 + s * W8_STAGE, &tmW, bar(BAR_TMA_FULL + s), kb * BK, wb * TW);
+                    if (is_x) {
+                        mbar_expect_tx(bar(full0 + s), X_STAGE);
+                        tma_load_2d(sX + s * X_STAGE, map, bar(full0 + s), kb * BK, tb * TT);
+                    } else {
+                        mbar_expect_tx(bar(full0 + s), W8_STAGE);
+                        tma_load_2d(sW8 + s * W8_STAGE, map, bar(full0 + s), kb * BK, wb * TW);
+                    }
                 }
             }
             if (!ok) {  // let the copies already issued land before the CTA exits
-                for (int j = it - 1; j >= 0 && j >= it - STAGES; --j)
-                    mbar_wait_drain(bar(BAR_TMA_FULL + j % STAGES), (j / STAGES) & 1);
+                for (int j = it - 1; j >= 0 && j >= it - nst; --j)
+                    mbar_wait_drain(bar(full0 + j % nst), (j / nst) & 1);
             }
         } else if (warp == 1 && lane == 0) {
             // --------------------------------------------------------- MMA
@@ -277,9 +295,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tc_fence_after();
                         dcol = (uint32_t)(buf * TT);
                     }
-                    const int s = it % STAGES;
+                    const int s = it % XSTAGES;
                     const int c = it % CSTAGES;
-                    if (!mbar_wait(bar(BAR_TMA_FULL + s), (it / STAGES) & 1, abort_flag, p.err) ||
+                    if (!mbar_wait(bar(BAR_X_FULL + s), (it / XSTAGES) & 1, abort_flag, p.err) ||
                         !mbar_wait(bar(BAR_CONV_FULL + c), (it / CSTAGES) & 1, abort_flag, p.err)) {
                         ok = false;
                         break;
@@ -291,7 +309,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint64_t bd = sw128_desc(sX + s * X_STAGE + kk * 32);
                         umma_f16(tmem + dcol, ad, bd, (kc > 0 || kk > 0) ? 1u : 0u);
                     }
-                    umma_commit(bar(BAR_TMA_EMPTY + s));
+                    umma_commit(bar(BAR_X_EMPTY + s));
                     umma_commit(bar(BAR_CONV_EMPTY + c));
                     if (kc == CHUNK_KB - 1 || kb == num_kb - 1) {
                         umma_commit(bar(BAR_ACC_FULL + (g & 1)));
@@ -317,9 +335,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
             for (int kb = 0; kb < num_kb; ++kb, ++it) {
-                const int s = it % STAGES;
+                const int s = it % WSTAGES;
                 const int c = it % CSTAGES;
-                if (!warp_wait(bar(BAR_TMA_FULL + s), (it / STAGES) & 1, abort_flag, p.err, lane) ||
+                if (!warp_wait(bar(BAR_W_FULL + s), (it / WSTAGES) & 1, abort_flag, p.err, lane) ||
                     !warp_wait(bar(BAR_CONV_EMPTY + c), ((it / CSTAGES) & 1) ^ 1, abort_flag, p.err, lane)) {
                     ok = false;
                     break;
@@ -352,7 +370,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(bar(BAR_TMA_EMPTY + s));
+                    mbar_arrive(bar(BAR_W_EMPTY + s));
                     mbar_arrive(bar(BAR_CONV_FULL + c));
                 }
             }
@@ -397,23 +415,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // store instruction of the warp writes 32 consecutive n of one row m.
             const int n = wb * TW + 32 * q + lane;
             const int m0 = tb * TT + h * 128;
+            const int mlim = p.M - m0;  // tokens of this column half that exist
+            const bool full = mlim >= 128;
             if (n < p.N) {
                 if constexpr (OUT_S32) {
-                    int32_t *out = static_cast<int32_t *>(p.out) + n;
-#pragma unroll
-                    for (int i = 0; i < 128; ++i)
-                        if (m0 + i < p.M) out[(int64_t)(m0 + i) * p.N] = acc[i];
-                } else {
-                    uint16_t *out = static_cast<uint16_t *>(p.out) + n;
-                    const float swn = __ldg(p.sb + n);
-                    const float bn = p.bias != nullptr ? bf16_bits_to_float(__ldg(p.bias + n)) : 0.f;
+                    int32_t *out = static_cast<int32_t *>(p.out) + (int64_t)m0 * p.N + n;
 #pragma unroll
                     for (int i = 0; i < 128; ++i) {
-                        const int m = m0 + i;
-                        if (m < p.M) {
-                            float y = __fmul_rn(__int2float_rn(acc[i]), __fmul_rn(__ldg(p.sa + m), swn));
-                            if (p.bias != nullptr) y = __fadd_rn(y, bn);
-                            out[(int64_t)m * p.N] = (uint16_t)float_to_bf16_bits(y);
+                        if (full || i < mlim) *out = acc[i];
+                        out += p.N;
+                    }
+                } else {
+                    uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)m0 * p.N + n;
+                    const float swn = __ldg(p.sb + n);
+                    const bool has_bias = p.bias != nullptr;
+                    const float bn = has_bias ? bf16_bits_to_float(__ldg(p.bias + n)) : 0.f;
+#pragma unroll
+                    for (int i4 = 0; i4 < 128; i4 += 4) {
+                        float sx[4];
+                        if (full) {
+                            const float4 v = __ldg(reinterpret_cast<const float4 *>(p.sa + m0 + i4));
+                            sx[0] = v.x, sx[1] = v.y, sx[2] = v.z, sx[3] = v.w;
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) sx[j] = i4 + j < mlim ? __ldg(p.sa + m0 + i4 + j) : 0.f;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            float y = __fmul_rn(__int2float_rn(acc[i4 + j]), __fmul_rn(sx[j], swn));
+                            if (has_bias) y = __fadd_rn(y, bn);
+                            if (full || i4 + j < mlim) *out = (uint16_t)float_to_bf16_bits(y);
+                            out += p.N;
                         }
                     }
                 }
