@@ -165,7 +165,7 @@ CONVROT_API size_t convrot_linear_fwd_noalloc_max_bytes(void);
 
 /* -------------------------------------------------------- frozen backward -- */
 
-/* Bytes of workspace convrot_prepare_bwd_weight needs ([K, N] fp64). */
+/* Bytes of workspace convrot_prepare_bwd_weight needs ([K, N] pairs of fp32). */
 CONVROT_API size_t convrot_bwd_weight_workspace_bytes(int64_t N, int64_t K);
 
 /* One-off preparation of the int8 backward weight (guide 7.1 and 4.1: the
@@ -173,7 +173,8 @@ CONVROT_API size_t convrot_bwd_weight_workspace_bytes(int64_t N, int64_t K);
  * GEMM as the forward; PR #2461 Summary: the base is frozen, so only grad_x).  The GEMM is reused
  * unchanged, so its weight operand must be a ConvRot quantization along the
  * new contraction dimension N:
- *   W_eff    = (scale_w (.) Wq) R      (the dequantized base in the original basis, fp64)
+ *   W_eff    = (scale_w (.) Wq) R      (the dequantized base in the original basis, kept as
+ *              double-float pairs, ~48 significant bits)
  *   WtQ      out int8 [K, N]: codes of the rows of W_eff^T rotated along N
  *   scale_wt out fp32 [K]
  * N and K multiples of block and of 16; workspace >= convrot_bwd_weight_workspace_bytes. */

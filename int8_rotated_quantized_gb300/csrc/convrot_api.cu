@@ -170,7 +170,7 @@ int convrot_linear_fwd(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq
 
 size_t convrot_bwd_weight_workspace_bytes(int64_t N, int64_t K) {
     if (N < 0 || K < 0) return 0;
-    return align256((size_t)N * (size_t)K * sizeof(double));
+    return align256((size_t)N * (size_t)K * 2 * sizeof(float));
 }
 
 int convrot_prepare_bwd_weight(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K, int block, int8_t *WtQ,
@@ -182,11 +182,8 @@ int convrot_prepare_bwd_weight(const int8_t *Wq, const float *scale_w, int64_t N
     unsigned *err = nullptr;
     int rc = device_setup(&err);
     if (rc != CONVROT_OK) return rc;
-    cudaStream_t st = (cudaStream_t)stream;
-    double *T = static_cast<double *>(workspace);
-    rc = cuda_status(convrot::launch_bwd_prep_transpose(Wq, scale_w, N, K, block, T, st));
-    if (rc != CONVROT_OK) return rc;
-    return cuda_status(convrot::launch_rotq_f64(T, K, N, block, WtQ, scale_wt, st));
+    return cuda_status(
+        convrot::launch_bwd_prep_df(Wq, scale_w, N, K, block, workspace, WtQ, scale_wt, (cudaStream_t)stream));
 }
 
 int convrot_linear_bwd_x(const uint16_t *dY, int64_t M, int64_t N, const int8_t *WtQ, const float *scale_wt,

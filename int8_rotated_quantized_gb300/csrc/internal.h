@@ -19,14 +19,13 @@ bool lookup_wide_ok(const void *Eq, int64_t D, const void *out);
 cudaError_t launch_lookup_wide(const int64_t *ids, int64_t n, const int8_t *Eq, const float *scale_e, int64_t V,
                                int64_t D, int block, uint16_t *out, unsigned *err, cudaStream_t st);
 
-cudaError_t launch_rotq_f64(const double *x, int64_t rows, int64_t K, int block, int8_t *q, float *scale,
-                            cudaStream_t st);
 
 cudaError_t launch_emb_lookup(const int64_t *ids, int64_t n, const int8_t *Eq, const float *scale_e, int64_t V,
                               int64_t D, int block, uint16_t *out, unsigned *err, cudaStream_t st);
 
-cudaError_t launch_bwd_prep_transpose(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K, int block,
-                                      double *T, cudaStream_t st);
+// One-off int8 backward weight (bwd_prep.cu); `work` holds K * N pairs of fp32.
+cudaError_t launch_bwd_prep_df(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K, int block, void *work,
+                               int8_t *WtQ, float *scale_wt, cudaStream_t st);
 
 cudaError_t launch_widen_i8(const int8_t *A, int64_t count, uint16_t *out, cudaStream_t st);
 

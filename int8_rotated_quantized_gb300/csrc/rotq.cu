@@ -1,6 +1,9 @@
-// Row-wise kernels of libconvrot: rotate + quantize (weights, activations,
-// gradients, embedding table), quantized embedding lookup, and the one-off
-// preparation of the int8 backward weight.
+// Row-wise kernels of libconvrot with 8 elements per thread: rotate +
+// quantize (the LoRA-merging weight quantizer, and rows that the 32-element
+// kernels of rotq_wide.cu cannot take: lengths that are not a multiple of 32
+// or pointers that are only 16-byte aligned) and the quantized embedding
+// lookup for such tables.  The launchers here dispatch to rotq_wide.cu when
+// its conditions hold.
 //
 // The rotation is the block-diagonal normalised Sylvester-Hadamard matrix
 // R = I (x) H_b / sqrt(b) (MOSS-Image LoRA training guide, section 7.1,
@@ -39,20 +42,8 @@ __device__ __forceinline__ void load8(const uint16_t *p, float (&e)[8]) {
     }
 }
 
-__device__ __forceinline__ void load8(const double *p, double (&e)[8]) {
-    const double2 *q = reinterpret_cast<const double2 *>(p);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        double2 v = __ldcs(q + i);
-        e[2 * i] = v.x;
-        e[2 * i + 1] = v.y;
-    }
-}
-
 __device__ __forceinline__ float absv(float v) { return fabsf(v); }
-__device__ __forceinline__ double absv(double v) { return fabs(v); }
 __device__ __forceinline__ float maxv(float a, float b) { return fmaxf(a, b); }
-__device__ __forceinline__ double maxv(double a, double b) { return fmax(a, b); }
 
 template <typename CT>
 __device__ __forceinline__ void zero8(CT (&e)[8]) {
@@ -217,30 +208,8 @@ struct Raw8<uint16_t> {
         }
     }
 };
-template <>
-struct Raw8<double> {
-    double v[8];
-    __device__ __forceinline__ void load(const double *p) {
-        const double2 *q = reinterpret_cast<const double2 *>(p);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const double2 d = __ldcs(q + i);
-            v[2 * i] = d.x;
-            v[2 * i + 1] = d.y;
-        }
-    }
-    __device__ __forceinline__ void zero() {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = 0.0;
-    }
-    __device__ __forceinline__ void unpack(double (&e)[8]) const {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) e[i] = v[i];
-    }
-};
-
-// InT: element type of x (uint16_t = bf16 bits, or double).  CT: arithmetic
-// type of the transform.  OutT: int8_t codes or __half-held codes.  S: 8-element
+// InT: element type of x (uint16_t = bf16 bits).  CT: arithmetic type of the
+// transform (float).  OutT: int8_t codes or __half-held codes.  S: 8-element
 // slots per thread.  RPT: rows held per thread group at once.  LORA: merge
 // W + coef * B@A (fp32, sequential fma over the rank, rounded to bf16) first.
 //
@@ -512,53 +481,6 @@ __global__ void __launch_bounds__(kMaxThreads) emb_lookup_kernel(const int64_t *
     }
 }
 
-// ------------------------------------------------------ int8 bwd weight prep --
-
-// T[k][n] = (scale_w[n] * (H_b q_n)[k]) / sqrt(b) in fp64: the dequantized base
-// rotated back to the original basis, written transposed.  A CTA covers 16
-// weight rows and one Hadamard block of b columns.
-constexpr int kPrepRows = 16;
-
-__global__ void __launch_bounds__(256) bwd_prep_transpose_kernel(const int8_t *Wq, const float *scale_w, int64_t N,
-                                                                 int64_t K, int b, double rsqrt_b, double *T) {
-    extern __shared__ double tile[];  // [b][kPrepRows]
-    const int lanes = b >> 3;
-    const int64_t n0 = (int64_t)blockIdx.x * kPrepRows;
-    const int64_t k0 = (int64_t)blockIdx.y * b;
-    const int total = kPrepRows * lanes;
-    const int lane = threadIdx.x & 31;
-    for (int j0 = 0; j0 < total; j0 += blockDim.x) {
-        const int j = j0 + threadIdx.x;
-        if (j0 + (threadIdx.x & ~31) >= total) break;  // warp-uniform
-        const bool valid = j < total;
-        const int rl = valid ? j / lanes : 0;
-        const int cb = valid ? j - rl * lanes : 0;
-        const int64_t n = n0 + rl;
-        double e[8];
-        if (valid && n < N) {
-            uint2 v = __ldg(reinterpret_cast<const uint2 *>(Wq + n * K + k0 + 8 * cb));
-            uint32_t w[2] = {v.x, v.y};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) e[i] = (double)(int8_t)((w[i >> 2] >> (8 * (i & 3))) & 0xff);
-        } else {
-            zero8(e);
-        }
-        fwht8(e);
-        fwht_lanes(e, lanes, lane);
-        const double s = (valid && n < N) ? (double)__ldg(scale_w + n) : 0.0;
-        if (valid) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) tile[(8 * cb + i) * kPrepRows + rl] = (s * e[i]) * rsqrt_b;
-        }
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < b * kPrepRows; idx += blockDim.x) {
-        const int kl = idx / kPrepRows;
-        const int rl = idx - kl * kPrepRows;
-        if (n0 + rl < N) T[(k0 + kl) * N + n0 + rl] = tile[idx];
-    }
-}
-
 __global__ void widen_i8_kernel(const int8_t *A, int64_t count8, __half *out) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count8; i += (int64_t)gridDim.x * blockDim.x) {
         uint2 v = __ldg(reinterpret_cast<const uint2 *>(A) + i);
@@ -599,21 +521,6 @@ cudaError_t launch_rotq_bf16(const uint16_t *x, int64_t rows, int64_t K, int64_t
     return launch_rotq_t<uint16_t, float, int8_t, false>(a, rows, K, st);
 }
 
-cudaError_t launch_rotq_f64(const double *x, int64_t rows, int64_t K, int block, int8_t *q, float *scale,
-                            cudaStream_t st) {
-    if (rows == 0) return cudaSuccess;
-    RotqArgs a{};
-    a.x = x;
-    a.rows = rows;
-    a.K = K;
-    a.ldx = K;
-    a.lanes = lanes_of(block);
-    a.scale_coef = 1.0 / (127.0 * sqrt((double)block));
-    a.q = q;
-    a.scale = scale;
-    return launch_rotq_t<double, double, int8_t, false>(a, rows, K, st);
-}
-
 cudaError_t launch_emb_lookup(const int64_t *ids, int64_t n, const int8_t *Eq, const float *scale_e, int64_t V,
                               int64_t D, int block, uint16_t *out, unsigned *err, cudaStream_t st) {
     if (n == 0) return cudaSuccess;
@@ -651,18 +558,6 @@ cudaError_t launch_emb_lookup(const int64_t *ids, int64_t n, const int8_t *Eq, c
         case 4: return go(emb_lookup_kernel<4, 1>, 1);
         default: return go(emb_lookup_kernel<8, 1>, 1);
     }
-}
-
-cudaError_t launch_bwd_prep_transpose(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K, int block,
-                                      double *T, cudaStream_t st) {
-    if (N == 0 || K == 0) return cudaSuccess;
-    const size_t smem = sizeof(double) * (size_t)block * kPrepRows;
-    cudaError_t e = cudaFuncSetAttribute(bwd_prep_transpose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(sizeof(double) * 256 * kPrepRows));
-    if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)((N + kPrepRows - 1) / kPrepRows), (unsigned)(K / block));
-    bwd_prep_transpose_kernel<<<grid, 256, smem, st>>>(Wq, scale_w, N, K, block, 1.0 / sqrt((double)block), T);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_widen_i8(const int8_t *A, int64_t count, uint16_t *out, cudaStream_t st) {
