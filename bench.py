@@ -35,6 +35,27 @@ WORKLOAD = ("train20k: packed 20k-token training step of one ConvRot INT8 linear
             "int8 grad_x GEMM -> dX")
 L2_FLUSH_BYTES = 256 << 20
 
+# DRAM bytes (read + write) per launch of gemm_s8_tc_kernel, from one-pass ncu
+# captures (dram__bytes_read.sum + dram__bytes_write.sum) of
+#   python -m int8_rotated_quantized_gb300.profile_case gemm --M 20480 --N 16384 --K 4096 --reps 1   (forward shape)
+#   python -m int8_rotated_quantized_gb300.profile_case gemm --M 20480 --N 4096 --K 16384 --reps 1   (grad_x shape)
+# keyed by the hash of the kernel source they were taken on; reported as null
+# once the kernel source differs.
+GEMM_TRAFFIC = {"source_sha256_16": "9bef5bba02530c86", "fwd": 417522176 + 647178496, "bwd": 1972629760 + 162354688}
+
+
+def gemm_traffic_per_launch():
+    import hashlib
+    path = os.path.join(ROOT, "int8_rotated_quantized_gb300", "csrc", "gemm_tc.cu")
+    try:
+        with open(path, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    except OSError:
+        return None
+    if sha != GEMM_TRAFFIC["source_sha256_16"]:
+        return None
+    return (GEMM_TRAFFIC["fwd"] + GEMM_TRAFFIC["bwd"]) // 2
+
 
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -233,7 +254,9 @@ def run_gpu(args):
                 "frac": round(gemm_tflops / pk["bf16"], 4),
                 "peak_note": f"{pk['source']} dense bf16 burst (the kind::f16 MMA that carries the int8 codes runs at the "
                              "bf16/fp16 rate; tcgen05 kind::i8 does not exist on sm_103a)",
-                "traffic": None,
+                "traffic": gemm_traffic_per_launch(),
+                "traffic_note": "mean DRAM bytes per launch over the forward and grad_x shapes (ncu, one pass); "
+                                "algorithmic bytes per launch 906117120 for both",
             },
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -453,7 +476,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["convrot", "reference"], default="convrot")
-    ap.add_argument("--cpu-rows", type=int, default=512, help="token rows in the CPU-oracle sample")
+    ap.add_argument("--cpu-rows", type=int, default=4096, help="token rows in the CPU-oracle sample")
     ap.add_argument("--ref-rows", type=int, default=64, help="token rows per step of --impl reference")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-kernel rows")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")

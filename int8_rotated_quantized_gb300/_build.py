@@ -15,8 +15,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libconvrot.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["rotq.cu", "rotq_wide.cu", "bwd_prep.cu", "gemm_tc.cu", "convrot_api.cu", "noalloc.cu", "selftest.cu"]
-HEADERS = ["common.cuh", "fwht.cuh", "mbar.cuh", "internal.h"]
+SOURCES = ["rotq.cu", "rotq_wide.cu", "lora_rotq.cu", "bwd_prep.cu", "gemm_tc.cu", "convrot_api.cu", "noalloc.cu", "selftest.cu"]
+HEADERS = ["common.cuh", "fwht.cuh", "mbar.cuh", "wide.cuh", "internal.h"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

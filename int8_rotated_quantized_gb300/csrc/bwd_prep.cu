@@ -63,7 +63,9 @@ constexpr int kThreads = 512;
 // T[k][n] = (scale_w[n] * (H_b q_n)[k]) / sqrt(b) as (hi, lo).
 __global__ void __launch_bounds__(256) prep_transpose_df_kernel(const int8_t *Wq, const float *scale_w, int64_t N,
                                                                 int64_t K, int b, float ch, float cl, float2 *T) {
-    extern __shared__ float2 tile[];  // [b][kPrepRows]
+    // [b][kPrepRows]; the row slot is xor-swizzled with the 8-column group so
+    // that the 16 lanes writing one row land in 16 distinct bank pairs.
+    extern __shared__ float2 tile[];
     const int lanes = b >> 3;
     const int64_t n0 = (int64_t)blockIdx.x * kPrepRows;
     const int64_t k0 = (int64_t)blockIdx.y * b;
@@ -113,7 +115,7 @@ __global__ void __launch_bounds__(256) prep_transpose_df_kernel(const int8_t *Wq
                 const float pe = __fmaf_rn(s, e[i], -p);
                 float rh, rlo;
                 df_mul(p, pe, ch, cl, rh, rlo);
-                tile[(8 * cb + i) * kPrepRows + rl] = make_float2(rh, rlo);
+                tile[(8 * cb + i) * kPrepRows + (rl ^ (cb & (kPrepRows - 1)))] = make_float2(rh, rlo);
             }
         }
     }
@@ -121,7 +123,7 @@ __global__ void __launch_bounds__(256) prep_transpose_df_kernel(const int8_t *Wq
     for (int idx = threadIdx.x; idx < b * kPrepRows; idx += blockDim.x) {
         const int kl = idx / kPrepRows;
         const int rl = idx - kl * kPrepRows;
-        if (n0 + rl < N) T[(k0 + kl) * N + n0 + rl] = tile[idx];
+        if (n0 + rl < N) T[(k0 + kl) * N + n0 + rl] = tile[kl * kPrepRows + (rl ^ ((kl >> 3) & (kPrepRows - 1)))];
     }
 }
 

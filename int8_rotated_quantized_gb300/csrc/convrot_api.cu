@@ -112,6 +112,9 @@ int convrot_quantize_weight(const uint16_t *W, int64_t N, int64_t K, int64_t ldw
     if (rc != CONVROT_OK) return rc;
     if (N == 0) return CONVROT_OK;
     const float coef = lora_A ? (float)((double)scale * (double)alpha / (double)rank) : 0.f;
+    if (lora_A && convrot::lora_cluster_ok(W, K, ldw, block, lora_A, rank, Wq))
+        return cuda_status(convrot::launch_lora_cluster(W, N, K, ldw, block, lora_A, lora_B, rank, coef, Wq, scale_w,
+                                                        err, (cudaStream_t)stream));
     return cuda_status(convrot::launch_rotq_bf16(W, N, K, ldw, block, lora_A, lora_B, lora_A ? rank : 0, coef, false,
                                                  Wq, scale_w, (cudaStream_t)stream));
 }

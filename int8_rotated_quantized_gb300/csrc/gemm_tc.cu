@@ -44,6 +44,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -82,6 +83,8 @@ constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(TT 
 
 struct GemmArgs {
     int M, N, K;
+    int group;         // tiles per raster group along the grouped dimension
+    int group_weight;  // 1: groups of weight tiles sweep the token tiles; 0: the reverse
     const float *sa, *sb;
     const uint16_t *bias;
     void *out;
@@ -149,17 +152,24 @@ __device__ __forceinline__ void regs_inc() {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
-// Grouped raster: 8 M-blocks per group so the CTAs in flight share A and B
-// tiles in L2.
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int &mb, int &nb) {
-    constexpr int GM = 8;
-    const int group_size = GM * num_n;
-    const int group = tile / group_size;
-    const int first_m = group * GM;
-    const int gm = min(num_m - first_m, GM);
-    const int in_group = tile - group * group_size;
-    mb = first_m + in_group % gm;
-    nb = in_group / gm;
+// Grouped raster.  A group of `group` tiles along one dimension sweeps every
+// tile of the other dimension, so the group's operand tiles stay in L2 while
+// the other operand streams through once per group; odd groups sweep
+// backwards and start on the tiles their predecessor read last.  The host
+// picks the grouped dimension and the group size from the operand sizes.
+__device__ __forceinline__ void tile_coords(int tile, int num_t, int num_w, int group, bool group_weight, int &tb,
+                                            int &wb) {
+    const int num_g = group_weight ? num_w : num_t;  // grouped dimension
+    const int num_s = group_weight ? num_t : num_w;  // swept dimension
+    const int gi = tile / (group * num_s);
+    const int first = gi * group;
+    const int gsize = min(num_g - first, group);
+    const int in_group = tile - gi * group * num_s;
+    const int g = first + in_group % gsize;
+    int sw = in_group / gsize;
+    if (gi & 1) sw = num_s - 1 - sw;
+    tb = group_weight ? sw : g;
+    wb = group_weight ? g : sw;
 }
 
 // int8 x 4 -> two fp16x2 words holding the same integers: bias each byte by
@@ -258,7 +268,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
                 int tb, wb;
-                tile_coords(tile, num_t, num_w, tb, wb);
+                tile_coords(tile, num_t, num_w, p.group, p.group_weight != 0, tb, wb);
                 for (int kb = 0; kb < num_kb; ++kb, ++it) {
                     const int s = it % nst;
                     if (!mbar_wait(bar(empty0 + s), ((it / nst) & 1) ^ 1, abort_flag, p.err)) {
@@ -385,7 +395,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
             int tb, wb;
-            tile_coords(tile, num_t, num_w, tb, wb);
+            tile_coords(tile, num_t, num_w, p.group, p.group_weight != 0, tb, wb);
             int acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0;
@@ -494,6 +504,24 @@ int sm_count_of_current_device() {
     return cached[dev];
 }
 
+// Raster choice.  The tiles of the grouped dimension are read from DRAM once
+// if `group` of them (plus the streaming tiles of one wave) stay in L2; the
+// swept operand is then read once per group.  Measured on GB300, groups whose
+// tiles total more than about 32 MB no longer stay resident, so the group is
+// the largest count of tiles within that budget, and the orientation with the
+// smaller estimated DRAM read volume wins.
+constexpr int64_t kRasterBudget = 32ll << 20;
+
+void choose_raster(int64_t num_t, int64_t num_w, int64_t K, int &group, int &group_weight) {
+    const int64_t t_tile = (int64_t)TT * K * 2, w_tile = (int64_t)TW * K;  // fp16 codes, int8 codes
+    const int64_t gt = std::max<int64_t>(1, std::min<int64_t>(num_t, kRasterBudget / t_tile));
+    const int64_t gw = std::max<int64_t>(1, std::min<int64_t>(num_w, kRasterBudget / w_tile));
+    const int64_t reads_t = num_t * t_tile + num_w * w_tile * ((num_t + gt - 1) / gt);
+    const int64_t reads_w = num_w * w_tile + num_t * t_tile * ((num_w + gw - 1) / gw);
+    group_weight = reads_w < reads_t ? 1 : 0;
+    group = (int)(group_weight ? gw : gt);
+}
+
 }  // namespace
 
 cudaError_t launch_gemm(const uint16_t *A, const float *sa, const int8_t *B, const float *sb, const uint16_t *bias,
@@ -507,8 +535,11 @@ cudaError_t launch_gemm(const uint16_t *A, const float *sa, const int8_t *B, con
         !encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, (uint64_t)K, (uint64_t)N, BK, TW,
                    CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    GemmArgs p{(int)M, (int)N, (int)K, sa, sb, bias, out, err};
-    const int64_t tiles = ((M + TT - 1) / TT) * ((N + TW - 1) / TW);
+    const int64_t num_t = (M + TT - 1) / TT, num_w = (N + TW - 1) / TW;
+    int group, group_weight;
+    choose_raster(num_t, num_w, K, group, group_weight);
+    GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, sa, sb, bias, out, err};
+    const int64_t tiles = num_t * num_w;
     const int sms = sm_count_of_current_device();
     const int grid = (int)(tiles < sms ? tiles : sms);
     if (out_s32) {

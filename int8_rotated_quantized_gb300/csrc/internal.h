@@ -15,6 +15,12 @@ cudaError_t launch_rotq_bf16(const uint16_t *x, int64_t rows, int64_t K, int64_t
 bool rotq_wide_ok(const void *x, int64_t K, int64_t ldx, const void *q);
 cudaError_t launch_rotq_wide(const uint16_t *x, int64_t rows, int64_t K, int64_t ldx, int block, bool out_f16, void *q,
                              float *scale, cudaStream_t st);
+// Fused LoRA merge + rotate + quantize with rows split along K over a cluster
+// (lora_rotq.cu): rank <= 16, K = (2 to 8 CTAs or 1) x a power-of-two slice.
+bool lora_cluster_ok(const void *W, int64_t K, int64_t ldw, int block, const float *A, int rank, const void *q);
+cudaError_t launch_lora_cluster(const uint16_t *W, int64_t rows, int64_t K, int64_t ldw, int block, const float *A,
+                                const float *B, int rank, float coef, int8_t *q, float *scale, unsigned *err,
+                                cudaStream_t st);
 bool lookup_wide_ok(const void *Eq, int64_t D, const void *out);
 cudaError_t launch_lookup_wide(const int64_t *ids, int64_t n, const int8_t *Eq, const float *scale_e, int64_t V,
                                int64_t D, int block, uint16_t *out, unsigned *err, cudaStream_t st);

@@ -127,12 +127,17 @@ def test_quantize_weight_with_row_stride():
     check_scales(sw.cpu().numpy(), s_ref)
 
 
-@pytest.mark.parametrize("N,K,rank", [(96, 512, 16), (50, 4096, 16), (33, 1024, 3)])
-def test_quantize_weight_lora_merge_parity(N, K, rank):
+# Cases of the cluster kernel (rank <= 16 padded to 4, 8 or 16; K split into
+# power-of-two slices over 1 to 8 CTAs: 512x1, 512x8, 512x2, 512x6, 512x5,
+# 2048x6 with 512 threads, 128x3 with one warp; ragged row tiles) and of the
+# row kernel it falls back to (rank 24; K = 96).
+@pytest.mark.parametrize("N,K,rank,block", [(96, 512, 16, 128), (50, 4096, 16, 128), (33, 1024, 3, 128),
+                                            (41, 3072, 16, 128), (23, 2560, 7, 64), (9, 12288, 16, 256),
+                                            (20, 384, 5, 128), (30, 256, 24, 32), (17, 96, 4, 32)])
+def test_quantize_weight_lora_merge_parity(N, K, rank, block):
     W = synth.normal_bf16(6, synth.STREAM_W, N, K, 0.02)
     A, B = synth.lora_pair(6, N, K, rank, 0.01)
-    q_ref, s_ref = oracle.quantize_weight(W, 128 if K % 128 == 0 else 32, A, B, 16.0, 1.0)
-    block = 128 if K % 128 == 0 else 32
+    q_ref, s_ref = oracle.quantize_weight(W, block, A, B, 16.0, 1.0)
     Wq, sw = cr.convrot_quantize_weight(torch_bf16(W), block, _f32(A), _f32(B), 16.0, 1.0)
     merged = oracle.lora_merge(W, A, B, 16.0, 1.0)
     check_codes(codes_of(Wq), q_ref, f64(merged), block)
@@ -141,6 +146,22 @@ def test_quantize_weight_lora_merge_parity(N, K, rank):
     Wq0, sw0 = cr.convrot_quantize_weight(torch_bf16(W), block, _f32(A), _f32(B), 16.0, 0.0)
     Wqp, swp = cr.convrot_quantize_weight(torch_bf16(W), block)
     assert torch.equal(Wq0, Wqp) and torch.equal(sw0, swp)
+
+
+def test_quantize_weight_lora_with_row_stride():
+    N, K, ld, rank, b = 37, 2048, 2560, 16, 128
+    Wfull = synth.normal_bf16(8, synth.STREAM_W, N, ld, 0.02)
+    W = np.ascontiguousarray(Wfull[:, :K])
+    A, B = synth.lora_pair(8, N, K, rank, 0.01)
+    q_ref, s_ref = oracle.quantize_weight(W, b, A, B, 16.0, 1.0)
+    t, At, Bt = torch_bf16(Wfull), _f32(A), _f32(B)
+    Wq = torch.empty((N, K), dtype=torch.int8, device="cuda")
+    sw = torch.empty((N,), dtype=torch.float32, device="cuda")
+    rc = cr.lib().convrot_quantize_weight(cr._ptr(t), N, K, ld, b, cr._ptr(At), cr._ptr(Bt), rank, 16.0, 1.0,
+                                          cr._ptr(Wq), cr._ptr(sw), cr._stream(None))
+    assert rc == cr.OK and cr.convrot_get_error() == cr.OK
+    check_codes(codes_of(Wq), q_ref, f64(oracle.lora_merge(W, A, B, 16.0, 1.0)), b)
+    check_scales(sw.cpu().numpy(), s_ref)
 
 
 # ------------------------------------------------------------------ fused GEMM + epilogue
