@@ -271,6 +271,19 @@ def run_gpu(args):
     return result
 
 
+def fp32_fma_peak(torch, dev):
+    """fp32 fused multiply-adds per second: 128 lanes per SM per clock at the maximum SM clock."""
+    props = torch.cuda.get_device_properties(dev)
+    mhz = 2070.0
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.max.sm", "--format=csv,noheader,nounits", "-i",
+                              str(dev.index or 0)], capture_output=True, text=True, timeout=10).stdout.strip()
+        mhz = float(out.splitlines()[0])
+    except (OSError, ValueError, IndexError, subprocess.SubprocessError):
+        pass
+    return props.multi_processor_count * 128 * mhz * 1e6
+
+
 def _hbm_row(nbytes, ms, pk, what):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"what": what, "ms": round(ms, 4), "algorithmic_bytes": int(nbytes), "GB/s": round(gbs, 1),
@@ -319,7 +332,7 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
     ws = torch.empty(cr.convrot_bwd_weight_workspace_bytes(N, K), dtype=torch.uint8, device=dev)
     ms = _time(torch, lambda i: cr.convrot_prepare_bwd_weight(Wq, sw, b, WtQ, swt, ws), flush, 3)
     rows["a6_prep_bwd_weight"] = _hbm_row(N * K + N * 4 + K * N + K * 4, ms, pk,
-                                          "C4 Wq [16384,4096] -> WtQ [4096,16384] (one-off, via an fp64 workspace)")
+                                          "C4 Wq [16384,4096] -> WtQ [4096,16384] (one-off, via a double-float workspace)")
     del W, Wq, WtQ, ws
     # a1 + a2: LoRA merge fused into the weight quantizer, C3 qkv weight
     wl3 = synth.WORKLOADS["qkv_lora"]
@@ -332,6 +345,12 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
                                                            sw3), flush, reps)
     rows["a1a2_lora_merge_quant"] = _hbm_row(N3 * K3 * 2 + N3 * K3 + N3 * 4 + r * K3 * 4 + N3 * r * 4, ms, pk,
                                              "C3 W [12288,4096] + LoRA r16 -> int8")
+    # the merge is r + 1 fp32 fused multiply-adds per element in a fixed order: its ALU roofline
+    fma = N3 * K3 * (r + 1)
+    fma_peak = fp32_fma_peak(torch, dev)
+    rows["a1a2_lora_merge_quant"].update({"fma_per_s_T": round(fma / (ms * 1e-3) / 1e12, 2),
+                                          "fma_peak_T": round(fma_peak / 1e12, 2),
+                                          "fma_frac": round(fma / (ms * 1e-3) / fma_peak, 4)})
     del W3, Wq3, A, B
     # a7: embedding table quantization (row-chunked: 8 slabs of 31000 rows)
     wl5 = synth.WORKLOADS["embed"]
