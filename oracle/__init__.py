@@ -58,6 +58,8 @@ def _load():
                 "oracle_prepare_bwd_weight": [P, P, I64, I64, I, P, P],
                 "oracle_linear_bwd_x": [P, I64, I64, P, P, I64, I, P, P, P],
                 "oracle_embedding_lookup": [P, I64, P, P, I64, I64, I, P, P],
+                "oracle_dequant_weight_t": [P, P, I64, I64, I, P],
+                "oracle_gemm_bf16": [P, P, I64, I64, I64, P],
                 "oracle_num_threads": [],
             }
             for name, args in sig.items():
@@ -199,6 +201,31 @@ def linear_bwd_x(dY_bits, WtQ, s_wt, b: int):
     _check(_load().oracle_linear_bwd_x(_p(dY), M, N, _p(WtQ), _p(_c(s_wt, np.float32)), K, b, _p(dX),
                                        _p(dyq), _p(sdy)), "linear_bwd_x")
     return dX, dyq, sdy
+
+
+def dequant_weight_t(Wq, s_w, b: int) -> np.ndarray:
+    """W_eff^T = bf16((s_w (.) Wq) R)^T, bf16 bits [K, N] (the bf16-mode backward weight)."""
+    Wq = _c(Wq, np.int8)
+    N, K = Wq.shape
+    out = np.empty((K, N), dtype=np.uint16)
+    _check(_load().oracle_dequant_weight_t(_p(Wq), _p(_c(s_w, np.float32)), N, K, b, _p(out)), "dequant_weight_t")
+    return out
+
+
+def gemm_bf16(A_bits, B_bits) -> np.ndarray:
+    """bf16(A . B^T) summed in fp64; A [M, K], B [N, K] bf16 bits."""
+    A = _c(A_bits, np.uint16)
+    B = _c(B_bits, np.uint16)
+    M, K = A.shape
+    N = B.shape[0]
+    C = np.empty((M, N), dtype=np.uint16)
+    _check(_load().oracle_gemm_bf16(_p(A), _p(B), M, N, K, _p(C)), "gemm_bf16")
+    return C
+
+
+def linear_bwd_x_bf16(dY_bits, Wq, s_w, b: int) -> np.ndarray:
+    """bf16-mode grad_x: dX = bf16(dY . W_eff) with W_eff = bf16((s_w (.) Wq) R)."""
+    return gemm_bf16(dY_bits, dequant_weight_t(Wq, s_w, b))
 
 
 def embedding_lookup(ids, Eq, s_e, b: int):

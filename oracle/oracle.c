@@ -45,6 +45,9 @@
  *       dX = bf16(acc * s_dy * s_wt).
  *   R7  Embedding lookup: out[t] = bf16_rne((s[id] * Eq[id,:]) R), fp64; an id
  *       outside [0, V) yields a zero row and is counted.
+ *   R8  bf16 backward (the default mode of the pages' backward option): the
+ *       frozen base is dequantized transiently, W_eff = bf16_rne((s_w (.) Wq) R)
+ *       (fp64 before the rounding), and dX = bf16_rne(dY . W_eff) summed in fp64.
  *
  * Build: gcc -O2 -fopenmp -ffp-contract=off -fPIC -shared (no fast-math: the
  * fp32 decisions of R3/R5 rely on IEEE single precision without contraction).
@@ -397,6 +400,47 @@ int oracle_linear_bwd_x(const uint16_t *dY, int64_t M, int64_t N, const int8_t *
                         int8_t *dyq_out, float *sdy_out)
 {
     return oracle_linear_fwd(dY, M, N, WtQ, s_wt, K, b, NULL, dX, dyq_out, sdy_out);
+}
+
+/* ---------------------------------------------- bf16 backward (R8) ---- */
+
+/* The default backward mode of the pages: the frozen base is dequantized
+ * transiently and grad_x is a bf16 matmul.  W_eff = bf16((s_w (.) Wq) R) along
+ * K, written transposed: WeffT [K, N] bf16 bits. */
+int oracle_dequant_weight_t(const int8_t *Wq, const float *s_w, int64_t N, int64_t K, int b, uint16_t *WeffT)
+{
+    if (!is_pow2(b) || K % b != 0)
+        return 1;
+    double *deq = malloc(sizeof(double) * (size_t)N * (size_t)K);
+    double *eff = malloc(sizeof(double) * (size_t)N * (size_t)K);
+    int rc = 2;
+    if (deq && eff) {
+        for (int64_t n = 0; n < N; n++)
+            for (int64_t k = 0; k < K; k++)
+                deq[n * K + k] = (double)s_w[n] * (double)Wq[n * K + k];
+        rc = oracle_rotate_rows(deq, N, K, b, eff);
+        if (rc == 0)
+            for (int64_t n = 0; n < N; n++)
+                for (int64_t k = 0; k < K; k++)
+                    WeffT[k * N + n] = f64_to_bf16(eff[n * K + k]);
+    }
+    free(deq);
+    free(eff);
+    return rc;
+}
+
+/* C[m, n] = bf16(sum_k A[m, k] B[n, k]) with bf16 inputs, summed in fp64. */
+int oracle_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t M, int64_t N, int64_t K, uint16_t *C)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; m++)
+        for (int64_t n = 0; n < N; n++) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; k++)
+                acc += bf16_to_f64(A[m * K + k]) * bf16_to_f64(B[n * K + k]);
+            C[m * N + n] = f64_to_bf16(acc);
+        }
+    return 0;
 }
 
 /* ------------------------------------------------- embedding lookup (R7) ---- */

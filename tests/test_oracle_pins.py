@@ -297,6 +297,65 @@ def test_bwd_weight_prep_recovers_base_and_bwd_close_to_bf16():
     np.testing.assert_array_equal(dx, oracle.dequant(oracle.gemm_s32(dyq, wtq), sdy, swt))
 
 
+def test_bf16_gemm_brute_force_and_numpy():
+    rng = np.random.default_rng(11)
+    A = _bf16(rng.normal(size=(3, 7)))
+    B = _bf16(rng.normal(size=(4, 7)))
+    C = oracle.gemm_bf16(A, B)
+    for m in range(3):          # pure-Python loops: the fp64 sum in k order, then one rounding
+        for n in range(4):
+            acc = 0.0
+            for k in range(7):
+                acc += float(_f64(A[m, k])) * float(_f64(B[n, k]))
+            assert C[m, n] == oracle.f64_to_bf16(acc)
+    A = synth.normal_bf16(12, 4, 33, 300, 1.0)
+    B = synth.normal_bf16(12, 1, 17, 300, 0.5)
+    ref = _bf16(_f64(A) @ _f64(B).T)
+    C = oracle.gemm_bf16(A, B)
+    ulps = np.abs(C.astype(np.int32) - ref.astype(np.int32))
+    assert np.all(ulps <= 1) and np.mean(ulps) < 1e-2   # summation order differs from numpy's
+
+
+def test_bf16_mode_dequant_weight():
+    K, N, b = 256, 96, 32
+    w = synth.normal_bf16(13, synth.STREAM_W, N, K, 0.02)
+    wq, sw = oracle.quantize_weight(w, b)
+    t = oracle.dequant_weight_t(wq, sw, b)
+    assert t.shape == (K, N) and t.dtype == np.uint16
+    # b = 1 (no rotation) is the plain dequantization s * q, rounded to bf16
+    wq1, sw1 = oracle.quantize_weight(w, 1)
+    np.testing.assert_array_equal(oracle.dequant_weight_t(wq1, sw1, 1),
+                                  _bf16(sw1[:, None].astype(np.float64) * wq1).T)
+    # the rotated-back weight recovers the base within half a step per element in the
+    # rotated basis (orthogonal R), plus one bf16 rounding
+    got = _f64(t).T                                              # [N, K]
+    per_row = np.linalg.norm(got - _f64(w), axis=1)
+    bound = np.sqrt(K) * sw * 0.5 + np.linalg.norm(got, axis=1) * 2.0 ** -8
+    assert np.all(per_row <= bound * (1 + 1e-6))
+    assert np.linalg.norm(got - _f64(w)) / np.linalg.norm(_f64(w)) < 2e-2
+    # it is one bf16 rounding of the W_eff that the int8 mode quantizes along N (a dense
+    # product with scipy's Hadamard; where the exact value is 0 the dense product leaves
+    # a rounding residue of ~1e-13)
+    w_eff = (sw[:, None].astype(np.float64) * wq) @ _kron_rotation(K, b)
+    assert np.all(np.abs(_f64(t).T - w_eff) <= np.abs(w_eff) * 2.0 ** -8 + 1e-12)
+
+
+def test_bf16_mode_grad_x_close_to_bf16_matmul():
+    M, K, N, b = 40, 128, 256, 32
+    w = synth.normal_bf16(14, synth.STREAM_W, N, K, 0.02)
+    wq, sw = oracle.quantize_weight(w, b)
+    dy = synth.normal_bf16(14, synth.STREAM_DY, M, N, 1e-3)
+    dx = oracle.linear_bwd_x_bf16(dy, wq, sw, b)
+    assert dx.shape == (M, K)
+    ref = _f64(dy) @ _f64(w)
+    rel = np.linalg.norm(_f64(dx) - ref) / np.linalg.norm(ref)
+    assert rel < 2e-2
+    # the int8 mode is further from the bf16 product than the bf16 mode
+    wtq, swt = oracle.prepare_bwd_weight(wq, sw, b)
+    dx8, _, _ = oracle.linear_bwd_x(dy, wtq, swt, b)
+    assert np.linalg.norm(_f64(dx8) - ref) > np.linalg.norm(_f64(dx) - ref)
+
+
 # ------------------------------------------------------------------ embedding
 
 
