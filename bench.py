@@ -39,21 +39,29 @@ L2_FLUSH_BYTES = 256 << 20
 # captures (dram__bytes_read.sum + dram__bytes_write.sum) of
 #   python -m int8_rotated_quantized_gb300.profile_case gemm --M 20480 --N 16384 --K 4096 --reps 1   (forward shape)
 #   python -m int8_rotated_quantized_gb300.profile_case gemm --M 20480 --N 4096 --K 16384 --reps 1   (grad_x shape)
+#   python -m int8_rotated_quantized_gb300.profile_case gemm_bf16 --M 20480 --N 4096 --K 16384 --reps 1   (bf16 grad_x)
 # keyed by the hash of the kernel source they were taken on; reported as null
 # once the kernel source differs.
-GEMM_TRAFFIC = {"source_sha256_16": "9bef5bba02530c86", "fwd": 417522176 + 647178496, "bwd": 1972629760 + 162354688}
+GEMM_TRAFFIC = {"source_sha256_16": "69fda478ceb34d4d", "fwd": 415623680 + 647219968, "bwd": 1970230528 + 162605824,
+                "bf16_bwd": 3198489088 + 162833408}
 
 
-def gemm_traffic_per_launch():
+def _gemm_source_current():
     import hashlib
     path = os.path.join(ROOT, "int8_rotated_quantized_gb300", "csrc", "gemm_tc.cu")
     try:
         with open(path, "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+            return hashlib.sha256(f.read()).hexdigest()[:16] == GEMM_TRAFFIC["source_sha256_16"]
     except OSError:
+        return False
+
+
+def gemm_traffic_per_launch(key=None):
+    """Measured DRAM bytes per launch (mean of the forward and grad_x shapes, or one key), or None."""
+    if not _gemm_source_current():
         return None
-    if sha != GEMM_TRAFFIC["source_sha256_16"]:
-        return None
+    if key is not None:
+        return GEMM_TRAFFIC[key]
     return (GEMM_TRAFFIC["fwd"] + GEMM_TRAFFIC["bwd"]) // 2
 
 
@@ -333,7 +341,20 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
     ms = _time(torch, lambda i: cr.convrot_prepare_bwd_weight(Wq, sw, b, WtQ, swt, ws), flush, 3)
     rows["a6_prep_bwd_weight"] = _hbm_row(N * K + N * 4 + K * N + K * 4, ms, pk,
                                           "C4 Wq [16384,4096] -> WtQ [4096,16384] (one-off, via a double-float workspace)")
-    del W, Wq, WtQ, ws
+    del WtQ, ws
+    # next row 1: the bf16 backward mode (transient dequantization + bf16 tcgen05 GEMM), C4 shapes
+    M = wl["M"]
+    weff_t = torch.empty((K, N), dtype=torch.bfloat16, device=dev)
+    ms = _time(torch, lambda i: cr.convrot_dequant_weight_t(Wq, sw, b, weff_t), flush, reps)
+    rows["n1_bf16_bwd_dequant"] = _hbm_row(N * K + N * 4 + K * N * 2, ms, pk,
+                                           "C4 Wq [16384,4096] -> W_eff^T bf16 [4096,16384] (per backward)")
+    dY = sg.normal_bf16(0, synth.STREAM_DY, M, N, wl["dy_sigma"], dev)
+    dX = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    ms = _time(torch, lambda i: cr.convrot_gemm_bf16(dY, weff_t, dX), flush, 5)
+    rows["n1_bf16_bwd_gemm"] = _tc_row(2.0 * M * N * K, ms, pk, "C4 dY [20480,16384] . W_eff -> dX bf16 [20480,4096]")
+    rows["n1_bf16_bwd_gemm"].update({"traffic": gemm_traffic_per_launch("bf16_bwd"),
+                                     "algorithmic_bytes": M * N * 2 + K * N * 2 + M * K * 2})
+    del W, Wq, weff_t, dY, dX
     # a1 + a2: LoRA merge fused into the weight quantizer, C3 qkv weight
     wl3 = synth.WORKLOADS["qkv_lora"]
     N3, K3, r = wl3["N"], wl3["K"], wl3["lora_rank"]
@@ -380,40 +401,70 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
     return rows
 
 
-def measure_e2e(cr, torch, dev, x, dY, Wq, sw, WtQ, swt, b, ops_step, steps=3):
-    """The step through the public calls with host buffers: H2D of x and dY from
-    pinned memory, forward and grad_x, D2H of y and dX, all inside the timed region."""
+def measure_e2e(cr, torch, dev, x, dY, Wq, sw, WtQ, swt, b, ops_step, steps=4):
+    """The step through the public calls with host buffers: every step copies its
+    x and dY from pinned host memory to the device, runs the forward and grad_x
+    calls, and copies y and dX back to pinned host memory, all inside the timed
+    region.  The copies run on their own streams (host-to-device, device-to-host)
+    with double-buffered device tensors, so a step's transfers overlap the
+    neighbouring steps' kernels; events order every reuse of a buffer."""
     M, K = x.shape
     N = dY.shape[1]
     xh = x.cpu().pin_memory()
     dyh = dY.cpu().pin_memory()
-    yh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
-    dxh = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
-    xd = torch.empty_like(x)
-    dyd = torch.empty_like(dY)
-    yd = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    dxd = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    yh = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dxh = [torch.empty((M, K), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    xd = [torch.empty_like(x) for _ in range(2)]
+    dyd = [torch.empty_like(dY) for _ in range(2)]
+    yd = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    dxd = [torch.empty((M, K), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     ws = torch.empty(max(cr.convrot_act_workspace_bytes(M, K), cr.convrot_act_workspace_bytes(M, N)),
                      dtype=torch.uint8, device=dev)
+    s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    x_in, dy_in, comp_done, y_ready, dx_ready, out_done = ([ev() for _ in range(2)] for _ in range(6))
+    used = [False, False]
 
-    def one():
-        xd.copy_(xh, non_blocking=True)
-        dyd.copy_(dyh, non_blocking=True)
-        cr.convrot_linear_fwd(xd, Wq, sw, b, y=yd, workspace=ws)
-        cr.convrot_linear_bwd_x(dyd, WtQ, swt, b, dX=dxd, workspace=ws)
-        yh.copy_(yd, non_blocking=True)
-        dxh.copy_(dxd, non_blocking=True)
+    def one(i):
+        j = i % 2
+        with torch.cuda.stream(s_in):
+            if used[j]:
+                s_in.wait_event(comp_done[j])           # step i-2 no longer reads xd[j], dyd[j]
+            xd[j].copy_(xh, non_blocking=True)
+            x_in[j].record(s_in)
+            dyd[j].copy_(dyh, non_blocking=True)
+            dy_in[j].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(x_in[j])
+            if used[j]:
+                s_comp.wait_event(out_done[j])          # step i-2's results have left yd[j], dxd[j]
+            cr.convrot_linear_fwd(xd[j], Wq, sw, b, y=yd[j], workspace=ws, stream=s_comp)
+            y_ready[j].record(s_comp)
+            s_comp.wait_event(dy_in[j])
+            cr.convrot_linear_bwd_x(dyd[j], WtQ, swt, b, dX=dxd[j], workspace=ws, stream=s_comp)
+            dx_ready[j].record(s_comp)
+            comp_done[j].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(y_ready[j])
+            yh[j].copy_(yd[j], non_blocking=True)
+            s_out.wait_event(dx_ready[j])
+            dxh[j].copy_(dxd[j], non_blocking=True)
+            out_done[j].record(s_out)
+        used[j] = True
 
-    one()
+    one(0)
+    one(1)
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for _ in range(steps):
-        one()
+    for i in range(steps):
+        one(i)
     torch.cuda.synchronize()
     dt = (time.perf_counter() - t0) / steps
     return {"value": round(ops_step / dt / 1e12, 3), "unit": "TOPS", "ms_per_step": round(dt * 1e3, 3),
             "h2d_bytes_per_step": int(x.numel() * 2 + dY.numel() * 2),
-            "d2h_bytes_per_step": int(M * N * 2 + M * K * 2)}
+            "d2h_bytes_per_step": int(M * N * 2 + M * K * 2),
+            "schedule": "3 streams (host-to-device copies, kernels, device-to-host copies), double-buffered; "
+                        "wall clock over the steps, synchronised on both sides"}
 
 
 # ---------------------------------------------------------------- oracle ----

@@ -190,6 +190,37 @@ CONVROT_API int convrot_linear_bwd_x(const uint16_t *dY, int64_t M, int64_t N, c
                          const float *scale_wt, int64_t K, int block, uint16_t *dX,
                          void *workspace, size_t ws_bytes, convrot_stream_t stream);
 
+/* ------------------------------------------------- bf16 frozen backward -- */
+
+/* The default backward mode of the layer (guide 4.1: the backward option
+ * takes bf16, the default, or int8; PR #2461 Summary: frozen base, grad_x
+ * only).  The base is dequantized transiently and the input gradient is a bf16
+ * matmul:
+ *   W_eff    = bf16_rne( (scale_w (.) Wq) R )  rounded once from a double-float
+ *              value; written transposed, WeffT bf16 [K, N] contiguous.
+ *   Wq int8 [N, K], scale_w fp32 [N]; N multiple of 16, K multiple of block and 16.
+ * Writes only WeffT; nothing is kept between calls. */
+CONVROT_API int convrot_dequant_weight_t(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K,
+                             int block, uint16_t *WeffT, convrot_stream_t stream);
+
+/* bf16 GEMM on the tensor cores: C[m,n] = bf16_rne( sum_k A[m,k] * B[n,k] ) with
+ * the sum accumulated in fp32.  A bf16 [M, K], B bf16 [N, K], C out bf16 [M, N],
+ * all contiguous and 16-byte aligned; K multiple of 16, N multiple of 16. */
+CONVROT_API int convrot_gemm_bf16(const uint16_t *A, int64_t M, int64_t K, const uint16_t *B, int64_t N,
+                      uint16_t *C, convrot_stream_t stream);
+
+/* Bytes of workspace convrot_linear_bwd_x_bf16 needs (WeffT, bf16 [K, N]). */
+CONVROT_API size_t convrot_bwd_x_bf16_workspace_bytes(int64_t N, int64_t K);
+
+/* Input gradient of the frozen layer in bf16 mode:
+ *   dX = bf16( dY . W_eff ),  W_eff as in convrot_dequant_weight_t
+ *   dY bf16 [M, N]; Wq int8 [N, K]; scale_w fp32 [N]; dX out bf16 [M, K];
+ *   workspace >= convrot_bwd_x_bf16_workspace_bytes(N, K), 256-byte aligned
+ *   (it receives WeffT). */
+CONVROT_API int convrot_linear_bwd_x_bf16(const uint16_t *dY, int64_t M, int64_t N, const int8_t *Wq,
+                              const float *scale_w, int64_t K, int block, uint16_t *dX,
+                              void *workspace, size_t ws_bytes, convrot_stream_t stream);
+
 /* -------------------------------------------------------------- embedding -- */
 
 /* Quantized token-embedding lookup (PR #2461 Summary: the int8 text encoder

@@ -56,6 +56,10 @@ def lib():
                 "convrot_prepare_bwd_weight": ([P, P, I64, I64, I, P, P, P, S, P], I),
                 "convrot_linear_bwd_x": ([P, I64, I64, P, P, I64, I, P, P, S, P], I),
                 "convrot_embedding_lookup": ([P, I64, P, P, I64, I64, I, P, P], I),
+                "convrot_dequant_weight_t": ([P, P, I64, I64, I, P, P], I),
+                "convrot_gemm_bf16": ([P, I64, I64, P, I64, P, P], I),
+                "convrot_bwd_x_bf16_workspace_bytes": ([I64, I64], S),
+                "convrot_linear_bwd_x_bf16": ([P, I64, I64, P, P, I64, I, P, P, S, P], I),
                 "convrot_gemm_s32_workspace_bytes": ([I64, I64], S),
                 "convrot_gemm_s32": ([P, P, I64, I64, I64, P, P, S, P], I),
                 "convrot_linear_fwd_noalloc": ([P, I64, I64, P, P, I64, I, P, P, P], I),
@@ -234,6 +238,54 @@ def convrot_linear_bwd_x(dY, WtQ, scale_wt, block, dX=None, workspace=None, stre
     ws = _workspace(nbytes, dY.device, workspace)
     _check(lib().convrot_linear_bwd_x(_ptr(dY), M, N, _ptr(WtQ), _ptr(scale_wt), K, block, _ptr(dX), _ptr(ws), nbytes,
                                       _stream(stream)), "convrot_linear_bwd_x")
+    return dX
+
+
+def convrot_dequant_weight_t(Wq, scale_w, block, out=None, stream=None):
+    """bf16-mode backward weight: W_eff^T = bf16((scale_w (.) Wq) R)^T, bf16 [K, N]."""
+    _need(Wq, torch.int8, "Wq", 2)
+    _need(scale_w, torch.float32, "scale_w", 1)
+    N, K = Wq.shape
+    if out is None:
+        out = torch.empty((K, N), dtype=torch.bfloat16, device=Wq.device)
+    _check(lib().convrot_dequant_weight_t(_ptr(Wq), _ptr(scale_w), N, K, block, _ptr(out), _stream(stream)),
+           "convrot_dequant_weight_t")
+    return out
+
+
+def convrot_gemm_bf16(A, B, out=None, stream=None):
+    """C = bf16(A . B^T) on the tensor cores (fp32 accumulation): A bf16 [M, K], B bf16 [N, K]."""
+    _need(A, torch.bfloat16, "A", 2)
+    _need(B, torch.bfloat16, "B", 2)
+    M, K = A.shape
+    N = B.shape[0]
+    if B.shape[1] != K:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.device)
+    _check(lib().convrot_gemm_bf16(_ptr(A), M, K, _ptr(B), N, _ptr(out), _stream(stream)), "convrot_gemm_bf16")
+    return out
+
+
+def convrot_bwd_x_bf16_workspace_bytes(N: int, K: int) -> int:
+    return lib().convrot_bwd_x_bf16_workspace_bytes(N, K)
+
+
+def convrot_linear_bwd_x_bf16(dY, Wq, scale_w, block, dX=None, workspace=None, stream=None):
+    """Input gradient in bf16 mode: dY bf16 [M, N], Wq int8 [N, K] -> dX = bf16(dY . W_eff) [M, K]."""
+    _need(dY, torch.bfloat16, "dY", 2)
+    _need(Wq, torch.int8, "Wq", 2)
+    _need(scale_w, torch.float32, "scale_w", 1)
+    M, N = dY.shape
+    if Wq.shape[0] != N:
+        raise ValueError("shape mismatch")
+    K = Wq.shape[1]
+    if dX is None:
+        dX = torch.empty((M, K), dtype=torch.bfloat16, device=dY.device)
+    nbytes = convrot_bwd_x_bf16_workspace_bytes(N, K)
+    ws = _workspace(nbytes, dY.device, workspace)
+    _check(lib().convrot_linear_bwd_x_bf16(_ptr(dY), M, N, _ptr(Wq), _ptr(scale_w), K, block, _ptr(dX), _ptr(ws),
+                                           nbytes, _stream(stream)), "convrot_linear_bwd_x_bf16")
     return dX
 
 

@@ -1,4 +1,7 @@
-// One-off preparation of the int8 backward weight, in double-float arithmetic.
+// Backward weights of a frozen ConvRot base, in double-float arithmetic: the
+// one-off int8 backward weight, and the transient bf16 weight of the default
+// bf16 backward mode (MOSS-Image LoRA training guide, section 4.1: the
+// backward option takes bf16 or int8; sd-scripts PR #2461, Summary).
 //
 // The input gradient goes through the same fused int8 GEMM as the forward
 // (MOSS-Image LoRA training guide, sections 4.1 and 7.1, the int8 backward
@@ -209,7 +212,133 @@ __global__ void __launch_bounds__(kThreads) rotq_df_kernel(const float2 *T, int6
     }
 }
 
+// ------------------------------------------------- bf16-mode backward weight --
+
+// The transient dequantization of the bf16 backward: WeffT[k][n] =
+// bf16(scale_w[n] * (H_b q_n)[k] / sqrt(b)), correctly rounded from a
+// double-float value.  A CTA takes 64 weight rows and one Hadamard block, so
+// each output row segment it writes is 128 contiguous bytes.
+constexpr int kDeqRows = 64;
+
+// bf16 bits of hi + lo (|lo| <= ulp(hi) / 2), rounded to nearest even: hi
+// decides unless its low 16 bits sit exactly on a bf16 tie, where the sign
+// of lo (or, if lo is 0, evenness) breaks it.  Rounding up means increasing
+// the magnitude, which is +1 on the sign-magnitude bits for either sign.
+__device__ __forceinline__ uint16_t df_to_bf16(float hi, float lo) {
+    const uint32_t u = __float_as_uint(hi);
+    const uint32_t low = u & 0xffffu;
+    const uint32_t r = u >> 16;
+    bool up;
+    if (low != 0x8000u)
+        up = low > 0x8000u;
+    else if (lo == 0.f)
+        up = (r & 1u) != 0;
+    else
+        up = (lo > 0.f) == (hi > 0.f);
+    return (uint16_t)(r + (up ? 1u : 0u));
+}
+
+// A CTA of 256 threads takes 64 weight rows and one Hadamard block of B
+// columns: all its row segments are loaded first (8 codes per item, ITEMS
+// items per thread, in flight together), transformed and written into a
+// shared tile [B][64] whose 8-column groups are xor-swizzled by the column
+// group of the writer, then the tile leaves as 16-byte stores (each output
+// row segment is 128 contiguous bytes).
+template <int B>
+__global__ void __launch_bounds__(256) dequant_t_kernel(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K,
+                                                        float ch, float cl, uint16_t *T) {
+    constexpr int LANES = B / 8;
+    constexpr int TOTAL = kDeqRows * LANES;
+    constexpr int ITEMS = (TOTAL + 255) / 256;
+    __shared__ __align__(16) uint16_t dtile[B * kDeqRows];
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int64_t n0 = (int64_t)blockIdx.x * kDeqRows;
+    const int64_t k0 = (int64_t)blockIdx.y * B;
+    uint2 raw[ITEMS];
+    float sc[ITEMS];
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int j = it * 256 + tid;
+        const int rl = j / LANES, cb = j - rl * LANES;
+        const int64_t n = n0 + rl;
+        const bool ok = j < TOTAL && n < N;
+        raw[it] = ok ? __ldg(reinterpret_cast<const uint2 *>(Wq + n * K + k0 + 8 * cb)) : make_uint2(0u, 0u);
+        sc[it] = ok ? __ldg(scale_w + n) : 0.f;
+    }
+#pragma unroll
+    for (int it = 0; it < ITEMS; ++it) {
+        const int j = it * 256 + tid;
+        const int rl = j / LANES, cb = j - rl * LANES;
+        const uint32_t w[2] = {raw[it].x, raw[it].y};
+        float e[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) e[i] = (float)(int8_t)((w[i >> 2] >> (8 * (i & 3))) & 0xff);
+        // exact integer transform along K (in-thread stages, then across lanes)
+#pragma unroll
+        for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if ((i & h) == 0) {
+                    const float a = e[i], c = e[i + h];
+                    e[i] = a + c;
+                    e[i + h] = a - c;
+                }
+#pragma unroll
+        for (int m = 1; m < LANES; m <<= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float p = __shfl_xor_sync(0xffffffffu, e[i], m);
+                e[i] = upper ? (p - e[i]) : (e[i] + p);
+            }
+        }
+        if (j < TOTAL) {
+            const int slot = rl ^ (8 * (cb & 7));
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float p = __fmul_rn(sc[it], e[i]);
+                const float pe = __fmaf_rn(sc[it], e[i], -p);  // s * u exactly as p + pe
+                float rh, rlo;
+                df_mul(p, pe, ch, cl, rh, rlo);
+                dtile[(8 * cb + i) * kDeqRows + slot] = df_to_bf16(rh, rlo);
+            }
+        }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < B * (kDeqRows / 8); idx += 256) {
+        const int kl = idx >> 3, g = idx & 7;
+        const uint4 v = *reinterpret_cast<const uint4 *>(&dtile[kl * kDeqRows + 8 * (g ^ ((kl >> 3) & 7))]);
+        const int64_t n = n0 + 8 * g;
+        uint16_t *dst = T + (k0 + kl) * N + n;
+        if (n + 8 <= N) {
+            *reinterpret_cast<uint4 *>(dst) = v;
+        } else {
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            for (int e = 0; e < 8 && n + e < N; ++e) dst[e] = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_dequant_t(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K, int block, uint16_t *T,
+                             cudaStream_t st) {
+    if (N == 0 || K == 0) return cudaSuccess;
+    const double c = 1.0 / sqrt((double)block);
+    const float ch = (float)c;
+    const float cl = (float)(c - (double)ch);
+    dim3 grid((unsigned)((N + kDeqRows - 1) / kDeqRows), (unsigned)(K / block));
+    switch (block) {
+        case 8: dequant_t_kernel<8><<<grid, 256, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
+        case 16: dequant_t_kernel<16><<<grid, 256, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
+        case 32: dequant_t_kernel<32><<<grid, 256, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
+        case 64: dequant_t_kernel<64><<<grid, 256, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
+        case 128: dequant_t_kernel<128><<<grid, 256, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
+        default: dequant_t_kernel<256><<<grid, 256, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
+    }
+    return cudaGetLastError();
+}
 
 cudaError_t launch_bwd_prep_df(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K, int block, void *work,
                                int8_t *WtQ, float *scale_wt, cudaStream_t st) {

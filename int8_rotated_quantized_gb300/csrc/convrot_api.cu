@@ -196,6 +196,54 @@ int convrot_linear_bwd_x(const uint16_t *dY, int64_t M, int64_t N, const int8_t 
     return convrot_linear_fwd(dY, M, N, WtQ, scale_wt, K, block, nullptr, dX, workspace, ws_bytes, stream);
 }
 
+int convrot_dequant_weight_t(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K, int block,
+                             uint16_t *WeffT, convrot_stream_t stream) {
+    CHECK(block_ok(block) && row_ok(K, block) && N >= 0 && N % 16 == 0 && N <= INT32_MAX);
+    CHECK(N == 0 || (Wq && scale_w && WeffT && aligned16(Wq) && aligned16(WeffT)));
+    unsigned *err = nullptr;
+    int rc = device_setup(&err);
+    if (rc != CONVROT_OK) return rc;
+    if (N == 0) return CONVROT_OK;
+    return cuda_status(convrot::launch_dequant_t(Wq, scale_w, N, K, block, WeffT, (cudaStream_t)stream));
+}
+
+int convrot_gemm_bf16(const uint16_t *A, int64_t M, int64_t K, const uint16_t *B, int64_t N, uint16_t *C,
+                      convrot_stream_t stream) {
+    CHECK(M >= 0 && N >= 0 && K > 0 && K % 16 == 0 && K <= (1 << 20) && N % 16 == 0);
+    CHECK(M <= INT32_MAX && N <= INT32_MAX);
+    CHECK(M == 0 || N == 0 || (A && B && C && aligned16(A) && aligned16(B) && aligned16(C)));
+    unsigned *err = nullptr;
+    int rc = device_setup(&err);
+    if (rc != CONVROT_OK) return rc;
+    if (M == 0 || N == 0) return CONVROT_OK;
+    return cuda_status(convrot::launch_gemm_bf16(A, B, M, N, K, C, err, (cudaStream_t)stream));
+}
+
+size_t convrot_bwd_x_bf16_workspace_bytes(int64_t N, int64_t K) {
+    if (N < 0 || K < 0) return 0;
+    return align256((size_t)N * (size_t)K * 2);
+}
+
+int convrot_linear_bwd_x_bf16(const uint16_t *dY, int64_t M, int64_t N, const int8_t *Wq, const float *scale_w,
+                              int64_t K, int block, uint16_t *dX, void *workspace, size_t ws_bytes,
+                              convrot_stream_t stream) {
+    CHECK(block_ok(block) && row_ok(K, block) && M >= 0 && N >= 0 && N % 16 == 0 && N <= (1 << 20));
+    CHECK(M <= INT32_MAX);
+    CHECK(M == 0 || N == 0 ||
+          (dY && Wq && scale_w && dX && workspace && aligned16(dY) && aligned16(Wq) && aligned16(dX) &&
+           ((uintptr_t)workspace & 255u) == 0 && ws_bytes >= convrot_bwd_x_bf16_workspace_bytes(N, K)));
+    unsigned *err = nullptr;
+    int rc = device_setup(&err);
+    if (rc != CONVROT_OK) return rc;
+    if (M == 0 || N == 0) return CONVROT_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint16_t *weff_t = static_cast<uint16_t *>(workspace);
+    rc = cuda_status(convrot::launch_dequant_t(Wq, scale_w, N, K, block, weff_t, st));
+    if (rc != CONVROT_OK) return rc;
+    // dX [M, K] = dY [M, N] . (WeffT [K, N])^T
+    return cuda_status(convrot::launch_gemm_bf16(dY, weff_t, M, K, N, dX, err, st));
+}
+
 int convrot_embedding_lookup(const int64_t *ids, int64_t n, const int8_t *Eq, const float *scale_e, int64_t V,
                              int64_t D, int block, uint16_t *out, convrot_stream_t stream) {
     CHECK(block_ok(block) && row_ok(D, block) && n >= 0 && V >= 0);

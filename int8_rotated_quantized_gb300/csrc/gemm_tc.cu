@@ -77,9 +77,16 @@ constexpr int TMEM_COLS = 512;
 constexpr int REGS_WG0 = 48, REGS_CONV = 72, REGS_EPI = 192;
 static_assert(128 * REGS_WG0 + 128 * REGS_CONV + 256 * REGS_EPI <= 65536, "register split exceeds the launch pool");
 
-// kind::f16 instruction descriptor: D fp32, A and B fp16, both K-major,
-// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(TT >> 3) << 17) | ((uint32_t)(TW >> 4) << 24);
+// kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A and B format
+// (bits 7-9, 10-12: 0 = fp16, 1 = bf16), both K-major, N >> 3 at bits 17-22,
+// M >> 4 at bits 24-28.
+constexpr uint32_t kIdescF16 = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(TT >> 3) << 17) | ((uint32_t)(TW >> 4) << 24);
+constexpr uint32_t kIdescBF16 = kIdescF16 | (1u << 7) | (1u << 10);
+
+// Kernel modes: integer codes with an int32 result, integer codes with the
+// dequantization epilogue, or bf16 operands with a bf16 result (the bf16
+// backward of a frozen base; no widening, one fp32 accumulation over all of K).
+constexpr int kModeS32 = 0, kModeDequant = 1, kModeBf16 = 2;
 
 struct GemmArgs {
     int M, N, K;
@@ -104,10 +111,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
@@ -199,7 +207,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, got);
 }
 
-template <bool OUT_S32>
+template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_s8_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const GemmArgs p) {
     extern __shared__ uint8_t smem_raw[];
@@ -224,7 +232,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar(BAR_W_EMPTY + i), 4);  // 4 converter warps
         }
         for (int i = 0; i < CSTAGES; ++i) {
-            mbar_init(bar(BAR_CONV_FULL + i), 4);
+            // converted by the 4 converter warps, or (bf16 mode) loaded by TMA
+            mbar_init(bar(BAR_CONV_FULL + i), MODE == kModeBf16 ? 1 : 4);
             mbar_init(bar(BAR_CONV_EMPTY + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -251,6 +260,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int num_w = (p.N + TW - 1) / TW;
     const int num_tiles = num_t * num_w;
     const int num_kb = (p.K + BK - 1) / BK;
+    // K blocks per TMEM accumulation: exact-integer chunks, or all of K for bf16
+    const int chunk_kb = MODE == kModeBf16 ? num_kb : CHUNK_KB;
 
     if (warp < 4) {
         regs_dec<REGS_WG0>();
@@ -258,10 +269,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // ---------------------------------------------------- producers
             // warp 0 streams activation tiles (freed by the MMA), warp 2 the
             // int8 weight tiles (freed by the converters), each in its own ring.
+            // In bf16 mode warp 2 loads the bf16 weight tiles straight into the
+            // ring the MMA reads (freed by the MMA).
             const bool is_x = warp == 0;
-            const int nst = is_x ? XSTAGES : WSTAGES;
-            const int full0 = is_x ? BAR_X_FULL : BAR_W_FULL;
-            const int empty0 = is_x ? BAR_X_EMPTY : BAR_W_EMPTY;
+            const bool w_direct = !is_x && MODE == kModeBf16;
+            const int nst = is_x ? XSTAGES : w_direct ? CSTAGES : WSTAGES;
+            const int full0 = is_x ? BAR_X_FULL : w_direct ? BAR_CONV_FULL : BAR_W_FULL;
+            const int empty0 = is_x ? BAR_X_EMPTY : w_direct ? BAR_CONV_EMPTY : BAR_W_EMPTY;
             const CUtensorMap *map = is_x ? &tmX : &tmW;
             asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
             int it = 0;
@@ -278,6 +292,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (is_x) {
                         mbar_expect_tx(bar(full0 + s), X_STAGE);
                         tma_load_2d(sX + s * X_STAGE, map, bar(full0 + s), kb * BK, tb * TT);
+                    } else if (w_direct) {
+                        mbar_expect_tx(bar(full0 + s), WH_STAGE);
+                        tma_load_2d(sWh + s * WH_STAGE, map, bar(full0 + s), kb * BK, wb * TW);
                     } else {
                         mbar_expect_tx(bar(full0 + s), W8_STAGE);
                         tma_load_2d(sW8 + s * W8_STAGE, map, bar(full0 + s), kb * BK, wb * TW);
@@ -295,7 +312,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t dcol = 0;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
                 for (int kb = 0; kb < num_kb; ++kb, ++it) {
-                    const int kc = kb % CHUNK_KB;
+                    const int kc = kb % chunk_kb;
                     if (kc == 0) {
                         const int buf = g & 1;
                         if (!mbar_wait(bar(BAR_ACC_EMPTY + buf), ((g >> 1) & 1) ^ 1, abort_flag, p.err)) {
@@ -317,11 +334,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int kk = 0; kk < BK / 16; ++kk) {
                         const uint64_t ad = sw128_desc(sWh + c * WH_STAGE + kk * 32);
                         const uint64_t bd = sw128_desc(sX + s * X_STAGE + kk * 32);
-                        umma_f16(tmem + dcol, ad, bd, (kc > 0 || kk > 0) ? 1u : 0u);
+                        umma_f16(tmem + dcol, ad, bd, MODE == kModeBf16 ? kIdescBF16 : kIdescF16,
+                                 (kc > 0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(bar(BAR_X_EMPTY + s));
                     umma_commit(bar(BAR_CONV_EMPTY + c));
-                    if (kc == CHUNK_KB - 1 || kb == num_kb - 1) {
+                    if (kc == chunk_kb - 1 || kb == num_kb - 1) {
                         umma_commit(bar(BAR_ACC_FULL + (g & 1)));
                         ++g;
                     }
@@ -342,7 +360,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         regs_dec<REGS_CONV>();
         const int ct = threadIdx.x - 128;
         int it = 0;
-        bool ok = true;
+        bool ok = MODE != kModeBf16;  // nothing to widen in bf16 mode
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
             for (int kb = 0; kb < num_kb; ++kb, ++it) {
                 const int s = it % WSTAGES;
@@ -399,7 +417,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             int acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0;
-            const int nchunks = (num_kb + CHUNK_KB - 1) / CHUNK_KB;
+            const int nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
             for (int ch = 0; ch < nchunks; ++ch, ++g) {
                 const int buf = g & 1;
                 if (!warp_wait(bar(BAR_ACC_FULL + buf), (g >> 1) & 1, abort_flag, p.err, lane)) {
@@ -413,8 +431,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     uint32_t r[16];
                     tmem_ld16(taddr + 16 * j, r);
                     tmem_wait_ld();
+                    if constexpr (MODE == kModeBf16) {  // one chunk: keep the fp32 bits
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[16 * j + i] += __float2int_rn(__uint_as_float(r[i]));
+                        for (int i = 0; i < 16; ++i) acc[16 * j + i] = (int)r[i];
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[16 * j + i] += __float2int_rn(__uint_as_float(r[i]));
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -428,11 +451,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int mlim = p.M - m0;  // tokens of this column half that exist
             const bool full = mlim >= 128;
             if (n < p.N) {
-                if constexpr (OUT_S32) {
+                if constexpr (MODE == kModeS32) {
                     int32_t *out = static_cast<int32_t *>(p.out) + (int64_t)m0 * p.N + n;
 #pragma unroll
                     for (int i = 0; i < 128; ++i) {
                         if (full || i < mlim) *out = acc[i];
+                        out += p.N;
+                    }
+                } else if constexpr (MODE == kModeBf16) {
+                    uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)m0 * p.N + n;
+#pragma unroll
+                    for (int i = 0; i < 128; ++i) {
+                        if (full || i < mlim) *out = (uint16_t)float_to_bf16_bits(__int_as_float(acc[i]));
                         out += p.N;
                     }
                 } else {
@@ -512,14 +542,25 @@ int sm_count_of_current_device() {
 // smaller estimated DRAM read volume wins.
 constexpr int64_t kRasterBudget = 32ll << 20;
 
-void choose_raster(int64_t num_t, int64_t num_w, int64_t K, int &group, int &group_weight) {
-    const int64_t t_tile = (int64_t)TT * K * 2, w_tile = (int64_t)TW * K;  // fp16 codes, int8 codes
+void choose_raster(int64_t num_t, int64_t num_w, int64_t K, int64_t w_elem, int &group, int &group_weight) {
+    const int64_t t_tile = (int64_t)TT * K * 2, w_tile = (int64_t)TW * K * w_elem;  // fp16/bf16 codes, int8 or bf16
     const int64_t gt = std::max<int64_t>(1, std::min<int64_t>(num_t, kRasterBudget / t_tile));
     const int64_t gw = std::max<int64_t>(1, std::min<int64_t>(num_w, kRasterBudget / w_tile));
     const int64_t reads_t = num_t * t_tile + num_w * w_tile * ((num_t + gt - 1) / gt);
     const int64_t reads_w = num_w * w_tile + num_t * t_tile * ((num_w + gw - 1) / gw);
     group_weight = reads_w < reads_t ? 1 : 0;
     group = (int)(group_weight ? gw : gt);
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap &tmX, const CUtensorMap &tmW, const GemmArgs &p, int64_t tiles,
+                        cudaStream_t st) {
+    const int sms = sm_count_of_current_device();
+    const int grid = (int)(tiles < sms ? tiles : sms);
+    cudaError_t e = cudaFuncSetAttribute(gemm_s8_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    gemm_s8_tc_kernel<MODE><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmX, tmW, p);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -537,21 +578,28 @@ cudaError_t launch_gemm(const uint16_t *A, const float *sa, const int8_t *B, con
         return cudaErrorInvalidValue;
     const int64_t num_t = (M + TT - 1) / TT, num_w = (N + TW - 1) / TW;
     int group, group_weight;
-    choose_raster(num_t, num_w, K, group, group_weight);
+    choose_raster(num_t, num_w, K, 1, group, group_weight);
     GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, sa, sb, bias, out, err};
-    const int64_t tiles = num_t * num_w;
-    const int sms = sm_count_of_current_device();
-    const int grid = (int)(tiles < sms ? tiles : sms);
-    if (out_s32) {
-        e = cudaFuncSetAttribute(gemm_s8_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        gemm_s8_tc_kernel<true><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmX, tmW, p);
-    } else {
-        e = cudaFuncSetAttribute(gemm_s8_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        gemm_s8_tc_kernel<false><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmX, tmW, p);
-    }
-    return cudaGetLastError();
+    return out_s32 ? launch_mode<kModeS32>(tmX, tmW, p, num_t * num_w, st)
+                   : launch_mode<kModeDequant>(tmX, tmW, p, num_t * num_w, st);
+}
+
+cudaError_t launch_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t M, int64_t N, int64_t K, uint16_t *out,
+                             unsigned *err, cudaStream_t st) {
+    if (M == 0 || N == 0) return cudaSuccess;
+    cudaError_t e = get_encoder();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tmX, tmW;
+    if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, (uint64_t)K, (uint64_t)M, BK, TT,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, (uint64_t)K, (uint64_t)N, BK, TW,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    const int64_t num_t = (M + TT - 1) / TT, num_w = (N + TW - 1) / TW;
+    int group, group_weight;
+    choose_raster(num_t, num_w, K, 2, group, group_weight);
+    GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, nullptr, nullptr, nullptr, out, err};
+    return launch_mode<kModeBf16>(tmX, tmW, p, num_t * num_w, st);
 }
 
 }  // namespace convrot

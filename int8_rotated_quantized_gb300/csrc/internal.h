@@ -33,6 +33,10 @@ cudaError_t launch_emb_lookup(const int64_t *ids, int64_t n, const int8_t *Eq, c
 cudaError_t launch_bwd_prep_df(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K, int block, void *work,
                                int8_t *WtQ, float *scale_wt, cudaStream_t st);
 
+// bf16-mode backward weight (bwd_prep.cu): T [K, N] bf16 = bf16((s_w (.) Wq) R)^T.
+cudaError_t launch_dequant_t(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K, int block, uint16_t *T,
+                             cudaStream_t st);
+
 cudaError_t launch_widen_i8(const int8_t *A, int64_t count, uint16_t *out, cudaStream_t st);
 
 // C[M,N] = A[M,K] . B[N,K]^T with A fp16-held integer codes and B int8 codes.
@@ -40,6 +44,10 @@ cudaError_t launch_widen_i8(const int8_t *A, int64_t count, uint16_t *out, cudaS
 // bf16(float(acc) * (sa[m] * sb[n]) + bias[n]).
 cudaError_t launch_gemm(const uint16_t *A, const float *sa, const int8_t *B, const float *sb, const uint16_t *bias,
                         int64_t M, int64_t N, int64_t K, void *out, bool out_s32, unsigned *err, cudaStream_t st);
+
+// C[M,N] = bf16(A[M,K] . B[N,K]^T) with bf16 operands, fp32 accumulation.
+cudaError_t launch_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t M, int64_t N, int64_t K, uint16_t *out,
+                             unsigned *err, cudaStream_t st);
 
 // Self-test of the bounded-wait failure path (selftest.cu).
 cudaError_t launch_wait_timeout(uint64_t limit_ns, unsigned *err, cudaStream_t st);

@@ -30,7 +30,7 @@ import synth.gpu as sg  # noqa: E402
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["gemm", "rotq", "lookup", "lora", "prep", "wquant"])
+    ap.add_argument("case", choices=["gemm", "gemm_bf16", "rotq", "lookup", "lora", "prep", "dequant", "wquant"])
     ap.add_argument("--M", type=int, default=8192)
     ap.add_argument("--N", type=int, default=16384)
     ap.add_argument("--K", type=int, default=4096)
@@ -52,6 +52,13 @@ def main():
         xq, sx = cr.convrot_quantize_activation(x, b)
         y = torch.empty((a.M, a.N), dtype=torch.bfloat16, device=dev)
         fn = lambda i: cr.convrot_gemm_dequant(xq, sx, Wq, sw, None, y)  # noqa: E731
+        work = 2.0 * a.M * a.N * a.K
+        unit = "TOPS"
+    elif a.case == "gemm_bf16":
+        A = sg.normal_bf16(0, synth.STREAM_DY, a.M, a.K, 1e-3, dev)
+        B = sg.normal_bf16(0, synth.STREAM_W, a.N, a.K, 0.02, dev)
+        y = torch.empty((a.M, a.N), dtype=torch.bfloat16, device=dev)
+        fn = lambda i: cr.convrot_gemm_bf16(A, B, y)  # noqa: E731
         work = 2.0 * a.M * a.N * a.K
         unit = "TOPS"
     elif a.case == "rotq":
@@ -84,6 +91,13 @@ def main():
         ws = torch.empty(cr.convrot_bwd_weight_workspace_bytes(a.N, a.K), dtype=torch.uint8, device=dev)
         fn = lambda i: cr.convrot_prepare_bwd_weight(Wq, sw, b, WtQ, swt, ws)  # noqa: E731
         work = 2 * a.N * a.K + 4 * (a.N + a.K)
+        unit = "GB/s"
+    elif a.case == "dequant":
+        W = sg.normal_bf16(0, synth.STREAM_W, a.N, a.K, 0.02, dev)
+        Wq, sw = cr.convrot_quantize_weight(W, b)
+        T = torch.empty((a.K, a.N), dtype=torch.bfloat16, device=dev)
+        fn = lambda i: cr.convrot_dequant_weight_t(Wq, sw, b, T)  # noqa: E731
+        work = a.N * a.K + a.N * 4 + 2 * a.N * a.K
         unit = "GB/s"
     else:
         T = sg.normal_bf16(0, synth.STREAM_TABLE, a.V, a.D, 0.02, dev)

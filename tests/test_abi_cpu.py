@@ -28,7 +28,8 @@ def test_header_declares_the_boundary():
     names = declared_symbols()
     for must in ["convrot_quantize_weight", "convrot_linear_fwd", "convrot_linear_bwd_x", "convrot_embedding_lookup",
                  "convrot_prepare_bwd_weight", "convrot_gemm_s32", "convrot_get_error", "convrot_status_string",
-                 "convrot_linear_fwd_noalloc", "convrot_selftest_wait_timeout"]:
+                 "convrot_linear_fwd_noalloc", "convrot_selftest_wait_timeout", "convrot_dequant_weight_t",
+                 "convrot_gemm_bf16", "convrot_linear_bwd_x_bf16", "convrot_bwd_x_bf16_workspace_bytes"]:
         assert must in names
 
 
@@ -83,6 +84,14 @@ def test_bad_shapes_are_rejected(L):
                                 need, None) == 1
     # s32 entry: K beyond the int32-safe limit
     assert L.convrot_gemm_s32(FAKE, FAKE, 1, 16, 1 << 18, FAKE, FAKE, 1 << 30, None) == 1
+    # bf16 backward: N not a multiple of 16, K not a multiple of the block, workspace too small
+    assert L.convrot_dequant_weight_t(FAKE, FAKE, 24, 256, 32, FAKE, None) == 1
+    assert L.convrot_dequant_weight_t(FAKE, FAKE, 32, 80, 32, FAKE, None) == 1
+    assert L.convrot_gemm_bf16(FAKE, 8, 24, FAKE, 32, FAKE, None) == 1
+    assert L.convrot_gemm_bf16(FAKE, 8, 32, FAKE, 24, FAKE, None) == 1
+    need = L.convrot_bwd_x_bf16_workspace_bytes(64, 256)
+    assert need == 64 * 256 * 2
+    assert L.convrot_linear_bwd_x_bf16(FAKE, 8, 64, FAKE, FAKE, 256, 32, FAKE, FAKE, need - 1, None) == 1
 
 
 def test_null_and_misaligned_pointers_are_rejected(L):

@@ -146,6 +146,36 @@ def test_train20k_forward_and_backward_full_size():
     assert rel_fro(f64(dx_s), f64(dy_rows) @ f64(w_rows_k)) <= REL_FRO_BF16
 
 
+def test_train20k_bf16_backward_full_size():
+    wl = synth.WORKLOADS["train20k"]
+    M, K, N, b = wl["M"], wl["K"], wl["N"], wl["block"]
+    W = sg.normal_bf16(0, synth.STREAM_W, N, K, wl["w_sigma"], "cuda")
+    Wq, sw = cr.convrot_quantize_weight(W, b)
+    dY = sg.normal_bf16(0, synth.STREAM_DY, M, N, wl["dy_sigma"], "cuda")
+    ws = torch.empty(cr.convrot_bwd_x_bf16_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
+    dX = cr.convrot_linear_bwd_x_bf16(dY, Wq, sw, b, workspace=ws)
+    assert cr.convrot_get_error() == cr.OK
+    rng = np.random.default_rng(6)
+    kblocks = np.sort(rng.choice(K // b, size=2, replace=False))
+    ks = np.concatenate([np.arange(kb * b, (kb + 1) * b) for kb in kblocks])
+    wq_np, sw_np = codes_of(Wq), sw.cpu().numpy()
+    weff_ref = np.concatenate([oracle.dequant_weight_t(np.ascontiguousarray(wq_np[:, kb * b:(kb + 1) * b]), sw_np, b)
+                               for kb in kblocks])                      # [len(ks), N]
+    weff_dev = ws[:K * N * 2].view(torch.int16).view(K, N)[torch.from_numpy(ks).cuda()].cpu().numpy().view(np.uint16)
+    np.testing.assert_array_equal(weff_dev, weff_ref)
+    ms = _rows(rng, M)
+    dy_rows = _normal_rows(synth.STREAM_DY, ms, N, wl["dy_sigma"])
+    assert np.array_equal(bits_of(dY[torch.from_numpy(ms).cuda()]), dy_rows)
+    dx_ref = oracle.gemm_bf16(dy_rows, weff_ref)
+    dx_s = bits_of(dX[torch.from_numpy(ms).cuda()][:, torch.from_numpy(ks).cuda()])
+    g, r = f64(dx_s), f64(dx_ref)
+    # one bf16 step, plus the fp32 accumulation of N terms near zero (see the parity tests)
+    assert np.all(np.abs(g - r) <= np.abs(r) * 2.0 ** -7 + 64 * 2.0 ** -24 * np.sqrt(N) * np.sqrt(np.mean(r * r)))
+    assert np.mean(dx_s == dx_ref) > 0.98
+    w_cols = bits_of(W[:, torch.from_numpy(ks).cuda()])
+    assert rel_fro(g, f64(dy_rows) @ f64(w_cols)) <= REL_FRO_BF16
+
+
 def test_embed_table_and_lookup_full_size():
     wl = synth.WORKLOADS["embed"]
     V, D, b, n = wl["V"], wl["D"], wl["block"], wl["n_ids"]

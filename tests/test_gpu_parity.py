@@ -239,6 +239,57 @@ def test_bwd_prep_and_grad_x_parity(block):
     assert rel_fro(d, f64(dY) @ f64(W)) <= REL_FRO_BF16
 
 
+# ------------------------------------------------------------------ bf16 backward
+
+
+def _check_bf16_sums(got_bits, ref_bits, K):
+    """bf16 results of fp32-accumulated sums of K terms against the fp64-summed
+    oracle: one bf16 rounding step apart (relative), plus an absolute allowance
+    for the fp32 accumulation (a random walk of K roundings of about 2^-24 of the
+    running sum, with a margin of 64) near zero; almost always identical."""
+    g, r = f64(got_bits), f64(ref_bits)
+    tol = np.abs(r) * 2.0 ** -7 + 64 * 2.0 ** -24 * math.sqrt(K) * np.sqrt(np.mean(r * r))
+    assert np.all(np.abs(g - r) <= tol)
+    assert np.mean(got_bits == ref_bits) > 0.98
+    assert rel_fro(g, r) <= REL_FRO_ORACLE
+
+
+@pytest.mark.parametrize("N,K,block", [(80, 256, 32), (192, 1024, 128), (16, 512, 256), (64, 64, 8)])
+def test_dequant_weight_t_parity(N, K, block):
+    W = synth.normal_bf16(15, synth.STREAM_W, N, K, 0.02)
+    wq, sw = oracle.quantize_weight(W, block)
+    ref = oracle.dequant_weight_t(wq, sw, block)
+    got = bits_of(cr.convrot_dequant_weight_t(_i8(wq), _f32(sw), block))
+    assert got.shape == (K, N)
+    # both sides round a value accurate to >= 44 bits once to bf16: identical
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 272, 1008), (64, 128, 64), (513, 400, 4096)])
+def test_gemm_bf16_parity(M, N, K):
+    A = synth.normal_bf16(16, synth.STREAM_DY, M, K, 1.0)
+    B = synth.normal_bf16(16, synth.STREAM_W, N, K, 0.05)
+    got = bits_of(cr.convrot_gemm_bf16(torch_bf16(A), torch_bf16(B)))
+    _check_bf16_sums(got, oracle.gemm_bf16(A, B), K)
+
+
+@pytest.mark.parametrize("block", [32, 128])
+def test_linear_bwd_x_bf16_parity(block):
+    M, K, N = 300, 384, 528
+    W = synth.normal_bf16(17, synth.STREAM_W, N, K, 0.02)
+    wq, sw = oracle.quantize_weight(W, block)
+    dY = synth.normal_bf16(17, synth.STREAM_DY, M, N, 1e-3)
+    ws = torch.empty(cr.convrot_bwd_x_bf16_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
+    dX = cr.convrot_linear_bwd_x_bf16(torch_bf16(dY), _i8(wq), _f32(sw), block, workspace=ws)
+    assert cr.convrot_get_error() == cr.OK
+    # the workspace holds the transient W_eff^T
+    weff_t = ws[:K * N * 2].view(torch.int16).view(K, N).cpu().numpy().view(np.uint16)
+    np.testing.assert_array_equal(weff_t, oracle.dequant_weight_t(wq, sw, block))
+    got = bits_of(dX)
+    _check_bf16_sums(got, oracle.linear_bwd_x_bf16(dY, wq, sw, block), N)
+    assert rel_fro(f64(got), f64(dY) @ f64(W)) <= REL_FRO_BF16
+
+
 # ------------------------------------------------------------------ embedding
 
 
