@@ -164,6 +164,46 @@ def test_quantize_weight_lora_with_row_stride():
     check_scales(sw.cpu().numpy(), s_ref)
 
 
+def test_fused_qkv_slabs_equal_separate_projections():
+    """A fused q/k/v weight is three row slabs: quantization is per row, so each
+    slab (with its own LoRA pair, or with its rows of a shared one) quantizes
+    through a slab view into the fused buffers, and the fused forward's column
+    blocks equal the per-slab forwards bit for bit.  Pre-quantized slabs (codes
+    and scales produced elsewhere) are used through the same views."""
+    D, K, b, r = 256, 512, 128, 8
+    W = synth.normal_bf16(18, synth.STREAM_W, 3 * D, K, 0.02)
+    pairs = [synth.lora_pair(18 + s, D, K, r, 0.01) for s in range(3)]
+    Wt = torch_bf16(W)
+    Wq = torch.empty((3 * D, K), dtype=torch.int8, device="cuda")
+    sw = torch.empty((3 * D,), dtype=torch.float32, device="cuda")
+    for s, (A, B) in enumerate(pairs):
+        rows = slice(s * D, (s + 1) * D)
+        cr.convrot_quantize_weight(Wt[rows], b, _f32(A), _f32(B), 16.0, 1.0, Wq=Wq[rows], scale_w=sw[rows])
+        q_ref, s_ref = oracle.quantize_weight(np.ascontiguousarray(W[rows]), b, A, B, 16.0, 1.0)
+        merged = oracle.lora_merge(np.ascontiguousarray(W[rows]), A, B, 16.0, 1.0)
+        check_codes(codes_of(Wq[rows]), q_ref, f64(merged), b, f"slab {s} codes")
+        check_scales(sw[rows].cpu().numpy(), s_ref, f"slab {s} scales")
+    x = torch_bf16(synth.activations_bf16(18, 200, K, 5, 30.0))
+    y = cr.convrot_linear_fwd(x, Wq, sw, b)
+    for s in range(3):
+        rows = slice(s * D, (s + 1) * D)
+        assert torch.equal(cr.convrot_linear_fwd(x, Wq[rows], sw[rows], b), y[:, rows])
+    # one LoRA pair over the stacked weight = the same pair's rows per slab
+    A, B = synth.lora_pair(21, 3 * D, K, r, 0.01)
+    Wq_f, sw_f = cr.convrot_quantize_weight(Wt, b, _f32(A), _f32(B), 16.0, 1.0)
+    for s in range(3):
+        rows = slice(s * D, (s + 1) * D)
+        Wq_s, sw_s = cr.convrot_quantize_weight(Wt[rows], b, _f32(A), _f32(np.ascontiguousarray(B[rows])), 16.0, 1.0)
+        assert torch.equal(Wq_s, Wq_f[rows]) and torch.equal(sw_s, sw_f[rows])
+    # pre-quantized ingest: oracle codes and scales, split by views, give the fused result per slab
+    wq_o, sw_o = oracle.quantize_weight(W, b)
+    Wq_o, sw_o_t = _i8(wq_o), _f32(sw_o)
+    y_o = cr.convrot_linear_fwd(x, Wq_o, sw_o_t, b)
+    for s in range(3):
+        rows = slice(s * D, (s + 1) * D)
+        assert torch.equal(cr.convrot_linear_fwd(x, Wq_o[rows], sw_o_t[rows], b), y_o[:, rows])
+
+
 # ------------------------------------------------------------------ fused GEMM + epilogue
 
 
