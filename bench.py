@@ -42,8 +42,8 @@ L2_FLUSH_BYTES = 256 << 20
 #   python -m int8_rotated_quantized_gb300.profile_case gemm_bf16 --M 20480 --N 4096 --K 16384 --reps 1   (bf16 grad_x)
 # keyed by the hash of the kernel source they were taken on; reported as null
 # once the kernel source differs.
-GEMM_TRAFFIC = {"source_sha256_16": "69fda478ceb34d4d", "fwd": 415623680 + 647219968, "bwd": 1970230528 + 162605824,
-                "bf16_bwd": 3198489088 + 162833408}
+GEMM_TRAFFIC = {"source_sha256_16": "cf263124db1f0b69", "fwd": 418867200 + 647664384, "bwd": 1972998656 + 161986304,
+                "bf16_bwd": 3195729408 + 162874112}
 
 
 def _gemm_source_current():

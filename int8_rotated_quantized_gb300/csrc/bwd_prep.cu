@@ -27,6 +27,7 @@
 // than 8 spread over b/8 consecutive lanes.
 #include "common.cuh"
 #include "internal.h"
+#include "wide.cuh"
 
 namespace convrot {
 namespace {
@@ -238,84 +239,64 @@ __device__ __forceinline__ uint16_t df_to_bf16(float hi, float lo) {
     return (uint16_t)(r + (up ? 1u : 0u));
 }
 
-// A CTA of 256 threads takes 64 weight rows and one Hadamard block of B
-// columns: all its row segments are loaded first (8 codes per item, ITEMS
-// items per thread, in flight together), transformed and written into a
-// shared tile [B][64] whose 8-column groups are xor-swizzled by the column
-// group of the writer, then the tile leaves as 16-byte stores (each output
-// row segment is 128 contiguous bytes).
+// A CTA takes 64 weight rows and KT = max(128, B) columns; each thread owns
+// 32 consecutive codes of one row (two 16-byte loads), transforms them in
+// registers (packed fp32 butterflies, log2(B / 32) stages across lanes), forms
+// every value as a double-float product with the row's double-float scale
+// s * (1/sqrt(B)), rounds it to bf16 and writes it into a shared tile
+// [KT][64] whose 8-column groups are xor-swizzled by the writer's 32-column
+// chunk; the tile leaves as 16-byte stores (128-byte row segments of T).
 template <int B>
-__global__ void __launch_bounds__(256) dequant_t_kernel(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K,
+__global__ void __launch_bounds__(512) dequant_t_kernel(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K,
                                                         float ch, float cl, uint16_t *T) {
-    constexpr int LANES = B / 8;
-    constexpr int TOTAL = kDeqRows * LANES;
-    constexpr int ITEMS = (TOTAL + 255) / 256;
-    __shared__ __align__(16) uint16_t dtile[B * kDeqRows];
+    constexpr int KT = B > 128 ? B : 128;
+    constexpr int TPR = KT / 32;  // threads per row
+    constexpr int LOGB = B == 8 ? 3 : B == 16 ? 4 : B == 32 ? 5 : B == 64 ? 6 : B == 128 ? 7 : 8;
+    __shared__ __align__(16) uint16_t dtile[KT * kDeqRows];
     const int tid = threadIdx.x;
     const int lane = tid & 31;
+    const int rl = tid / TPR, c = tid - rl * TPR;
     const int64_t n0 = (int64_t)blockIdx.x * kDeqRows;
-    const int64_t k0 = (int64_t)blockIdx.y * B;
-    uint2 raw[ITEMS];
-    float sc[ITEMS];
-#pragma unroll
-    for (int it = 0; it < ITEMS; ++it) {
-        const int j = it * 256 + tid;
-        const int rl = j / LANES, cb = j - rl * LANES;
-        const int64_t n = n0 + rl;
-        const bool ok = j < TOTAL && n < N;
-        raw[it] = ok ? __ldg(reinterpret_cast<const uint2 *>(Wq + n * K + k0 + 8 * cb)) : make_uint2(0u, 0u);
-        sc[it] = ok ? __ldg(scale_w + n) : 0.f;
+    const int64_t k0 = (int64_t)blockIdx.y * KT;
+    const int64_t n = n0 + rl;
+    const bool ok = n < N && k0 + 32 * c < K;
+    uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    float s = 0.f;
+    if (ok) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(Wq + n * K + k0 + 32 * c);
+        const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+        w[0] = v0.x, w[1] = v0.y, w[2] = v0.z, w[3] = v0.w, w[4] = v1.x, w[5] = v1.y, w[6] = v1.z, w[7] = v1.w;
+        s = __ldg(scale_w + n);
     }
+    // the row's scale times 1/sqrt(B) as a double-float (sh + sl)
+    const float sh = __fmul_rn(s, ch);
+    const float sl = __fmaf_rn(s, cl, __fmaf_rn(s, ch, -sh));
+    float e[32];
 #pragma unroll
-    for (int it = 0; it < ITEMS; ++it) {
-        const int j = it * 256 + tid;
-        const int rl = j / LANES, cb = j - rl * LANES;
-        const uint32_t w[2] = {raw[it].x, raw[it].y};
-        float e[8];
+    for (int i = 0; i < 32; ++i) e[i] = (float)(int8_t)((w[i >> 2] >> (8 * (i & 3))) & 0xff);
+    fwht32<LOGB>(e, lane);  // exact: integer sums below 2^15
+    const int slot = rl ^ (8 * (c & 7));
 #pragma unroll
-        for (int i = 0; i < 8; ++i) e[i] = (float)(int8_t)((w[i >> 2] >> (8 * (i & 3))) & 0xff);
-        // exact integer transform along K (in-thread stages, then across lanes)
-#pragma unroll
-        for (int h = 1; h < 8; h <<= 1)
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if ((i & h) == 0) {
-                    const float a = e[i], c = e[i + h];
-                    e[i] = a + c;
-                    e[i + h] = a - c;
-                }
-#pragma unroll
-        for (int m = 1; m < LANES; m <<= 1) {
-            const bool upper = (lane & m) != 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float p = __shfl_xor_sync(0xffffffffu, e[i], m);
-                e[i] = upper ? (p - e[i]) : (e[i] + p);
-            }
-        }
-        if (j < TOTAL) {
-            const int slot = rl ^ (8 * (cb & 7));
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float p = __fmul_rn(sc[it], e[i]);
-                const float pe = __fmaf_rn(sc[it], e[i], -p);  // s * u exactly as p + pe
-                float rh, rlo;
-                df_mul(p, pe, ch, cl, rh, rlo);
-                dtile[(8 * cb + i) * kDeqRows + slot] = df_to_bf16(rh, rlo);
-            }
-        }
+    for (int i = 0; i < 32; ++i) {
+        // u * (sh + sl) as hi + lo: the product u * sh exactly, plus u * sl
+        const float hi = __fmul_rn(e[i], sh);
+        const float lo = __fmaf_rn(e[i], sl, __fmaf_rn(e[i], sh, -hi));
+        float rh, rlo;
+        fast_two_sum(hi, lo, rh, rlo);
+        dtile[(32 * c + i) * kDeqRows + slot] = df_to_bf16(rh, rlo);
     }
     __syncthreads();
-    for (int idx = tid; idx < B * (kDeqRows / 8); idx += 256) {
+    for (int idx = tid; idx < KT * (kDeqRows / 8); idx += blockDim.x) {
         const int kl = idx >> 3, g = idx & 7;
-        const uint4 v = *reinterpret_cast<const uint4 *>(&dtile[kl * kDeqRows + 8 * (g ^ ((kl >> 3) & 7))]);
-        const int64_t n = n0 + 8 * g;
-        uint16_t *dst = T + (k0 + kl) * N + n;
-        if (n + 8 <= N) {
+        if (k0 + kl >= K) continue;
+        const uint4 v = *reinterpret_cast<const uint4 *>(&dtile[kl * kDeqRows + 8 * (g ^ ((kl >> 5) & 7))]);
+        const int64_t nn = n0 + 8 * g;
+        uint16_t *dst = T + (k0 + kl) * N + nn;
+        if (nn + 8 <= N) {
             *reinterpret_cast<uint4 *>(dst) = v;
         } else {
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            for (int e = 0; e < 8 && n + e < N; ++e) dst[e] = (uint16_t)(w[e >> 1] >> (16 * (e & 1)));
+            const uint32_t q[4] = {v.x, v.y, v.z, v.w};
+            for (int j = 0; j < 8 && nn + j < N; ++j) dst[j] = (uint16_t)(q[j >> 1] >> (16 * (j & 1)));
         }
     }
 }
@@ -328,14 +309,16 @@ cudaError_t launch_dequant_t(const int8_t *Wq, const float *scale_w, int64_t N, 
     const double c = 1.0 / sqrt((double)block);
     const float ch = (float)c;
     const float cl = (float)(c - (double)ch);
-    dim3 grid((unsigned)((N + kDeqRows - 1) / kDeqRows), (unsigned)(K / block));
+    const int kt = block > 128 ? block : 128;
+    dim3 grid((unsigned)((N + kDeqRows - 1) / kDeqRows), (unsigned)((K + kt - 1) / kt));
+    const int threads = 2 * kt;  // 64 rows x kt / 32 threads per row
     switch (block) {
-        case 8: dequant_t_kernel<8><<<grid, 256, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
-        case 16: dequant_t_kernel<16><<<grid, 256, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
-        case 32: dequant_t_kernel<32><<<grid, 256, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
-        case 64: dequant_t_kernel<64><<<grid, 256, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
-        case 128: dequant_t_kernel<128><<<grid, 256, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
-        default: dequant_t_kernel<256><<<grid, 256, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
+        case 8: dequant_t_kernel<8><<<grid, threads, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
+        case 16: dequant_t_kernel<16><<<grid, threads, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
+        case 32: dequant_t_kernel<32><<<grid, threads, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
+        case 64: dequant_t_kernel<64><<<grid, threads, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
+        case 128: dequant_t_kernel<128><<<grid, threads, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
+        default: dequant_t_kernel<256><<<grid, threads, 0, st>>>(Wq, scale_w, N, K, ch, cl, T); break;
     }
     return cudaGetLastError();
 }

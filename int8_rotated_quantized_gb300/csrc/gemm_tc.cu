@@ -34,11 +34,11 @@
 //   warps 4-7     int8 -> fp16 converters of the weight tiles
 //   warps 8-15    epilogue: TMEM -> registers, int32 accumulation, output
 // Pipelines: a 4-stage activation ring (fp16 32 KB, refilled when the MMA
-// is done with a slot), a 6-stage int8 weight ring (8 KB, refilled when the
+// is done with a slot), a 4-stage int8 weight ring (8 KB, refilled when the
 // converters are done, so weight loads and their widening run ahead of the
-// MMA), a 3-stage converted-weight ring (16 KB), and two 128x256 fp32 TMEM
-// accumulators (512 columns) alternating per K chunk so the epilogue drains
-// one while the MMA fills the other.
+// MMA), a 4-stage converted-weight ring (16 KB; 4 + 4 measured 3% faster than
+// 6 + 3), and two 128x256 fp32 TMEM accumulators (512 columns) alternating
+// per K chunk so the epilogue drains one while the MMA fills the other.
 // Every wait is bounded: on expiry the kernel records DEVERR_TIMEOUT, lets
 // in-flight copies and MMAs finish, frees TMEM and exits.
 #include <cuda.h>
@@ -55,7 +55,7 @@ namespace convrot {
 namespace {
 
 constexpr int TW = 128, TT = 256, BK = 64;  // weight rows (MMA M), tokens (MMA N), K per stage
-constexpr int XSTAGES = 4, WSTAGES = 6, CSTAGES = 3;
+constexpr int XSTAGES = 4, WSTAGES = 4, CSTAGES = 4;
 constexpr int CHUNK_KB = 16;  // K blocks per exact fp32 chunk: 16 * 64 = 1024
 constexpr int NUM_THREADS = 512;
 constexpr int W8_STAGE = TW * BK;      // 8 KB int8 weight tile (TMA)
@@ -74,7 +74,7 @@ constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 constexpr int TMEM_COLS = 512;
-constexpr int REGS_WG0 = 48, REGS_CONV = 72, REGS_EPI = 192;
+constexpr int REGS_WG0 = 48, REGS_CONV = 80, REGS_EPI = 184;
 static_assert(128 * REGS_WG0 + 128 * REGS_CONV + 256 * REGS_EPI <= 65536, "register split exceeds the launch pool");
 
 // kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A and B format
