@@ -31,19 +31,19 @@ if ROOT not in sys.path:
 METRIC = "ConvRot int8 linear TOPS & quantizer GB/s (1×GB300, % of roofline)"
 WORKLOAD = ("train20k: packed 20k-token training step of one ConvRot INT8 linear layer, x bf16 [20480,4096] "
             "N(0,1) with 41 outlier channels x30, W bf16 [16384,4096] N(0,0.02), dY bf16 [20480,16384] N(0,1e-3), "
-            "Hadamard block 128; per step: rotate+quantize x, int8 GEMM + dequant -> y, rotate+quantize dY, "
-            "int8 grad_x GEMM -> dX")
+            "Hadamard block 128; per step: rotate+quantize x, widen W codes to a transient fp16 operand, int8 GEMM "
+            "+ dequant -> y, rotate+quantize dY, widen the int8 backward weight, int8 grad_x GEMM -> dX")
 L2_FLUSH_BYTES = 256 << 20
 
 # DRAM bytes (read + write) per launch of gemm_s8_tc_kernel, from one-pass ncu
 # captures (dram__bytes_read.sum + dram__bytes_write.sum) of
-#   python -m int8_rotated_quantized_gb300.profile_case gemm --M 20480 --N 16384 --K 4096 --reps 1   (forward shape)
-#   python -m int8_rotated_quantized_gb300.profile_case gemm --M 20480 --N 4096 --K 16384 --reps 1   (grad_x shape)
-#   python -m int8_rotated_quantized_gb300.profile_case gemm_bf16 --M 20480 --N 4096 --K 16384 --reps 1   (bf16 grad_x)
+#   python -m int8_rotated_quantized_gb300.profile_case gemm_w16 --M 20480 --N 16384 --K 4096 --reps 3   (forward)
+#   python -m int8_rotated_quantized_gb300.profile_case gemm_w16 --M 20480 --N 4096 --K 16384 --reps 3   (grad_x)
+#   python -m int8_rotated_quantized_gb300.profile_case gemm_bf16 --M 20480 --N 4096 --K 16384 --reps 3  (bf16 grad_x)
 # keyed by the hash of the kernel source they were taken on; reported as null
-# once the kernel source differs.
-GEMM_TRAFFIC = {"source_sha256_16": "cf263124db1f0b69", "fwd": 418867200 + 647664384, "bwd": 1972998656 + 161986304,
-                "bf16_bwd": 3195729408 + 162874112}
+# once the kernel source differs (or where no capture was taken on it).
+GEMM_TRAFFIC = {"source_sha256_16": "c1dcb44dff9c1b49", "fwd": 869766144 + 651746560, "bwd": 3195821312 + 162856192,
+                "bf16_bwd": None}
 
 
 def _gemm_source_current():
@@ -169,30 +169,36 @@ def run_gpu(args):
     torch.cuda.synchronize()
     assert cr.convrot_get_error() == cr.OK
 
-    def step(ev=None):
-        if ev:
-            ev[0].record(stream)
-        cr.convrot_quantize_activation(x, b, xq, sx)
-        if ev:
-            ev[1].record(stream)
-        cr.convrot_gemm_dequant(xq, sx, Wq, sw, None, y)
-        if ev:
-            ev[2].record(stream)
-        cr.convrot_quantize_activation(dY, b, dyq, sdy)
-        if ev:
-            ev[3].record(stream)
-        cr.convrot_gemm_dequant(dyq, sdy, WtQ, swt, None, dX)
-        if ev:
-            ev[4].record(stream)
+    # transient fp16 copies of the weight codes (the int8 weights stay int8 at rest)
+    w16 = torch.empty((N, K), dtype=torch.float16, device=dev)
+    wt16 = torch.empty((K, N), dtype=torch.float16, device=dev)
 
-    launches_per_step = 4
+    def step(ev=None):
+        def mark(i):
+            if ev:
+                ev[i].record(stream)
+        mark(0)
+        cr.convrot_quantize_activation(x, b, xq, sx)
+        mark(1)
+        cr.convrot_widen_codes(Wq, w16)
+        mark(2)
+        cr.convrot_gemm_dequant_w16(xq, sx, w16, sw, None, y)
+        mark(3)
+        cr.convrot_quantize_activation(dY, b, dyq, sdy)
+        mark(4)
+        cr.convrot_widen_codes(WtQ, wt16)
+        mark(5)
+        cr.convrot_gemm_dequant_w16(dyq, sdy, wt16, swt, None, dX)
+        mark(6)
+
+    launches_per_step = 6
     for _ in range(args.warmup):
         flush.zero_()
         step()
     torch.cuda.synchronize()
     assert cr.convrot_get_error() == cr.OK
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
     sampler = ClockSampler(local) if rank == 0 else None
     if world > 1:
         dist.barrier()
@@ -207,11 +213,13 @@ def run_gpu(args):
     t_wall = time.perf_counter() - t_wall
     clocks = sampler.stop() if sampler else None
 
-    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[6]) for e in evs]
     k1x = [e[0].elapsed_time(e[1]) for e in evs]
-    gf = [e[1].elapsed_time(e[2]) for e in evs]
-    k1d = [e[2].elapsed_time(e[3]) for e in evs]
-    gb = [e[3].elapsed_time(e[4]) for e in evs]
+    wf = [e[1].elapsed_time(e[2]) for e in evs]
+    gf = [e[2].elapsed_time(e[3]) for e in evs]
+    k1d = [e[3].elapsed_time(e[4]) for e in evs]
+    wb = [e[4].elapsed_time(e[5]) for e in evs]
+    gb = [e[5].elapsed_time(e[6]) for e in evs]
     total_ms = sum(step_ms)
     t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
     if world > 1:
@@ -231,6 +239,8 @@ def run_gpu(args):
                                              "C4 x [20480,4096] bf16 -> fp16-held codes + fp32 scales")
         rows["a6_dy_rotate_quant"] = _hbm_row(M * N * 2 + M * N * 2 + M * 4, statistics.median(k1d), pk,
                                               "C4 dY [20480,16384] bf16 -> fp16-held codes + fp32 scales")
+        rows["a4_widen_weight_codes"] = _hbm_row(3 * N * K, statistics.median(wf + wb), pk,
+                                                 "C4 int8 codes [16384,4096] -> transient fp16 operand (fwd and bwd)")
         rows["a4a5_fwd_gemm"] = _tc_row(2.0 * M * N * K, statistics.median(gf), pk, "C4 20480x16384x4096")
         rows["a6_bwd_gemm"] = _tc_row(2.0 * M * N * K, statistics.median(gb), pk, "C4 20480x4096x16384")
         e2e = measure_e2e(cr, torch, dev, x, dY, Wq, sw, WtQ, swt, b, ops_step)
@@ -254,7 +264,7 @@ def run_gpu(args):
                        "tokens_per_gpu": M, "l2": "flushed between steps (256 MiB write, outside the events)",
                        "parallelism": f"replicas x{world} (rows sharded, no collective)"},
             "roofline": {
-                "kernel": "gemm_s8_tc_kernel (fwd and grad_x launches)",
+                "kernel": "gemm_s8_tc_kernel, widened-weight mode (fwd and grad_x launches)",
                 "bound": "tensor",
                 "achieved": round(gemm_tflops, 1),
                 "peak": pk["bf16"],
@@ -264,7 +274,8 @@ def run_gpu(args):
                              "bf16/fp16 rate; tcgen05 kind::i8 does not exist on sm_103a)",
                 "traffic": gemm_traffic_per_launch(),
                 "traffic_note": "mean DRAM bytes per launch over the forward and grad_x shapes (ncu, one pass); "
-                                "algorithmic bytes per launch 906117120 for both",
+                                "algorithmic bytes per launch 973225984 for both (fp16 activation and weight "
+                                "codes, bf16 output, fp32 scales)",
             },
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -418,7 +429,7 @@ def measure_e2e(cr, torch, dev, x, dY, Wq, sw, WtQ, swt, b, ops_step, steps=4):
     dyd = [torch.empty_like(dY) for _ in range(2)]
     yd = [torch.empty((M, N), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     dxd = [torch.empty((M, K), dtype=torch.bfloat16, device=dev) for _ in range(2)]
-    ws = torch.empty(max(cr.convrot_act_workspace_bytes(M, K), cr.convrot_act_workspace_bytes(M, N)),
+    ws = torch.empty(max(cr.convrot_linear_workspace_bytes(M, K, N), cr.convrot_linear_workspace_bytes(M, N, K)),
                      dtype=torch.uint8, device=dev)
     s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event()  # noqa: E731

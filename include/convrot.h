@@ -121,15 +121,37 @@ CONVROT_API int convrot_gemm_dequant(const uint16_t *xq, const float *scale_x, i
                          const int8_t *Wq, const float *scale_w, int64_t N, const uint16_t *bias,
                          uint16_t *y, convrot_stream_t stream);
 
+/* int8 codes -> fp16 values of the same integers (every code in [-127, 127]
+ * is exact in fp16): the operand format of the tensor-core path, which has no
+ * int8 kind on this GPU.  q int8 [count], out16 fp16 [count], both 16-byte
+ * aligned; count a multiple of 16. */
+CONVROT_API int convrot_widen_codes(const int8_t *q, int64_t count, uint16_t *out16, convrot_stream_t stream);
+
+/* convrot_gemm_dequant with the weight codes already widened to fp16 values
+ * (Wq16 [N, K], from convrot_widen_codes): the same exact integer accumulation
+ * and epilogue, without widening inside the GEMM. */
+CONVROT_API int convrot_gemm_dequant_w16(const uint16_t *xq, const float *scale_x, int64_t M, int64_t K,
+                             const uint16_t *Wq16, const float *scale_w, int64_t N, const uint16_t *bias,
+                             uint16_t *y, convrot_stream_t stream);
+
 /* Bytes of workspace convrot_linear_fwd / convrot_linear_bwd_x need for M rows
  * of length K (the fp16-held codes and the fp32 scales). */
 CONVROT_API size_t convrot_act_workspace_bytes(int64_t M, int64_t K);
 
+/* Bytes of workspace with which convrot_linear_fwd (and convrot_linear_bwd_x
+ * with N and K exchanged) takes its faster path: the activation codes and
+ * scales plus a transient fp16 copy of the weight codes, [N, K] (see below). */
+CONVROT_API size_t convrot_linear_workspace_bytes(int64_t M, int64_t K, int64_t N);
+
 /* Forward of the ConvRot INT8 linear layer: convrot_quantize_activation into
- * `workspace`, then convrot_gemm_dequant.  x bf16 [M, K] contiguous; y bf16
- * [M, N]; workspace device memory of at least convrot_act_workspace_bytes(M, K),
- * 256-byte aligned.  The workspace must not be shared by calls in flight on
- * other streams. */
+ * `workspace`, then the int8 GEMM with the dequantization epilogue.  x bf16
+ * [M, K] contiguous; y bf16 [M, N]; workspace device memory of at least
+ * convrot_act_workspace_bytes(M, K), 256-byte aligned.  With at least
+ * convrot_linear_workspace_bytes(M, K, N) bytes the weight codes are first
+ * widened into the workspace as fp16 values (convrot_widen_codes) and the GEMM
+ * reads them directly (convrot_gemm_dequant_w16); the weight stays int8 at
+ * rest and the result is bit-identical either way.  The workspace must not be
+ * shared by calls in flight on other streams. */
 CONVROT_API int convrot_linear_fwd(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq,
                        const float *scale_w, int64_t N, int block, const uint16_t *bias,
                        uint16_t *y, void *workspace, size_t ws_bytes, convrot_stream_t stream);

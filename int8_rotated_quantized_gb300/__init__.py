@@ -57,6 +57,9 @@ def lib():
                 "convrot_linear_bwd_x": ([P, I64, I64, P, P, I64, I, P, P, S, P], I),
                 "convrot_embedding_lookup": ([P, I64, P, P, I64, I64, I, P, P], I),
                 "convrot_dequant_weight_t": ([P, P, I64, I64, I, P, P], I),
+                "convrot_linear_workspace_bytes": ([I64, I64, I64], S),
+                "convrot_widen_codes": ([P, I64, P, P], I),
+                "convrot_gemm_dequant_w16": ([P, P, I64, I64, P, P, I64, P, P, P], I),
                 "convrot_gemm_bf16": ([P, I64, I64, P, I64, P, P], I),
                 "convrot_bwd_x_bf16_workspace_bytes": ([I64, I64], S),
                 "convrot_linear_bwd_x_bf16": ([P, I64, I64, P, P, I64, I, P, P, S, P], I),
@@ -179,8 +182,50 @@ def convrot_gemm_dequant(xq, scale_x, Wq, scale_w, bias=None, y=None, stream=Non
     return y
 
 
+def convrot_widen_codes(q, out=None, stream=None):
+    """int8 codes -> fp16 values of the same integers (same shape)."""
+    _need(q, torch.int8, "q", q.dim())
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float16, device=q.device)
+    _check(lib().convrot_widen_codes(_ptr(q), q.numel(), _ptr(out), _stream(stream)), "convrot_widen_codes")
+    return out
+
+
+def convrot_gemm_dequant_w16(xq, scale_x, Wq16, scale_w, bias=None, y=None, stream=None):
+    """convrot_gemm_dequant with fp16-held weight codes Wq16 [N, K] (from convrot_widen_codes)."""
+    _need(xq, torch.float16, "xq", 2)
+    _need(Wq16, torch.float16, "Wq16", 2)
+    _need(scale_x, torch.float32, "scale_x", 1)
+    _need(scale_w, torch.float32, "scale_w", 1)
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias", 1)
+    M, K = xq.shape
+    N = Wq16.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    _check(lib().convrot_gemm_dequant_w16(_ptr(xq), _ptr(scale_x), M, K, _ptr(Wq16), _ptr(scale_w), N, _ptr(bias),
+                                          _ptr(y), _stream(stream)), "convrot_gemm_dequant_w16")
+    return y
+
+
 def convrot_act_workspace_bytes(M: int, K: int) -> int:
     return lib().convrot_act_workspace_bytes(M, K)
+
+
+def convrot_linear_workspace_bytes(M: int, K: int, N: int) -> int:
+    return lib().convrot_linear_workspace_bytes(M, K, N)
+
+
+def _linear_ws(M, K, N, device, workspace):
+    """The caller's workspace (its whole size is passed on, so a large enough one
+    takes the widened-weight path), or a new one of the fast size."""
+    if workspace is None:
+        nbytes = convrot_linear_workspace_bytes(M, K, N)
+        return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device), nbytes
+    nbytes = workspace.numel() * workspace.element_size()
+    if nbytes < convrot_act_workspace_bytes(M, K):
+        raise ValueError("workspace too small")
+    return workspace, nbytes
 
 
 def convrot_linear_fwd(x, Wq, scale_w, block, bias=None, y=None, workspace=None, stream=None):
@@ -196,8 +241,7 @@ def convrot_linear_fwd(x, Wq, scale_w, block, bias=None, y=None, workspace=None,
         raise ValueError("shape mismatch")
     if y is None:
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
-    nbytes = convrot_act_workspace_bytes(M, K)
-    ws = _workspace(nbytes, x.device, workspace)
+    ws, nbytes = _linear_ws(M, K, N, x.device, workspace)
     _check(lib().convrot_linear_fwd(_ptr(x), M, K, _ptr(Wq), _ptr(scale_w), N, block, _ptr(bias), _ptr(y), _ptr(ws),
                                     nbytes, _stream(stream)), "convrot_linear_fwd")
     return y
@@ -234,8 +278,7 @@ def convrot_linear_bwd_x(dY, WtQ, scale_wt, block, dX=None, workspace=None, stre
         raise ValueError("shape mismatch")
     if dX is None:
         dX = torch.empty((M, K), dtype=torch.bfloat16, device=dY.device)
-    nbytes = convrot_act_workspace_bytes(M, N)
-    ws = _workspace(nbytes, dY.device, workspace)
+    ws, nbytes = _linear_ws(M, N, K, dY.device, workspace)
     _check(lib().convrot_linear_bwd_x(_ptr(dY), M, N, _ptr(WtQ), _ptr(scale_wt), K, block, _ptr(dX), _ptr(ws), nbytes,
                                       _stream(stream)), "convrot_linear_bwd_x")
     return dX

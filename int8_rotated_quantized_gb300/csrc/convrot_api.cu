@@ -150,6 +150,37 @@ size_t convrot_act_workspace_bytes(int64_t M, int64_t K) {
     return align256((size_t)M * (size_t)K * 2) + align256((size_t)M * 4);
 }
 
+size_t convrot_linear_workspace_bytes(int64_t M, int64_t K, int64_t N) {
+    if (M < 0 || K < 0 || N < 0) return 0;
+    return convrot_act_workspace_bytes(M, K) + align256((size_t)N * (size_t)K * 2);
+}
+
+int convrot_widen_codes(const int8_t *q, int64_t count, uint16_t *out16, convrot_stream_t stream) {
+    CHECK(count >= 0 && count % 16 == 0);
+    CHECK(count == 0 || (q && out16 && aligned16(q) && aligned16(out16)));
+    unsigned *err = nullptr;
+    int rc = device_setup(&err);
+    if (rc != CONVROT_OK) return rc;
+    if (count == 0) return CONVROT_OK;
+    return cuda_status(convrot::launch_widen_codes(q, count, out16, (cudaStream_t)stream));
+}
+
+int convrot_gemm_dequant_w16(const uint16_t *xq, const float *scale_x, int64_t M, int64_t K, const uint16_t *Wq16,
+                             const float *scale_w, int64_t N, const uint16_t *bias, uint16_t *y,
+                             convrot_stream_t stream) {
+    CHECK(M >= 0 && N >= 0 && K > 0 && K % 16 == 0 && K <= (1 << 20) && N % 16 == 0);
+    CHECK(M <= INT32_MAX && N <= INT32_MAX);
+    CHECK(M == 0 || N == 0 ||
+          (xq && scale_x && Wq16 && scale_w && y && aligned16(xq) && aligned16(Wq16) && aligned16(y) &&
+           aligned16(scale_x) && aligned16(scale_w) && (bias == nullptr || aligned16(bias))));
+    unsigned *err = nullptr;
+    int rc = device_setup(&err);
+    if (rc != CONVROT_OK) return rc;
+    if (M == 0 || N == 0) return CONVROT_OK;
+    return cuda_status(
+        convrot::launch_gemm_w16(xq, scale_x, Wq16, scale_w, bias, M, N, K, y, err, (cudaStream_t)stream));
+}
+
 int convrot_linear_fwd(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq, const float *scale_w, int64_t N,
                        int block, const uint16_t *bias, uint16_t *y, void *workspace, size_t ws_bytes,
                        convrot_stream_t stream) {
@@ -168,6 +199,13 @@ int convrot_linear_fwd(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq
     float *sx = reinterpret_cast<float *>(static_cast<char *>(workspace) + align256((size_t)M * (size_t)K * 2));
     rc = quantize_act_impl(x, M, K, K, block, xq, sx, st);
     if (rc != CONVROT_OK) return rc;
+    if (ws_bytes >= convrot_linear_workspace_bytes(M, K, N)) {
+        // transient fp16 copy of the weight codes, then the GEMM without widening in its loop
+        uint16_t *w16 = reinterpret_cast<uint16_t *>(static_cast<char *>(workspace) + convrot_act_workspace_bytes(M, K));
+        rc = cuda_status(convrot::launch_widen_codes(Wq, N * K, w16, st));
+        if (rc != CONVROT_OK) return rc;
+        return cuda_status(convrot::launch_gemm_w16(xq, sx, w16, scale_w, bias, M, N, K, y, err, st));
+    }
     return gemm_impl(xq, sx, M, K, Wq, scale_w, N, bias, y, err, st);
 }
 

@@ -50,6 +50,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "mbar.cuh"
+#include "wide.cuh"
 
 namespace convrot {
 namespace {
@@ -83,10 +84,14 @@ static_assert(128 * REGS_WG0 + 128 * REGS_CONV + 256 * REGS_EPI <= 65536, "regis
 constexpr uint32_t kIdescF16 = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(TT >> 3) << 17) | ((uint32_t)(TW >> 4) << 24);
 constexpr uint32_t kIdescBF16 = kIdescF16 | (1u << 7) | (1u << 10);
 
-// Kernel modes: integer codes with an int32 result, integer codes with the
-// dequantization epilogue, or bf16 operands with a bf16 result (the bf16
-// backward of a frozen base; no widening, one fp32 accumulation over all of K).
-constexpr int kModeS32 = 0, kModeDequant = 1, kModeBf16 = 2;
+// Kernel modes: integer codes with an int32 result; integer codes with the
+// dequantization epilogue; bf16 operands with a bf16 result (the bf16
+// backward of a frozen base: one fp32 accumulation over all of K); and the
+// dequantization epilogue on weight codes that a separate pass already
+// widened to fp16 (no converter in the loop, the same exact integer chunks).
+constexpr int kModeS32 = 0, kModeDequant = 1, kModeBf16 = 2, kModeDequantW16 = 3;
+// modes whose weight tiles arrive by TMA already in the MMA's format
+constexpr bool weight_direct(int mode) { return mode == kModeBf16 || mode == kModeDequantW16; }
 
 struct GemmArgs {
     int M, N, K;
@@ -180,21 +185,6 @@ __device__ __forceinline__ void tile_coords(int tile, int num_t, int num_w, int 
     wb = group_weight ? g : sw;
 }
 
-// int8 x 4 -> two fp16x2 words holding the same integers: bias each byte by
-// 128 (xor 0x80), splice it under the fp16 exponent of 1024 (0x64), and
-// subtract 1152 = 1024 + 128 exactly.
-__device__ __forceinline__ void widen4(uint32_t w, uint32_t &lo, uint32_t &hi) {
-    const uint32_t x = w ^ 0x80808080u;
-    uint32_t a, b;
-    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(x), "r"(0x64646464u));
-    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(x), "r"(0x64646464u));
-    const __half2 k = __half2half2(__ushort_as_half((unsigned short)0x6480));
-    __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), k);
-    __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), k);
-    lo = *reinterpret_cast<uint32_t *>(&ha);
-    hi = *reinterpret_cast<uint32_t *>(&hb);
-}
-
 // ------------------------------------------------------------------ kernel --
 
 // Every lane of the warp polls the barrier (a single polling lane with the
@@ -233,7 +223,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int i = 0; i < CSTAGES; ++i) {
             // converted by the 4 converter warps, or (bf16 mode) loaded by TMA
-            mbar_init(bar(BAR_CONV_FULL + i), MODE == kModeBf16 ? 1 : 4);
+            mbar_init(bar(BAR_CONV_FULL + i), weight_direct(MODE) ? 1 : 4);
             mbar_init(bar(BAR_CONV_EMPTY + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -272,7 +262,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // In bf16 mode warp 2 loads the bf16 weight tiles straight into the
             // ring the MMA reads (freed by the MMA).
             const bool is_x = warp == 0;
-            const bool w_direct = !is_x && MODE == kModeBf16;
+            const bool w_direct = !is_x && weight_direct(MODE);
             const int nst = is_x ? XSTAGES : w_direct ? CSTAGES : WSTAGES;
             const int full0 = is_x ? BAR_X_FULL : w_direct ? BAR_CONV_FULL : BAR_W_FULL;
             const int empty0 = is_x ? BAR_X_EMPTY : w_direct ? BAR_CONV_EMPTY : BAR_W_EMPTY;
@@ -360,7 +350,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         regs_dec<REGS_CONV>();
         const int ct = threadIdx.x - 128;
         int it = 0;
-        bool ok = MODE != kModeBf16;  // nothing to widen in bf16 mode
+        bool ok = !weight_direct(MODE);  // nothing to widen when the weight tiles come ready
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
             for (int kb = 0; kb < num_kb; ++kb, ++it) {
                 const int s = it % WSTAGES;
@@ -465,7 +455,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (full || i < mlim) *out = (uint16_t)float_to_bf16_bits(__int_as_float(acc[i]));
                         out += p.N;
                     }
-                } else {
+                } else {  // kModeDequant, kModeDequantW16
                     uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)m0 * p.N + n;
                     const float swn = __ldg(p.sb + n);
                     const bool has_bias = p.bias != nullptr;
@@ -582,6 +572,25 @@ cudaError_t launch_gemm(const uint16_t *A, const float *sa, const int8_t *B, con
     GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, sa, sb, bias, out, err};
     return out_s32 ? launch_mode<kModeS32>(tmX, tmW, p, num_t * num_w, st)
                    : launch_mode<kModeDequant>(tmX, tmW, p, num_t * num_w, st);
+}
+
+cudaError_t launch_gemm_w16(const uint16_t *A, const float *sa, const uint16_t *B16, const float *sb,
+                            const uint16_t *bias, int64_t M, int64_t N, int64_t K, uint16_t *out, unsigned *err,
+                            cudaStream_t st) {
+    if (M == 0 || N == 0) return cudaSuccess;
+    cudaError_t e = get_encoder();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tmX, tmW;
+    if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, (uint64_t)K, (uint64_t)M, BK, TT,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B16, (uint64_t)K, (uint64_t)N, BK, TW,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    const int64_t num_t = (M + TT - 1) / TT, num_w = (N + TW - 1) / TW;
+    int group, group_weight;
+    choose_raster(num_t, num_w, K, 2, group, group_weight);
+    GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, sa, sb, bias, out, err};
+    return launch_mode<kModeDequantW16>(tmX, tmW, p, num_t * num_w, st);
 }
 
 cudaError_t launch_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t M, int64_t N, int64_t K, uint16_t *out,

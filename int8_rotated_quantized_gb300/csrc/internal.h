@@ -45,6 +45,14 @@ cudaError_t launch_widen_i8(const int8_t *A, int64_t count, uint16_t *out, cudaS
 cudaError_t launch_gemm(const uint16_t *A, const float *sa, const int8_t *B, const float *sb, const uint16_t *bias,
                         int64_t M, int64_t N, int64_t K, void *out, bool out_s32, unsigned *err, cudaStream_t st);
 
+// The dequantization GEMM on weight codes already widened to fp16 values
+// (B16 [N, K], from launch_widen_codes): same result as launch_gemm.
+cudaError_t launch_gemm_w16(const uint16_t *A, const float *sa, const uint16_t *B16, const float *sb,
+                            const uint16_t *bias, int64_t M, int64_t N, int64_t K, uint16_t *out, unsigned *err,
+                            cudaStream_t st);
+// int8 codes -> fp16 values holding the same integers, 32 per thread (rotq_wide.cu).
+cudaError_t launch_widen_codes(const int8_t *A, int64_t count, uint16_t *out, cudaStream_t st);
+
 // C[M,N] = bf16(A[M,K] . B[N,K]^T) with bf16 operands, fp32 accumulation.
 cudaError_t launch_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t M, int64_t N, int64_t K, uint16_t *out,
                              unsigned *err, cudaStream_t st);

@@ -170,6 +170,20 @@ __global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) lookup_wide_kernel(c
     }
 }
 
+// int8 codes -> fp16 values of the same integers: 32 codes per thread per
+// step (one 256-bit load, two 256-bit stores), grid-stride.
+__global__ void __launch_bounds__(kThreads) widen_codes_kernel(const int8_t *A, int64_t n32, uint16_t *out) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n32; i += (int64_t)gridDim.x * blockDim.x) {
+        uint32_t r[8];
+        ld256(A + 32 * i, r);
+        uint32_t w[16];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) widen4(r[k], w[2 * k], w[2 * k + 1]);
+        st256(out + 32 * i, w);
+        st256(out + 32 * i + 16, w + 8);
+    }
+}
+
 int log2_of(int b) {
     int l = 0;
     while ((1 << l) < b) ++l;
@@ -257,6 +271,19 @@ cudaError_t launch_rotq_wide(const uint16_t *x, int64_t rows, int64_t K, int64_t
                       : rotq_wide_dispatch<__half, 2>(logb, a, threads, nblocks, st);
     return S == 1 ? rotq_wide_dispatch<int8_t, 1>(logb, a, threads, nblocks, st)
                   : rotq_wide_dispatch<int8_t, 2>(logb, a, threads, nblocks, st);
+}
+
+cudaError_t launch_widen_codes(const int8_t *A, int64_t count, uint16_t *out, cudaStream_t st) {
+    if (count == 0) return cudaSuccess;
+    if (count % 32 != 0 || !a32(A) || !a32(out)) return launch_widen_i8(A, count, out, st);
+    const int64_t n32 = count / 32;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t want = (n32 + kThreads - 1) / kThreads;
+    const int64_t grid = want < (int64_t)sms * 4 ? want : (int64_t)sms * 4;
+    widen_codes_kernel<<<(unsigned)grid, kThreads, 0, st>>>(A, n32, out);
+    return cudaGetLastError();
 }
 
 bool lookup_wide_ok(const void *Eq, int64_t D, const void *out) {

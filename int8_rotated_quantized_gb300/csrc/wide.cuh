@@ -111,4 +111,19 @@ __device__ __forceinline__ float amax32(const float (&e)[32]) {
     return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
 }
 
+// int8 x 4 -> two fp16x2 words holding the same integers: bias each byte by
+// 128 (xor 0x80), splice it under the fp16 exponent of 1024 (0x64), and
+// subtract 1152 = 1024 + 128 exactly.
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t x = w ^ 0x80808080u;
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(x), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(x), "r"(0x64646464u));
+    const __half2 k = __half2half2(__ushort_as_half((unsigned short)0x6480));
+    __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), k);
+    __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), k);
+    lo = *reinterpret_cast<uint32_t *>(&ha);
+    hi = *reinterpret_cast<uint32_t *>(&hb);
+}
+
 }  // namespace convrot

@@ -30,7 +30,8 @@ import synth.gpu as sg  # noqa: E402
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["gemm", "gemm_bf16", "rotq", "lookup", "lora", "prep", "dequant", "wquant"])
+    ap.add_argument("case", choices=["gemm", "gemm_w16", "gemm_bf16", "widen", "rotq", "lookup", "lora", "prep",
+                                     "dequant", "wquant"])
     ap.add_argument("--M", type=int, default=8192)
     ap.add_argument("--N", type=int, default=16384)
     ap.add_argument("--K", type=int, default=4096)
@@ -54,6 +55,23 @@ def main():
         fn = lambda i: cr.convrot_gemm_dequant(xq, sx, Wq, sw, None, y)  # noqa: E731
         work = 2.0 * a.M * a.N * a.K
         unit = "TOPS"
+    elif a.case == "gemm_w16":
+        x = sg.activations_bf16(0, a.M, a.K, 41, 30.0, dev)
+        W = sg.normal_bf16(0, synth.STREAM_W, a.N, a.K, 0.02, dev)
+        Wq, sw = cr.convrot_quantize_weight(W, b)
+        W16 = cr.convrot_widen_codes(Wq)
+        xq, sx = cr.convrot_quantize_activation(x, b)
+        y = torch.empty((a.M, a.N), dtype=torch.bfloat16, device=dev)
+        fn = lambda i: cr.convrot_gemm_dequant_w16(xq, sx, W16, sw, None, y)  # noqa: E731
+        work = 2.0 * a.M * a.N * a.K
+        unit = "TOPS"
+    elif a.case == "widen":
+        W = sg.normal_bf16(0, synth.STREAM_W, a.N, a.K, 0.02, dev)
+        Wq, sw = cr.convrot_quantize_weight(W, b)
+        W16 = torch.empty((a.N, a.K), dtype=torch.float16, device=dev)
+        fn = lambda i: cr.convrot_widen_codes(Wq, W16)  # noqa: E731
+        work = 3 * a.N * a.K
+        unit = "GB/s"
     elif a.case == "gemm_bf16":
         A = sg.normal_bf16(0, synth.STREAM_DY, a.M, a.K, 1e-3, dev)
         B = sg.normal_bf16(0, synth.STREAM_W, a.N, a.K, 0.02, dev)

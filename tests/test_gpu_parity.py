@@ -227,6 +227,30 @@ def test_gemm_dequant_on_oracle_codes(with_bias):
     assert np.mean(yb == y_ref) > 0.99
 
 
+@pytest.mark.parametrize("M,K,N", [(300, 1024, 400), (64, 256, 128), (513, 4096, 272)])
+def test_widened_weight_path_is_bit_identical(M, K, N):
+    """The widened-weight path (fp16 copy of the codes in the workspace, GEMM without
+    in-loop widening) and the fused path give the same bits; both match the oracle."""
+    b = 128 if K % 128 == 0 else 32
+    x = synth.activations_bf16(19, M, K, 8, 30.0)
+    W = synth.normal_bf16(19, synth.STREAM_W, N, K, 0.02)
+    Wq, sw = cr.convrot_quantize_weight(torch_bf16(W), b)
+    w16 = cr.convrot_widen_codes(Wq)
+    assert torch.equal(w16.float(), Wq.float())
+    fast = cr.convrot_linear_fwd(torch_bf16(x), Wq, sw, b)
+    small = torch.empty(cr.convrot_act_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    fused = cr.convrot_linear_fwd(torch_bf16(x), Wq, sw, b, workspace=small)
+    assert torch.equal(fast, fused)
+    xq, sx = cr.convrot_quantize_activation(torch_bf16(x), b)
+    assert torch.equal(cr.convrot_gemm_dequant_w16(xq, sx, w16, sw), cr.convrot_gemm_dequant(xq, sx, Wq, sw))
+    y_ref, _, _ = oracle.linear_fwd(x, codes_of(Wq), sw.cpu().numpy(), b)
+    assert rel_fro(f64(bits_of(fast)), f64(y_ref)) <= REL_FRO_ORACLE
+    # int32 path of the widened operand: exact integer sums
+    A = np.random.default_rng(19).integers(-127, 128, size=(M, K), dtype=np.int8)
+    acc = cr.convrot_gemm_s32(_i8(A), Wq)
+    np.testing.assert_array_equal(acc.cpu().numpy(), oracle.gemm_s32(A, codes_of(Wq)))
+
+
 def test_linear_fwd_tiny_workload():
     wl = synth.WORKLOADS["tiny"]
     M, K, N, b = wl["M"], wl["K"], wl["N"], wl["block"]
