@@ -43,7 +43,7 @@ L2_FLUSH_BYTES = 256 << 20
 # keyed by the hash of the kernel source they were taken on; reported as null
 # once the kernel source differs (or where no capture was taken on it).
 GEMM_TRAFFIC = {"source_sha256_16": "c1dcb44dff9c1b49", "fwd": 869766144 + 651746560, "bwd": 3195821312 + 162856192,
-                "bf16_bwd": None}
+                "bf16_bwd": 3195284224 + 162341376}
 
 
 def _gemm_source_current():
