@@ -62,18 +62,40 @@ constexpr int NUM_THREADS = 512;
 constexpr int W8_STAGE = TW * BK;      // 8 KB int8 weight tile (TMA)
 constexpr int X_STAGE = TT * BK * 2;   // 32 KB fp16 activation tile (TMA)
 constexpr int WH_STAGE = TW * BK * 2;  // 16 KB widened weight tile
-constexpr int OFF_X = 0;
-constexpr int OFF_W8 = OFF_X + XSTAGES * X_STAGE;
-constexpr int OFF_WH = OFF_W8 + WSTAGES * W8_STAGE;
-constexpr int OFF_BAR = OFF_WH + CSTAGES * WH_STAGE;
-// Barrier indices.
-constexpr int BAR_X_FULL = 0, BAR_X_EMPTY = XSTAGES, BAR_W_FULL = 2 * XSTAGES, BAR_W_EMPTY = BAR_W_FULL + WSTAGES,
-              BAR_CONV_FULL = BAR_W_EMPTY + WSTAGES, BAR_CONV_EMPTY = BAR_CONV_FULL + CSTAGES,
-              BAR_ACC_FULL = BAR_CONV_EMPTY + CSTAGES, BAR_ACC_EMPTY = BAR_ACC_FULL + 2, BAR_DRAIN = BAR_ACC_EMPTY + 2,
-              NUM_BARS = BAR_DRAIN + 1;
-constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
-static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+// Kernel modes: integer codes with an int32 result; integer codes with the
+// dequantization epilogue; bf16 operands with a bf16 result (the bf16
+// backward of a frozen base: one fp32 accumulation over all of K); and the
+// dequantization epilogue on weight codes that a separate pass already
+// widened to fp16 (no converter in the loop, the same exact integer chunks).
+constexpr int kModeS32 = 0, kModeDequant = 1, kModeBf16 = 2, kModeDequantW16 = 3;
+// modes whose weight tiles arrive by TMA already in the MMA's format
+constexpr bool weight_direct(int mode) { return mode == kModeBf16 || mode == kModeDequantW16; }
+
+// Stages of the rings when the weight tiles arrive ready by TMA (widened-weight
+// and bf16 modes).  There is no int8 ring; the space it frees is left to the
+// L1 cache: deeper rings (4 + 5, 4 + 6, 5 + 4, 3 + 8) and shallower ones
+// (3 + 3, 3 + 4, 4 + 3) all measured slower than 4 + 4.
+constexpr int XSTAGES_D = 4, CSTAGES_D = 4;
+
+// Shared-memory layout of one kernel mode: ring offsets and barrier indices.
+template <int MODE>
+struct Layout {
+    static constexpr bool kDirect = weight_direct(MODE);
+    static constexpr int XS = kDirect ? XSTAGES_D : XSTAGES;  // activation ring
+    static constexpr int WS = kDirect ? 0 : WSTAGES;          // int8 weight ring
+    static constexpr int CS = kDirect ? CSTAGES_D : CSTAGES;  // ring the MMA reads the weights from
+    static constexpr int OFF_X = 0;
+    static constexpr int OFF_W8 = OFF_X + XS * X_STAGE;
+    static constexpr int OFF_WH = OFF_W8 + WS * W8_STAGE;
+    static constexpr int OFF_BAR = OFF_WH + CS * WH_STAGE;
+    static constexpr int BAR_X_FULL = 0, BAR_X_EMPTY = XS, BAR_W_FULL = 2 * XS, BAR_W_EMPTY = BAR_W_FULL + WS,
+                         BAR_CONV_FULL = BAR_W_EMPTY + WS, BAR_CONV_EMPTY = BAR_CONV_FULL + CS,
+                         BAR_ACC_FULL = BAR_CONV_EMPTY + CS, BAR_ACC_EMPTY = BAR_ACC_FULL + 2,
+                         BAR_DRAIN = BAR_ACC_EMPTY + 2, NUM_BARS = BAR_DRAIN + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
 constexpr int TMEM_COLS = 512;
 constexpr int REGS_WG0 = 48, REGS_CONV = 80, REGS_EPI = 184;
 static_assert(128 * REGS_WG0 + 128 * REGS_CONV + 256 * REGS_EPI <= 65536, "register split exceeds the launch pool");
@@ -84,14 +106,6 @@ static_assert(128 * REGS_WG0 + 128 * REGS_CONV + 256 * REGS_EPI <= 65536, "regis
 constexpr uint32_t kIdescF16 = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(TT >> 3) << 17) | ((uint32_t)(TW >> 4) << 24);
 constexpr uint32_t kIdescBF16 = kIdescF16 | (1u << 7) | (1u << 10);
 
-// Kernel modes: integer codes with an int32 result; integer codes with the
-// dequantization epilogue; bf16 operands with a bf16 result (the bf16
-// backward of a frozen base: one fp32 accumulation over all of K); and the
-// dequantization epilogue on weight codes that a separate pass already
-// widened to fp16 (no converter in the loop, the same exact integer chunks).
-constexpr int kModeS32 = 0, kModeDequant = 1, kModeBf16 = 2, kModeDequantW16 = 3;
-// modes whose weight tiles arrive by TMA already in the MMA's format
-constexpr bool weight_direct(int mode) { return mode == kModeBf16 || mode == kModeDequantW16; }
 
 struct GemmArgs {
     int M, N, K;
@@ -200,37 +214,38 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_s8_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const GemmArgs p) {
+    using L = Layout<MODE>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base - raw);
-    const uint32_t sX = base + OFF_X, sW8 = base + OFF_W8, sWh = base + OFF_WH, sBar = base + OFF_BAR;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+    const uint32_t sX = base + L::OFF_X, sW8 = base + L::OFF_W8, sWh = base + L::OFF_WH, sBar = base + L::OFF_BAR;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_MISC + 4);
     auto bar = [&](int i) -> uint32_t { return sBar + 8u * (uint32_t)i; };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < XSTAGES; ++i) {
-            mbar_init(bar(BAR_X_FULL + i), 1);
-            mbar_init(bar(BAR_X_EMPTY + i), 1);  // MMA commit
+        for (int i = 0; i < L::XS; ++i) {
+            mbar_init(bar(L::BAR_X_FULL + i), 1);
+            mbar_init(bar(L::BAR_X_EMPTY + i), 1);  // MMA commit
         }
-        for (int i = 0; i < WSTAGES; ++i) {
-            mbar_init(bar(BAR_W_FULL + i), 1);
-            mbar_init(bar(BAR_W_EMPTY + i), 4);  // 4 converter warps
+        for (int i = 0; i < L::WS; ++i) {
+            mbar_init(bar(L::BAR_W_FULL + i), 1);
+            mbar_init(bar(L::BAR_W_EMPTY + i), 4);  // 4 converter warps
         }
-        for (int i = 0; i < CSTAGES; ++i) {
+        for (int i = 0; i < L::CS; ++i) {
             // converted by the 4 converter warps, or (bf16 mode) loaded by TMA
-            mbar_init(bar(BAR_CONV_FULL + i), weight_direct(MODE) ? 1 : 4);
-            mbar_init(bar(BAR_CONV_EMPTY + i), 1);
+            mbar_init(bar(L::BAR_CONV_FULL + i), weight_direct(MODE) ? 1 : 4);
+            mbar_init(bar(L::BAR_CONV_EMPTY + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(BAR_ACC_FULL + i), 1);
-            mbar_init(bar(BAR_ACC_EMPTY + i), 8);
+            mbar_init(bar(L::BAR_ACC_FULL + i), 1);
+            mbar_init(bar(L::BAR_ACC_EMPTY + i), 8);
         }
-        mbar_init(bar(BAR_DRAIN), 1);
+        mbar_init(bar(L::BAR_DRAIN), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -263,9 +278,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // ring the MMA reads (freed by the MMA).
             const bool is_x = warp == 0;
             const bool w_direct = !is_x && weight_direct(MODE);
-            const int nst = is_x ? XSTAGES : w_direct ? CSTAGES : WSTAGES;
-            const int full0 = is_x ? BAR_X_FULL : w_direct ? BAR_CONV_FULL : BAR_W_FULL;
-            const int empty0 = is_x ? BAR_X_EMPTY : w_direct ? BAR_CONV_EMPTY : BAR_W_EMPTY;
+            const int nst = is_x ? L::XS : w_direct ? L::CS : L::WS;
+            const int full0 = is_x ? L::BAR_X_FULL : w_direct ? L::BAR_CONV_FULL : L::BAR_W_FULL;
+            const int empty0 = is_x ? L::BAR_X_EMPTY : w_direct ? L::BAR_CONV_EMPTY : L::BAR_W_EMPTY;
             const CUtensorMap *map = is_x ? &tmX : &tmW;
             asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
             int it = 0;
@@ -305,17 +320,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int kc = kb % chunk_kb;
                     if (kc == 0) {
                         const int buf = g & 1;
-                        if (!mbar_wait(bar(BAR_ACC_EMPTY + buf), ((g >> 1) & 1) ^ 1, abort_flag, p.err)) {
+                        if (!mbar_wait(bar(L::BAR_ACC_EMPTY + buf), ((g >> 1) & 1) ^ 1, abort_flag, p.err)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         dcol = (uint32_t)(buf * TT);
                     }
-                    const int s = it % XSTAGES;
-                    const int c = it % CSTAGES;
-                    if (!mbar_wait(bar(BAR_X_FULL + s), (it / XSTAGES) & 1, abort_flag, p.err) ||
-                        !mbar_wait(bar(BAR_CONV_FULL + c), (it / CSTAGES) & 1, abort_flag, p.err)) {
+                    const int s = it % L::XS;
+                    const int c = it % L::CS;
+                    if (!mbar_wait(bar(L::BAR_X_FULL + s), (it / L::XS) & 1, abort_flag, p.err) ||
+                        !mbar_wait(bar(L::BAR_CONV_FULL + c), (it / L::CS) & 1, abort_flag, p.err)) {
                         ok = false;
                         break;
                     }
@@ -327,17 +342,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         umma_f16(tmem + dcol, ad, bd, MODE == kModeBf16 ? kIdescBF16 : kIdescF16,
                                  (kc > 0 || kk > 0) ? 1u : 0u);
                     }
-                    umma_commit(bar(BAR_X_EMPTY + s));
-                    umma_commit(bar(BAR_CONV_EMPTY + c));
+                    umma_commit(bar(L::BAR_X_EMPTY + s));
+                    umma_commit(bar(L::BAR_CONV_EMPTY + c));
                     if (kc == chunk_kb - 1 || kb == num_kb - 1) {
-                        umma_commit(bar(BAR_ACC_FULL + (g & 1)));
+                        umma_commit(bar(L::BAR_ACC_FULL + (g & 1)));
                         ++g;
                     }
                 }
             }
             // All MMAs issued by this thread have completed once this fires.
-            umma_commit(bar(BAR_DRAIN));
-            mbar_wait_drain(bar(BAR_DRAIN), 0);
+            umma_commit(bar(L::BAR_DRAIN));
+            mbar_wait_drain(bar(L::BAR_DRAIN), 0);
         }
         __syncwarp();
         end_barrier();
@@ -348,20 +363,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp < 8) {
         // ----------------------------------------------------------- converters
         regs_dec<REGS_CONV>();
+        if constexpr (!L::kDirect) {  // nothing to widen when the weight tiles come ready
         const int ct = threadIdx.x - 128;
         int it = 0;
-        bool ok = !weight_direct(MODE);  // nothing to widen when the weight tiles come ready
+        bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
             for (int kb = 0; kb < num_kb; ++kb, ++it) {
-                const int s = it % WSTAGES;
-                const int c = it % CSTAGES;
-                if (!warp_wait(bar(BAR_W_FULL + s), (it / WSTAGES) & 1, abort_flag, p.err, lane) ||
-                    !warp_wait(bar(BAR_CONV_EMPTY + c), ((it / CSTAGES) & 1) ^ 1, abort_flag, p.err, lane)) {
+                const int s = it % L::WS;
+                const int c = it % L::CS;
+                if (!warp_wait(bar(L::BAR_W_FULL + s), (it / L::WS) & 1, abort_flag, p.err, lane) ||
+                    !warp_wait(bar(L::BAR_CONV_EMPTY + c), ((it / L::CS) & 1) ^ 1, abort_flag, p.err, lane)) {
                     ok = false;
                     break;
                 }
-                const uint8_t *src = smem + OFF_W8 + s * W8_STAGE;
-                uint8_t *dst = smem + OFF_WH + c * WH_STAGE;
+                const uint8_t *src = smem + L::OFF_W8 + s * W8_STAGE;
+                uint8_t *dst = smem + L::OFF_WH + c * WH_STAGE;
                 // 128 rows x 64 int8 (rows of 64 bytes, no swizzle) -> 128 rows x 64 fp16
                 // in 128B-swizzle atoms (8 rows x 128 bytes, 16-byte chunk j of row r at j ^ (r & 7)).
                 uint4 v[(TW * BK / 16) / 128];
@@ -388,10 +404,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(bar(BAR_W_EMPTY + s));
-                    mbar_arrive(bar(BAR_CONV_FULL + c));
+                    mbar_arrive(bar(L::BAR_W_EMPTY + s));
+                    mbar_arrive(bar(L::BAR_CONV_FULL + c));
                 }
             }
+        }
         }
         end_barrier();
     } else {
@@ -410,7 +427,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
             for (int ch = 0; ch < nchunks; ++ch, ++g) {
                 const int buf = g & 1;
-                if (!warp_wait(bar(BAR_ACC_FULL + buf), (g >> 1) & 1, abort_flag, p.err, lane)) {
+                if (!warp_wait(bar(L::BAR_ACC_FULL + buf), (g >> 1) & 1, abort_flag, p.err, lane)) {
                     ok = false;
                     break;
                 }
@@ -431,7 +448,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(BAR_ACC_EMPTY + buf));
+                if (lane == 0) mbar_arrive(bar(L::BAR_ACC_EMPTY + buf));
             }
             if (!ok) break;
             // Thread = weight row n, registers = 128 consecutive tokens m: each
@@ -547,9 +564,10 @@ cudaError_t launch_mode(const CUtensorMap &tmX, const CUtensorMap &tmW, const Ge
                         cudaStream_t st) {
     const int sms = sm_count_of_current_device();
     const int grid = (int)(tiles < sms ? tiles : sms);
-    cudaError_t e = cudaFuncSetAttribute(gemm_s8_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    constexpr int kSmem = Layout<MODE>::SMEM_BYTES;
+    cudaError_t e = cudaFuncSetAttribute(gemm_s8_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    gemm_s8_tc_kernel<MODE><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(tmX, tmW, p);
+    gemm_s8_tc_kernel<MODE><<<grid, NUM_THREADS, kSmem, st>>>(tmX, tmW, p);
     return cudaGetLastError();
 }
 
