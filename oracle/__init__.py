@@ -60,6 +60,7 @@ def _load():
                 "oracle_embedding_lookup": [P, I64, P, P, I64, I64, I, P, P],
                 "oracle_dequant_weight_t": [P, P, I64, I64, I, P],
                 "oracle_gemm_bf16": [P, P, I64, I64, I64, P],
+                "oracle_linear_fwd_lora": [P, I64, I64, P, P, I64, I, P, P, P, I, F, F, P],
                 "oracle_num_threads": [],
             }
             for name, args in sig.items():
@@ -177,6 +178,22 @@ def linear_fwd(x_bits, Wq, s_w, b: int, bias_bits=None):
     _check(_load().oracle_linear_fwd(_p(x), M, K, _p(Wq), _p(_c(s_w, np.float32)), N, b,
                                      _p(_c(bias_bits, np.uint16)), _p(y), _p(xq), _p(sx)), "linear_fwd")
     return y, xq, sx
+
+
+def linear_fwd_lora(x_bits, Wq, s_w, b: int, A, B, alpha: float, scale: float, bias_bits=None) -> np.ndarray:
+    """Forward with the LoRA branch as a bypass (not merged): bf16 bits [M, N]."""
+    x = _c(x_bits, np.uint16)
+    Wq = _c(Wq, np.int8)
+    A = _c(A, np.float32)
+    B = _c(B, np.float32)
+    M, K = x.shape
+    N = Wq.shape[0]
+    rank = A.shape[0]
+    y = np.empty((M, N), dtype=np.uint16)
+    _check(_load().oracle_linear_fwd_lora(_p(x), M, K, _p(Wq), _p(_c(s_w, np.float32)), N, b,
+                                          _p(_c(bias_bits, np.uint16)), _p(A), _p(B), rank, alpha, scale, _p(y)),
+           "linear_fwd_lora")
+    return y
 
 
 def prepare_bwd_weight(Wq, s_w, b: int):

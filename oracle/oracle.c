@@ -45,6 +45,9 @@
  *       dX = bf16(acc * s_dy * s_wt).
  *   R7  Embedding lookup: out[t] = bf16_rne((s[id] * Eq[id,:]) R), fp64; an id
  *       outside [0, V) yields a zero row and is counted.
+ *   R9  LoRA bypass in the forward: instead of merging, the adapter's branch
+ *       c * (x A^T) B^T on the unrotated input is added to the dequantized
+ *       product before the output rounding (fp64 here).
  *   R8  bf16 backward (the default mode of the pages' backward option): the
  *       frozen base is dequantized transiently, W_eff = bf16_rne((s_w (.) Wq) R)
  *       (fp64 before the rounding), and dX = bf16_rne(dY . W_eff) summed in fp64.
@@ -360,6 +363,55 @@ int oracle_linear_fwd(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq,
     if (!sx_out)
         free(sx);
     free(acc);
+    return rc;
+}
+
+/* LoRA bypass in the forward (R9): the adapter is not merged into W; its
+ * branch sees the unrotated input and is added before the output rounding:
+ *   y = bf16(acc * s_x * s_w + bias + c * sum_j (sum_k x[m,k] A[j,k]) B[n,j])
+ * in fp64, c = fp32(scale * alpha / rank), A [rank, K], B [N, rank] fp32. */
+int oracle_linear_fwd_lora(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq, const float *s_w,
+                           int64_t N, int b, const uint16_t *bias, const float *A, const float *B, int rank,
+                           float alpha, float scale, uint16_t *y)
+{
+    if (rank <= 0)
+        return 1;
+    int8_t *xq = malloc((size_t)M * (size_t)K);
+    float *sx = malloc(sizeof(float) * (size_t)M);
+    int32_t *acc = malloc(sizeof(int32_t) * (size_t)M * (size_t)N);
+    double *xa = malloc(sizeof(double) * (size_t)M * (size_t)rank);
+    int rc = 2;
+    if (xq && sx && acc && xa) {
+        rc = oracle_quantize_rows_bf16(x, M, K, K, b, xq, sx);
+        if (rc == 0)
+            rc = oracle_gemm_s32(xq, Wq, M, N, K, acc);
+        if (rc == 0) {
+            double c = (double)(float)((double)scale * (double)alpha / (double)rank);
+#pragma omp parallel for schedule(static)
+            for (int64_t m = 0; m < M; m++)
+                for (int j = 0; j < rank; j++) {
+                    double d = 0.0;
+                    for (int64_t k = 0; k < K; k++)
+                        d += bf16_to_f64(x[m * K + k]) * (double)A[(int64_t)j * K + k];
+                    xa[m * rank + j] = d;
+                }
+#pragma omp parallel for schedule(static)
+            for (int64_t m = 0; m < M; m++)
+                for (int64_t n = 0; n < N; n++) {
+                    double v = (double)acc[m * N + n] * (double)sx[m] * (double)s_w[n];
+                    if (bias)
+                        v += bf16_to_f64(bias[n]);
+                    double l = 0.0;
+                    for (int j = 0; j < rank; j++)
+                        l += xa[m * rank + j] * (double)B[n * rank + j];
+                    y[m * N + n] = f64_to_bf16(v + c * l);
+                }
+        }
+    }
+    free(xq);
+    free(sx);
+    free(acc);
+    free(xa);
     return rc;
 }
 

@@ -276,6 +276,29 @@ def test_lora_merge_identities_and_value():
     assert np.array_equal(q0, qp) and np.array_equal(s0, sp)
 
 
+def test_lora_bypass_forward():
+    M, K, N, b, r = 24, 256, 64, 32, 8
+    x = synth.activations_bf16(20, M, K, 4, 20.0)
+    w = synth.normal_bf16(20, synth.STREAM_W, N, K, 0.02)
+    A, B = synth.lora_pair(20, N, K, r, 0.05)
+    wq, sw = oracle.quantize_weight(w, b)
+    # scale 0 is the plain forward, bit for bit
+    y0, _, _ = oracle.linear_fwd(x, wq, sw, b)
+    np.testing.assert_array_equal(oracle.linear_fwd_lora(x, wq, sw, b, A, B, 16.0, 0.0), y0)
+    # zero weight codes leave only the branch: the closed form c * x A^T B^T (numpy), one bf16 rounding
+    c = float(np.float32(1.0 * 16.0 / r))
+    yz = oracle.linear_fwd_lora(x, np.zeros_like(wq), sw, b, A, B, 16.0, 1.0)
+    ref = _bf16(c * ((_f64(x) @ A.astype(np.float64).T) @ B.astype(np.float64).T))
+    assert np.all(np.abs(yz.astype(np.int32) - ref.astype(np.int32)) <= 1)
+    # the bypass and the merged weight compute the same layer up to quantization
+    y = oracle.linear_fwd_lora(x, wq, sw, b, A, B, 16.0, 1.0)
+    merged = _f64(w) + c * (B.astype(np.float64) @ A.astype(np.float64))
+    full = _f64(x) @ merged.T
+    assert np.linalg.norm(_f64(y) - full) / np.linalg.norm(full) < 5e-2
+    lora_only = c * (_f64(x) @ A.astype(np.float64).T) @ B.astype(np.float64).T
+    assert np.linalg.norm(lora_only) > 0.1 * np.linalg.norm(full)   # the branch is not negligible here
+
+
 # ------------------------------------------------------------------ backward
 
 
