@@ -383,7 +383,21 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
     rows["a1a2_lora_merge_quant"].update({"fma_per_s_T": round(fma / (ms * 1e-3) / 1e12, 2),
                                           "fma_peak_T": round(fma_peak / 1e12, 2),
                                           "fma_frac": round(fma / (ms * 1e-3) / fma_peak, 4)})
-    del W3, Wq3, A, B
+    # next row 2: the same adapter as an unmerged bypass in the forward (x [4096,4096] of the qkv workload)
+    M3 = wl3["M"]
+    x3 = sg.activations_bf16(0, M3, K3, wl3["x_outliers"], wl3["x_factor"], dev)
+    Wq3p, sw3p = cr.convrot_quantize_weight(W3, b)
+    y3 = torch.empty((M3, N3), dtype=torch.bfloat16, device=dev)
+    wsl = torch.empty(cr.convrot_linear_lora_workspace_bytes(M3, K3, N3), dtype=torch.uint8, device=dev)
+    wsp = torch.empty(cr.convrot_linear_workspace_bytes(M3, K3, N3), dtype=torch.uint8, device=dev)
+    ms_l = _time(torch, lambda i: cr.convrot_linear_fwd_lora(x3, Wq3p, sw3p, b, A, B, wl3["lora_alpha"],
+                                                             wl3["lora_scale"], y=y3, workspace=wsl), flush, reps)
+    ms_p = _time(torch, lambda i: cr.convrot_linear_fwd(x3, Wq3p, sw3p, b, y=y3, workspace=wsp), flush, reps)
+    rows["n2_lora_bypass_fwd"] = _tc_row(2.0 * M3 * N3 * K3, ms_l, pk,
+                                         "C3 x [4096,4096] . W [12288,4096] + LoRA r16 bypass, whole forward call")
+    rows["n2_lora_bypass_fwd"].update({"plain_fwd_ms": round(ms_p, 4),
+                                       "bypass_overhead_frac": round(ms_l / ms_p - 1.0, 4)})
+    del W3, Wq3, A, B, x3, Wq3p, sw3p, y3, wsl, wsp
     # a7: embedding table quantization (row-chunked: 8 slabs of 31000 rows)
     wl5 = synth.WORKLOADS["embed"]
     V, D = wl5["V"], wl5["D"]

@@ -156,6 +156,24 @@ CONVROT_API int convrot_linear_fwd(const uint16_t *x, int64_t M, int64_t K, cons
                        const float *scale_w, int64_t N, int block, const uint16_t *bias,
                        uint16_t *y, void *workspace, size_t ws_bytes, convrot_stream_t stream);
 
+/* Bytes of workspace convrot_linear_fwd_lora needs: those of the widened-weight
+ * path plus the scaled down-projection (16 rows of M rounded up to 256, fp32). */
+CONVROT_API size_t convrot_linear_lora_workspace_bytes(int64_t M, int64_t K, int64_t N);
+
+/* Forward with an unmerged LoRA adapter as a bypass (the LoRA branch of a
+ * frozen ConvRot layer sees the unrotated input; guide 7.1, PR #2461 Summary;
+ * the merge formula of the voxprint-model-forge MOSS page gives the scaling):
+ *   y = bf16( acc * scale_x[m] * scale_w[n] + bias[n]
+ *             + sum_j (coef * sum_k x[m,k] lora_A[j,k]) * lora_B[n,j] ),
+ *   coef = fp32(scale * alpha / rank), the branch summed in fp32.
+ * x bf16 [M, K] (K multiple of 32); lora_A fp32 [rank, K] (16-byte aligned); lora_B fp32 [N, rank];
+ * 1 <= rank <= 16; workspace >= convrot_linear_lora_workspace_bytes(M, K, N),
+ * 256-byte aligned.  Weight codes as in convrot_linear_fwd. */
+CONVROT_API int convrot_linear_fwd_lora(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq,
+                            const float *scale_w, int64_t N, int block, const uint16_t *bias,
+                            const float *lora_A, const float *lora_B, int rank, float alpha, float scale,
+                            uint16_t *y, void *workspace, size_t ws_bytes, convrot_stream_t stream);
+
 /* Forward without a workspace, for callers that cannot allocate device
  * memory on this path: a host framework or plugin that only passes in
  * pointers to memory it owns, a latency-critical loop where cudaMalloc (which

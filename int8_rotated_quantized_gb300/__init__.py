@@ -58,6 +58,8 @@ def lib():
                 "convrot_embedding_lookup": ([P, I64, P, P, I64, I64, I, P, P], I),
                 "convrot_dequant_weight_t": ([P, P, I64, I64, I, P, P], I),
                 "convrot_linear_workspace_bytes": ([I64, I64, I64], S),
+                "convrot_linear_lora_workspace_bytes": ([I64, I64, I64], S),
+                "convrot_linear_fwd_lora": ([P, I64, I64, P, P, I64, I, P, P, P, I, F, F, P, P, S, P], I),
                 "convrot_widen_codes": ([P, I64, P, P], I),
                 "convrot_gemm_dequant_w16": ([P, P, I64, I64, P, P, I64, P, P, P], I),
                 "convrot_gemm_bf16": ([P, I64, I64, P, I64, P, P], I),
@@ -244,6 +246,35 @@ def convrot_linear_fwd(x, Wq, scale_w, block, bias=None, y=None, workspace=None,
     ws, nbytes = _linear_ws(M, K, N, x.device, workspace)
     _check(lib().convrot_linear_fwd(_ptr(x), M, K, _ptr(Wq), _ptr(scale_w), N, block, _ptr(bias), _ptr(y), _ptr(ws),
                                     nbytes, _stream(stream)), "convrot_linear_fwd")
+    return y
+
+
+def convrot_linear_lora_workspace_bytes(M: int, K: int, N: int) -> int:
+    return lib().convrot_linear_lora_workspace_bytes(M, K, N)
+
+
+def convrot_linear_fwd_lora(x, Wq, scale_w, block, lora_A, lora_B, alpha, scale=1.0, bias=None, y=None,
+                            workspace=None, stream=None):
+    """Forward with an unmerged LoRA adapter as a bypass branch on the unrotated input."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(Wq, torch.int8, "Wq", 2)
+    _need(scale_w, torch.float32, "scale_w", 1)
+    _need(lora_A, torch.float32, "lora_A", 2)
+    _need(lora_B, torch.float32, "lora_B", 2)
+    if bias is not None:
+        _need(bias, torch.bfloat16, "bias", 1)
+    M, K = x.shape
+    N = Wq.shape[0]
+    rank = lora_A.shape[0]
+    if Wq.shape[1] != K or lora_A.shape[1] != K or lora_B.shape != (N, rank):
+        raise ValueError("shape mismatch")
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    nbytes = convrot_linear_lora_workspace_bytes(M, K, N)
+    ws = _workspace(nbytes, x.device, workspace)
+    _check(lib().convrot_linear_fwd_lora(_ptr(x), M, K, _ptr(Wq), _ptr(scale_w), N, block, _ptr(bias), _ptr(lora_A),
+                                         _ptr(lora_B), rank, alpha, scale, _ptr(y), _ptr(ws), nbytes,
+                                         _stream(stream)), "convrot_linear_fwd_lora")
     return y
 
 

@@ -209,6 +209,43 @@ int convrot_linear_fwd(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq
     return gemm_impl(xq, sx, M, K, Wq, scale_w, N, bias, y, err, st);
 }
 
+size_t convrot_linear_lora_workspace_bytes(int64_t M, int64_t K, int64_t N) {
+    if (M < 0 || K < 0 || N < 0) return 0;
+    return convrot_linear_workspace_bytes(M, K, N) + align256((size_t)convrot::lora_xa_ld(M) * 16 * sizeof(float));
+}
+
+int convrot_linear_fwd_lora(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq, const float *scale_w,
+                            int64_t N, int block, const uint16_t *bias, const float *lora_A, const float *lora_B,
+                            int rank, float alpha, float scale, uint16_t *y, void *workspace, size_t ws_bytes,
+                            convrot_stream_t stream) {
+    CHECK(block_ok(block) && row_ok(K, block) && K % 32 == 0 && M >= 0 && N >= 0 && N % 16 == 0);
+    CHECK(M <= INT32_MAX && N <= INT32_MAX && rank >= 1 && rank <= 16);
+    CHECK(M == 0 || N == 0 ||
+          (x && Wq && scale_w && y && lora_A && lora_B && workspace && aligned16(x) && aligned16(Wq) &&
+           aligned16(y) && aligned16(scale_w) && aligned16(lora_A) && ((uintptr_t)lora_B & 3u) == 0 &&
+           ((uintptr_t)workspace & 255u) == 0 && (bias == nullptr || aligned16(bias))));
+    CHECK(M == 0 || N == 0 || ws_bytes >= convrot_linear_lora_workspace_bytes(M, K, N));
+    unsigned *err = nullptr;
+    int rc = device_setup(&err);
+    if (rc != CONVROT_OK) return rc;
+    if (M == 0 || N == 0) return CONVROT_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    char *ws = static_cast<char *>(workspace);
+    uint16_t *xq = reinterpret_cast<uint16_t *>(ws);
+    float *sx = reinterpret_cast<float *>(ws + align256((size_t)M * (size_t)K * 2));
+    uint16_t *w16 = reinterpret_cast<uint16_t *>(ws + convrot_act_workspace_bytes(M, K));
+    float *xa = reinterpret_cast<float *>(ws + convrot_linear_workspace_bytes(M, K, N));
+    const float coef = (float)((double)scale * (double)alpha / (double)rank);
+    rc = quantize_act_impl(x, M, K, K, block, xq, sx, st);
+    if (rc != CONVROT_OK) return rc;
+    rc = cuda_status(convrot::launch_lora_down(x, M, K, lora_A, rank, coef, xa, st));
+    if (rc != CONVROT_OK) return rc;
+    rc = cuda_status(convrot::launch_widen_codes(Wq, N * K, w16, st));
+    if (rc != CONVROT_OK) return rc;
+    return cuda_status(
+        convrot::launch_gemm_w16_lora(xq, sx, w16, scale_w, bias, xa, lora_B, rank, M, N, K, y, err, st));
+}
+
 size_t convrot_bwd_weight_workspace_bytes(int64_t N, int64_t K) {
     if (N < 0 || K < 0) return 0;
     return align256((size_t)N * (size_t)K * 2 * sizeof(float));

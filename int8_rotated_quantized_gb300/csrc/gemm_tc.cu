@@ -68,8 +68,13 @@ constexpr int WH_STAGE = TW * BK * 2;  // 16 KB widened weight tile
 // dequantization epilogue on weight codes that a separate pass already
 // widened to fp16 (no converter in the loop, the same exact integer chunks).
 constexpr int kModeS32 = 0, kModeDequant = 1, kModeBf16 = 2, kModeDequantW16 = 3;
+// The widened-weight dequantization mode plus a LoRA bypass term in the
+// epilogue: y += sum_j xa[m, j] * B[n, j] (xa already scaled, stored transposed).
+constexpr int kModeDequantW16Lora = 4;
 // modes whose weight tiles arrive by TMA already in the MMA's format
-constexpr bool weight_direct(int mode) { return mode == kModeBf16 || mode == kModeDequantW16; }
+constexpr bool weight_direct(int mode) {
+    return mode == kModeBf16 || mode == kModeDequantW16 || mode == kModeDequantW16Lora;
+}
 
 // Stages of the rings when the weight tiles arrive ready by TMA (widened-weight
 // and bf16 modes).  There is no int8 ring; the space it frees is left to the
@@ -87,11 +92,17 @@ struct Layout {
     static constexpr int OFF_X = 0;
     static constexpr int OFF_W8 = OFF_X + XS * X_STAGE;
     static constexpr int OFF_WH = OFF_W8 + WS * W8_STAGE;
-    static constexpr int OFF_BAR = OFF_WH + CS * WH_STAGE;
+    // bypass mode: the down-projection of the tile's tokens, [2 halves][16][128] fp32
+    static constexpr int XA_BYTES = MODE == kModeDequantW16Lora ? 2 * 16 * 128 * 4 : 0;
+    static constexpr int OFF_XA = OFF_WH + CS * WH_STAGE;
+    static constexpr int OFF_BAR = OFF_XA + XA_BYTES;
     static constexpr int BAR_X_FULL = 0, BAR_X_EMPTY = XS, BAR_W_FULL = 2 * XS, BAR_W_EMPTY = BAR_W_FULL + WS,
                          BAR_CONV_FULL = BAR_W_EMPTY + WS, BAR_CONV_EMPTY = BAR_CONV_FULL + CS,
                          BAR_ACC_FULL = BAR_CONV_EMPTY + CS, BAR_ACC_EMPTY = BAR_ACC_FULL + 2,
-                         BAR_DRAIN = BAR_ACC_EMPTY + 2, NUM_BARS = BAR_DRAIN + 1;
+                         BAR_DRAIN = BAR_ACC_EMPTY + 2,
+                         BAR_XS_READY = BAR_DRAIN + 1,  // bypass rows staged (per half, 128 arrivals)
+                         BAR_XS_FREE = BAR_XS_READY + 2,  // bypass rows read (per half, 4 warp arrivals)
+                         NUM_BARS = BAR_XS_FREE + 2;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -115,6 +126,10 @@ struct GemmArgs {
     const uint16_t *bias;
     void *out;
     unsigned *err;
+    const float *lora_xa;  // [16][lora_ld], transposed, coef folded in (bypass mode)
+    const float *lora_b;   // [N, lora_rank] (bypass mode)
+    int lora_rank;
+    int64_t lora_ld;       // row stride of lora_xa: M rounded up to 256
 };
 
 // ------------------------------------------------------------- PTX wrappers --
@@ -246,6 +261,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar(L::BAR_ACC_EMPTY + i), 8);
         }
         mbar_init(bar(L::BAR_DRAIN), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(L::BAR_XS_READY + i), 128);
+            mbar_init(bar(L::BAR_XS_FREE + i), 4);
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -416,11 +435,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         regs_inc<REGS_EPI>();
         const int q = warp & 3;          // TMEM lane quarter = weight rows 32q .. 32q+31
         const int h = (warp - 8) >> 2;   // token half of the 256-wide tile
-        int g = 0;
+        int g = 0, u = 0;  // u: tiles this CTA has processed
         bool ok = true;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++u) {
             int tb, wb;
             tile_coords(tile, num_t, num_w, p.group, p.group_weight != 0, tb, wb);
+            if constexpr (MODE == kModeDequantW16Lora) {
+                // stage this half-tile's bypass rows (rank x 128 tokens) in shared memory
+                // while the chunks accumulate, once the four warps of this half have read
+                // the previous tile's rows (bounded waits, like every pipeline wait)
+                if (u > 0 && !warp_wait(bar(L::BAR_XS_FREE + h), (u - 1) & 1, abort_flag, p.err, lane)) {
+                    ok = false;
+                    break;
+                }
+                const float *xt = p.lora_xa + (int64_t)tb * TT + h * 128;
+                float *xs = reinterpret_cast<float *>(smem + L::OFF_XA) + h * 16 * 128;
+                const int ht = threadIdx.x & 127;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int idx = ht + 128 * r, j = idx >> 5, c4 = idx & 31;
+                    if (j < p.lora_rank)
+                        *reinterpret_cast<float4 *>(xs + j * 128 + 4 * c4) =
+                            __ldg(reinterpret_cast<const float4 *>(xt + (int64_t)j * p.lora_ld + 4 * c4));
+                }
+                mbar_arrive(bar(L::BAR_XS_READY + h));
+            }
             int acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0;
@@ -457,6 +496,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int m0 = tb * TT + h * 128;
             const int mlim = p.M - m0;  // tokens of this column half that exist
             const bool full = mlim >= 128;
+            if constexpr (MODE == kModeDequantW16Lora) {  // every thread of the half takes part
+                if (!warp_wait(bar(L::BAR_XS_READY + h), u & 1, abort_flag, p.err, lane)) {
+                    ok = false;
+                    break;
+                }
+            }
             if (n < p.N) {
                 if constexpr (MODE == kModeS32) {
                     int32_t *out = static_cast<int32_t *>(p.out) + (int64_t)m0 * p.N + n;
@@ -466,6 +511,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         out += p.N;
                     }
                 } else if constexpr (MODE == kModeBf16) {
+                    uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)m0 * p.N + n;
+#pragma unroll
+                    for (int i = 0; i < 128; ++i) {
+                        if (full || i < mlim) *out = (uint16_t)float_to_bf16_bits(__int_as_float(acc[i]));
+                        out += p.N;
+                    }
+                } else if constexpr (MODE == kModeDequantW16Lora) {
+                    // pass 1: y = acc * (sx * sw) + bias in place (the registers now hold fp32)
+                    const float swn = __ldg(p.sb + n);
+                    const bool has_bias = p.bias != nullptr;
+                    const float bn = has_bias ? bf16_bits_to_float(__ldg(p.bias + n)) : 0.f;
+#pragma unroll
+                    for (int i4 = 0; i4 < 128; i4 += 4) {
+                        float sx[4];
+                        if (full) {
+                            const float4 v = __ldg(reinterpret_cast<const float4 *>(p.sa + m0 + i4));
+                            sx[0] = v.x, sx[1] = v.y, sx[2] = v.z, sx[3] = v.w;
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) sx[j] = i4 + j < mlim ? __ldg(p.sa + m0 + i4 + j) : 0.f;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            float y = __fmul_rn(__int2float_rn(acc[i4 + j]), __fmul_rn(sx[j], swn));
+                            if (has_bias) y = __fadd_rn(y, bn);
+                            acc[i4 + j] = __float_as_int(y);
+                        }
+                    }
+                    // pass 2: the bypass branch on the unrotated input, y += sum_j xa[m, j] B[n, j]
+                    // in j order, from the staged rows (transposed, coef folded in): each load
+                    // brings 4 consecutive tokens of one j and the 128 sums are independent
+                    const float *xs = reinterpret_cast<const float *>(smem + L::OFF_XA) + h * 16 * 128;
+                    for (int j = 0; j < p.lora_rank; ++j) {
+                        const float bj = __ldg(p.lora_b + (int64_t)n * p.lora_rank + j);
+                        const float4 *row = reinterpret_cast<const float4 *>(xs + j * 128);
+#pragma unroll
+                        for (int i4 = 0; i4 < 128; i4 += 4) {
+                            const float4 v = row[i4 >> 2];  // every lane reads the same 16 bytes
+                            acc[i4] = __float_as_int(__fmaf_rn(v.x, bj, __int_as_float(acc[i4])));
+                            acc[i4 + 1] = __float_as_int(__fmaf_rn(v.y, bj, __int_as_float(acc[i4 + 1])));
+                            acc[i4 + 2] = __float_as_int(__fmaf_rn(v.z, bj, __int_as_float(acc[i4 + 2])));
+                            acc[i4 + 3] = __float_as_int(__fmaf_rn(v.w, bj, __int_as_float(acc[i4 + 3])));
+                        }
+                    }
+                    // pass 3: round and store
                     uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)m0 * p.N + n;
 #pragma unroll
                     for (int i = 0; i < 128; ++i) {
@@ -496,6 +586,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                 }
+            }
+            if constexpr (MODE == kModeDequantW16Lora) {  // this warp is done with the staged rows
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::BAR_XS_FREE + h));
             }
         }
         end_barrier();
@@ -609,6 +703,26 @@ cudaError_t launch_gemm_w16(const uint16_t *A, const float *sa, const uint16_t *
     choose_raster(num_t, num_w, K, 2, group, group_weight);
     GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, sa, sb, bias, out, err};
     return launch_mode<kModeDequantW16>(tmX, tmW, p, num_t * num_w, st);
+}
+
+cudaError_t launch_gemm_w16_lora(const uint16_t *A, const float *sa, const uint16_t *B16, const float *sb,
+                                 const uint16_t *bias, const float *xa, const float *lora_b, int rank, int64_t M,
+                                 int64_t N, int64_t K, uint16_t *out, unsigned *err, cudaStream_t st) {
+    if (M == 0 || N == 0) return cudaSuccess;
+    cudaError_t e = get_encoder();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tmX, tmW;
+    if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, (uint64_t)K, (uint64_t)M, BK, TT,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B16, (uint64_t)K, (uint64_t)N, BK, TW,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    const int64_t num_t = (M + TT - 1) / TT, num_w = (N + TW - 1) / TW;
+    int group, group_weight;
+    choose_raster(num_t, num_w, K, 2, group, group_weight);
+    GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, sa, sb, bias, out, err, xa, lora_b, rank,
+               lora_xa_ld(M)};
+    return launch_mode<kModeDequantW16Lora>(tmX, tmW, p, num_t * num_w, st);
 }
 
 cudaError_t launch_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t M, int64_t N, int64_t K, uint16_t *out,

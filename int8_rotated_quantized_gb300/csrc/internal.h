@@ -50,6 +50,17 @@ cudaError_t launch_gemm(const uint16_t *A, const float *sa, const int8_t *B, con
 cudaError_t launch_gemm_w16(const uint16_t *A, const float *sa, const uint16_t *B16, const float *sb,
                             const uint16_t *bias, int64_t M, int64_t N, int64_t K, uint16_t *out, unsigned *err,
                             cudaStream_t st);
+// The same with the LoRA bypass term added in the epilogue: y += sum_j xa[m, j]
+// lora_b[n, j], xa from launch_lora_down (transposed, already scaled).
+cudaError_t launch_gemm_w16_lora(const uint16_t *A, const float *sa, const uint16_t *B16, const float *sb,
+                                 const uint16_t *bias, const float *xa, const float *lora_b, int rank, int64_t M,
+                                 int64_t N, int64_t K, uint16_t *out, unsigned *err, cudaStream_t st);
+// Row stride of the transposed down-projection [16][ld]: M rounded up to 256,
+// so the epilogue's 128-token halves never leave the rows.
+__host__ __device__ inline int64_t lora_xa_ld(int64_t M) { return (M + 255) / 256 * 256; }
+// xa^T[j, m] = coef * sum_k x[m, k] A[j, k] for j < rank (lora_rotq.cu); K % 32 == 0.
+cudaError_t launch_lora_down(const uint16_t *x, int64_t M, int64_t K, const float *A, int rank, float coef, float *xa,
+                             cudaStream_t st);
 // int8 codes -> fp16 values holding the same integers, 32 per thread (rotq_wide.cu).
 cudaError_t launch_widen_codes(const int8_t *A, int64_t count, uint16_t *out, cudaStream_t st);
 

@@ -357,7 +357,84 @@ cudaError_t launch_lora_rb(const LoraArgs &a, int cs, int logb, cudaStream_t st)
     }
 }
 
+// ----------------------------------------------------------- LoRA bypass --
+
+// The down-projection of the LoRA bypass on the unrotated input, scaled and
+// transposed: xa^T[j, m] = coef * sum_k x[m, k] * A[j, k] (fp32, j < rank), so
+// the GEMM epilogue reads 4 consecutive tokens of one j per 16-byte load.
+// A CTA of 8 warps takes 16 rows (2 per warp).  Per 128-column chunk the A
+// slice [16][128] is staged once in shared memory for all 16 rows; lane l
+// owns columns 4l .. 4l + 3 of its warp's two rows, and the 32 partial sums
+// of a lane are reduced across the warp at the end.
+constexpr int kDownRows = 16, kDownRowsPerWarp = 2, kDownChunk = 128;
+
+__global__ void __launch_bounds__(256) lora_down_kernel(const uint16_t *x, int64_t M, int64_t K, const float *A,
+                                                        int rank, float coef, float *xa) {
+    __shared__ __align__(16) float As[kLoraMaxRank][kDownChunk];
+    const int lane = threadIdx.x & 31;
+    const int64_t m0 = (int64_t)blockIdx.x * kDownRows + (threadIdx.x >> 5) * kDownRowsPerWarp;
+    float acc[kDownRowsPerWarp][kLoraMaxRank];
+#pragma unroll
+    for (int r = 0; r < kDownRowsPerWarp; ++r)
+#pragma unroll
+        for (int j = 0; j < kLoraMaxRank; ++j) acc[r][j] = 0.f;
+    for (int64_t k0 = 0; k0 < K; k0 += kDownChunk) {
+        __syncthreads();  // the previous slice has been read
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int i = threadIdx.x + 256 * e, j = i >> 5, c4 = i & 31;
+            const int64_t k = k0 + 4 * c4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < rank && k < K) v = __ldg(reinterpret_cast<const float4 *>(A + (int64_t)j * K + k));
+            *reinterpret_cast<float4 *>(&As[j][4 * c4]) = v;
+        }
+        __syncthreads();
+        const int64_t k = k0 + 4 * lane;
+        float xv[kDownRowsPerWarp][4];
+#pragma unroll
+        for (int r = 0; r < kDownRowsPerWarp; ++r) {
+            const int64_t m = m0 + r;
+            uint2 w = make_uint2(0u, 0u);
+            if (m < M && k < K) w = __ldg(reinterpret_cast<const uint2 *>(x + m * K + k));
+            xv[r][0] = __uint_as_float(w.x << 16), xv[r][1] = __uint_as_float(w.x & 0xffff0000u);
+            xv[r][2] = __uint_as_float(w.y << 16), xv[r][3] = __uint_as_float(w.y & 0xffff0000u);
+        }
+#pragma unroll
+        for (int j = 0; j < kLoraMaxRank; ++j) {
+            const float4 a4 = *reinterpret_cast<const float4 *>(&As[j][4 * lane]);
+#pragma unroll
+            for (int r = 0; r < kDownRowsPerWarp; ++r) {
+                acc[r][j] = __fmaf_rn(xv[r][0], a4.x, acc[r][j]);
+                acc[r][j] = __fmaf_rn(xv[r][1], a4.y, acc[r][j]);
+                acc[r][j] = __fmaf_rn(xv[r][2], a4.z, acc[r][j]);
+                acc[r][j] = __fmaf_rn(xv[r][3], a4.w, acc[r][j]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kDownRowsPerWarp; ++r)
+#pragma unroll
+        for (int j = 0; j < kLoraMaxRank; ++j)
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) acc[r][j] += __shfl_xor_sync(0xffffffffu, acc[r][j], o);
+    if (lane == 0) {
+        const int64_t ld = lora_xa_ld(M);
+#pragma unroll
+        for (int r = 0; r < kDownRowsPerWarp; ++r)
+#pragma unroll
+            for (int j = 0; j < kLoraMaxRank; ++j)
+                if (j < rank && m0 + r < M) xa[(int64_t)j * ld + m0 + r] = __fmul_rn(coef, acc[r][j]);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_lora_down(const uint16_t *x, int64_t M, int64_t K, const float *A, int rank, float coef, float *xa,
+                             cudaStream_t st) {
+    if (M == 0) return cudaSuccess;
+    lora_down_kernel<<<(unsigned)((M + kDownRows - 1) / kDownRows), 256, 0, st>>>(x, M, K, A, rank, coef, xa);
+    return cudaGetLastError();
+}
 
 bool lora_cluster_ok(const void *W, int64_t K, int64_t ldw, int block, const float *A, int rank, const void *q) {
     if (rank < 1 || rank > kLoraMaxRank || block > 256) return false;

@@ -29,7 +29,9 @@ def test_header_declares_the_boundary():
     for must in ["convrot_quantize_weight", "convrot_linear_fwd", "convrot_linear_bwd_x", "convrot_embedding_lookup",
                  "convrot_prepare_bwd_weight", "convrot_gemm_s32", "convrot_get_error", "convrot_status_string",
                  "convrot_linear_fwd_noalloc", "convrot_selftest_wait_timeout", "convrot_dequant_weight_t",
-                 "convrot_gemm_bf16", "convrot_linear_bwd_x_bf16", "convrot_bwd_x_bf16_workspace_bytes"]:
+                 "convrot_gemm_bf16", "convrot_linear_bwd_x_bf16", "convrot_bwd_x_bf16_workspace_bytes",
+                 "convrot_linear_workspace_bytes", "convrot_widen_codes", "convrot_gemm_dequant_w16",
+                 "convrot_linear_fwd_lora", "convrot_linear_lora_workspace_bytes"]:
         assert must in names
 
 
@@ -89,6 +91,16 @@ def test_bad_shapes_are_rejected(L):
     assert L.convrot_dequant_weight_t(FAKE, FAKE, 32, 80, 32, FAKE, None) == 1
     assert L.convrot_gemm_bf16(FAKE, 8, 24, FAKE, 32, FAKE, None) == 1
     assert L.convrot_gemm_bf16(FAKE, 8, 32, FAKE, 24, FAKE, None) == 1
+    # LoRA bypass: rank out of range, K not a multiple of 32, workspace too small
+    need_l = L.convrot_linear_lora_workspace_bytes(8, 256, 32)
+    assert need_l == L.convrot_linear_workspace_bytes(8, 256, 32) + 256 * 16 * 4
+    assert L.convrot_linear_fwd_lora(FAKE, 8, 256, FAKE, FAKE, 32, 32, None, FAKE, FAKE, 17, 1.0, 1.0, FAKE, FAKE,
+                                     need_l, None) == 1
+    assert L.convrot_linear_fwd_lora(FAKE, 8, 48, FAKE, FAKE, 32, 16, None, FAKE, FAKE, 4, 1.0, 1.0, FAKE, FAKE,
+                                     1 << 30, None) == 1
+    assert L.convrot_linear_fwd_lora(FAKE, 8, 256, FAKE, FAKE, 32, 32, None, FAKE, FAKE, 4, 1.0, 1.0, FAKE, FAKE,
+                                     need_l - 1, None) == 1
+    assert L.convrot_widen_codes(FAKE, 24, FAKE, None) == 1
     need = L.convrot_bwd_x_bf16_workspace_bytes(64, 256)
     assert need == 64 * 256 * 2
     assert L.convrot_linear_bwd_x_bf16(FAKE, 8, 64, FAKE, FAKE, 256, 32, FAKE, FAKE, need - 1, None) == 1

@@ -108,6 +108,32 @@ def test_qkv_lora_merge_and_forward_full_size():
     assert rel_fro(f64(y_s), f64(x_rows) @ f64(merged).T) <= REL_FRO_BF16
 
 
+def test_qkv_lora_bypass_forward_full_size():
+    wl = synth.WORKLOADS["qkv_lora"]
+    M, K, N, b = wl["M"], wl["K"], wl["N"], wl["block"]
+    r, alpha, scale = wl["lora_rank"], wl["lora_alpha"], wl["lora_scale"]
+    W = sg.normal_bf16(0, synth.STREAM_W, N, K, wl["w_sigma"], "cuda")
+    A, B = sg.lora_pair(0, N, K, r, wl["lora_sigma"], "cuda")
+    Wq, sw = cr.convrot_quantize_weight(W, b)
+    x = sg.activations_bf16(0, M, K, wl["x_outliers"], wl["x_factor"], "cuda")
+    y = cr.convrot_linear_fwd_lora(x, Wq, sw, b, A, B, alpha, scale)
+    assert cr.convrot_get_error() == cr.OK
+    rng = np.random.default_rng(7)
+    ns, ms = _rows(rng, N), _rows(rng, M)
+    A_np, B_np = synth.lora_pair(0, N, K, r, wl["lora_sigma"])
+    x_rows = _act_rows(wl, ms, K)
+    assert np.array_equal(bits_of(x[torch.from_numpy(ms).cuda()]), x_rows)
+    wq_s = codes_of(Wq[torch.from_numpy(ns).cuda()])
+    sw_s = sw.cpu().numpy()[ns]
+    ref = oracle.linear_fwd_lora(x_rows, wq_s, sw_s, b, A_np, B_np[ns], alpha, scale)
+    got = bits_of(y[torch.from_numpy(ms).cuda()][:, torch.from_numpy(ns).cuda()])
+    assert rel_fro(f64(got), f64(ref)) <= REL_FRO_ORACLE
+    assert np.mean(got == ref) > 0.9
+    w_rows = _normal_rows(synth.STREAM_W, ns, K, wl["w_sigma"])
+    merged = oracle.lora_merge(w_rows, A_np, B_np[ns], alpha, scale)
+    assert rel_fro(f64(got), f64(x_rows) @ f64(merged).T) <= REL_FRO_BF16
+
+
 def test_train20k_forward_and_backward_full_size():
     wl = synth.WORKLOADS["train20k"]
     M, K, N, b = wl["M"], wl["K"], wl["N"], wl["block"]

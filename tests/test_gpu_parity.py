@@ -251,6 +251,37 @@ def test_widened_weight_path_is_bit_identical(M, K, N):
     np.testing.assert_array_equal(acc.cpu().numpy(), oracle.gemm_s32(A, codes_of(Wq)))
 
 
+@pytest.mark.parametrize("M,K,N,rank,with_bias", [(300, 1024, 272, 16, False), (65, 512, 128, 5, True),
+                                                   (513, 4096, 400, 16, True)])
+def test_linear_fwd_lora_bypass_parity(M, K, N, rank, with_bias):
+    b = 128
+    x = synth.activations_bf16(21, M, K, 8, 30.0)
+    W = synth.normal_bf16(21, synth.STREAM_W, N, K, 0.02)
+    A, B = synth.lora_pair(21, N, K, rank, 0.05)
+    bias = synth.normal_bf16(21, 9, 1, N, 0.5)[0] if with_bias else None
+    wq, sw = oracle.quantize_weight(W, b)
+    y = cr.convrot_linear_fwd_lora(torch_bf16(x), _i8(wq), _f32(sw), b, _f32(A), _f32(B), 16.0, 1.0,
+                                   bias=None if bias is None else torch_bf16(bias))
+    assert cr.convrot_get_error() == cr.OK
+    ref = oracle.linear_fwd_lora(x, wq, sw, b, A, B, 16.0, 1.0, bias)
+    yb = bits_of(y)
+    assert rel_fro(f64(yb), f64(ref)) <= REL_FRO_ORACLE
+    ulps = np.abs(yb.astype(np.int32) - ref.astype(np.int32))
+    same_sign = (yb >> 15) == (ref >> 15)
+    assert np.mean(ulps[same_sign] <= 1) > 0.999 and np.mean(yb == ref) > 0.9
+    # scale 0: exactly the plain forward
+    y0 = cr.convrot_linear_fwd_lora(torch_bf16(x), _i8(wq), _f32(sw), b, _f32(A), _f32(B), 16.0, 0.0,
+                                    bias=None if bias is None else torch_bf16(bias))
+    yp = cr.convrot_linear_fwd(torch_bf16(x), _i8(wq), _f32(sw), b, bias=None if bias is None else torch_bf16(bias))
+    assert torch.equal(y0, yp)
+    # the bypass and the merged-then-quantized weight compute the same layer up to quantization
+    c = np.float32(16.0 / rank)
+    full = f64(x) @ (f64(W) + float(c) * (B.astype(np.float64) @ A.astype(np.float64))).T
+    if bias is not None:
+        full = full + f64(bias)
+    assert rel_fro(f64(yb), full) <= REL_FRO_BF16
+
+
 def test_linear_fwd_tiny_workload():
     wl = synth.WORKLOADS["tiny"]
     M, K, N, b = wl["M"], wl["K"], wl["N"], wl["block"]
