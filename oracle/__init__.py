@@ -61,6 +61,7 @@ def _load():
                 "oracle_dequant_weight_t": [P, P, I64, I64, I, P],
                 "oracle_gemm_bf16": [P, P, I64, I64, I64, P],
                 "oracle_linear_fwd_lora": [P, I64, I64, P, P, I64, I, P, P, P, I, F, F, P],
+                "oracle_linear_bwd_x_r2": [P, I64, I64, P, P, I64, I, P, P, P],
                 "oracle_num_threads": [],
             }
             for name, args in sig.items():
@@ -243,6 +244,20 @@ def gemm_bf16(A_bits, B_bits) -> np.ndarray:
 def linear_bwd_x_bf16(dY_bits, Wq, s_w, b: int) -> np.ndarray:
     """bf16-mode grad_x: dX = bf16(dY . W_eff) with W_eff = bf16((s_w (.) Wq) R)."""
     return gemm_bf16(dY_bits, dequant_weight_t(Wq, s_w, b))
+
+
+def linear_bwd_x_r2(dY_bits, Wq, s_w, b: int):
+    """int8 backward, second reading: returns (dX bf16 bits [M,K], codes of dY*s_w [M,N], s_d [M])."""
+    dY = _c(dY_bits, np.uint16)
+    Wq = _c(Wq, np.int8)
+    M, N = dY.shape
+    K = Wq.shape[1]
+    dX = np.empty((M, K), dtype=np.uint16)
+    dq = np.empty((M, N), dtype=np.int8)
+    sd = np.empty(M, dtype=np.float32)
+    _check(_load().oracle_linear_bwd_x_r2(_p(dY), M, N, _p(Wq), _p(_c(s_w, np.float32)), K, b, _p(dX), _p(dq),
+                                          _p(sd)), "linear_bwd_x_r2")
+    return dX, dq, sd
 
 
 def embedding_lookup(ids, Eq, s_e, b: int):

@@ -45,6 +45,9 @@
  *       dX = bf16(acc * s_dy * s_wt).
  *   R7  Embedding lookup: out[t] = bf16_rne((s[id] * Eq[id,:]) R), fp64; an id
  *       outside [0, V) yields a zero row and is counted.
+ *   R10 int8 backward, second reading: s_w folded into the columns of dY, dY
+ *       quantized per row without rotation, the int8 GEMM on Wq as it is
+ *       (contraction over N), the rotation along K applied to the product.
  *   R9  LoRA bypass in the forward: instead of merging, the adapter's branch
  *       c * (x A^T) B^T on the unrotated input is added to the dequantized
  *       product before the output rounding (fp64 here).
@@ -493,6 +496,59 @@ int oracle_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t M, int64_t N,
             C[m * N + n] = f64_to_bf16(acc);
         }
     return 0;
+}
+
+/* ----------------------------------- int8 backward, second reading (R10) ---- */
+
+/* The scale of the frozen weight is folded into the columns of dY, which is
+ * quantized per row without a rotation, and the int8 GEMM takes Wq as it is
+ * (contraction over N); the rotation along K is applied to the product:
+ *   D   = fp32(dY[m,n] * s_w[n]),  Dq, s_d = per-row absmax codes of D
+ *   dX  = bf16( (s_d[m] * sum_n Dq[m,n] Wq[n,k]) R )   (fp64 here). */
+int oracle_linear_bwd_x_r2(const uint16_t *dY, int64_t M, int64_t N, const int8_t *Wq, const float *s_w,
+                           int64_t K, int b, uint16_t *dX, int8_t *dq_out, float *sd_out)
+{
+    if (!is_pow2(b) || K % b != 0)
+        return 1;
+    double *D = malloc(sizeof(double) * (size_t)M * (size_t)N);
+    int8_t *dq = dq_out ? dq_out : malloc((size_t)M * (size_t)N);
+    float *sd = sd_out ? sd_out : malloc(sizeof(float) * (size_t)M);
+    int8_t *wt = malloc((size_t)N * (size_t)K);
+    int32_t *acc = malloc(sizeof(int32_t) * (size_t)M * (size_t)K);
+    double *v = malloc(sizeof(double) * (size_t)M * (size_t)K);
+    double *vr = malloc(sizeof(double) * (size_t)M * (size_t)K);
+    int rc = 2;
+    if (D && dq && sd && wt && acc && v && vr) {
+        for (int64_t m = 0; m < M; m++)
+            for (int64_t n = 0; n < N; n++)
+                D[m * N + n] = (double)((float)bf16_to_f64(dY[m * N + n]) * s_w[n]);
+        rc = quantize_rows_f64(D, M, N, N, 1, dq, sd);
+        if (rc == 0) {
+            for (int64_t n = 0; n < N; n++)
+                for (int64_t k = 0; k < K; k++)
+                    wt[k * N + n] = Wq[n * K + k];
+            rc = oracle_gemm_s32(dq, wt, M, K, N, acc);
+        }
+        if (rc == 0) {
+            for (int64_t m = 0; m < M; m++)
+                for (int64_t k = 0; k < K; k++)
+                    v[m * K + k] = (double)sd[m] * (double)acc[m * K + k];
+            rc = oracle_rotate_rows(v, M, K, b, vr);
+        }
+        if (rc == 0)
+            for (int64_t i = 0; i < M * K; i++)
+                dX[i] = f64_to_bf16(vr[i]);
+    }
+    free(D);
+    if (!dq_out)
+        free(dq);
+    if (!sd_out)
+        free(sd);
+    free(wt);
+    free(acc);
+    free(v);
+    free(vr);
+    return rc;
 }
 
 /* ------------------------------------------------- embedding lookup (R7) ---- */

@@ -379,6 +379,28 @@ def test_bf16_mode_grad_x_close_to_bf16_matmul():
     assert np.linalg.norm(_f64(dx8) - ref) > np.linalg.norm(_f64(dx) - ref)
 
 
+def test_int8_backward_second_reading():
+    M, K, N = 40, 128, 256
+    w = synth.normal_bf16(22, synth.STREAM_W, N, K, 0.02)
+    dy = synth.normal_bf16(22, synth.STREAM_DY, M, N, 1e-3)
+    for b in (1, 32):
+        wq, sw = oracle.quantize_weight(w, b)
+        dx, dq, sd = oracle.linear_bwd_x_r2(dy, wq, sw, b)
+        # the codes are the per-row absmax codes of the fp32 product dY * s_w, without rotation
+        d32 = (_f64(dy).astype(np.float32) * sw[None, :]).astype(np.float64)
+        q1, s1 = oracle.quantize_rows_f64(d32, 1)
+        np.testing.assert_array_equal(dq, q1)
+        np.testing.assert_array_equal(sd, s1)
+        acc = dq.astype(np.int64) @ wq.astype(np.int64)            # numpy integer product over N
+        if b == 1:   # no rotation: one rounding of s_d * acc
+            np.testing.assert_array_equal(dx, _bf16(sd[:, None].astype(np.float64) * acc))
+        else:        # the rotation preserves row norms (up to the bf16 rounding)
+            base = sd[:, None].astype(np.float64) * acc
+            np.testing.assert_allclose(np.linalg.norm(_f64(dx), axis=1), np.linalg.norm(base, axis=1), rtol=4e-3)
+        ref = _f64(dy) @ _f64(w)
+        assert np.linalg.norm(_f64(dx) - ref) / np.linalg.norm(ref) < 5e-2
+
+
 # ------------------------------------------------------------------ embedding
 
 
