@@ -352,7 +352,7 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
     ms = _time(torch, lambda i: cr.convrot_prepare_bwd_weight(Wq, sw, b, WtQ, swt, ws), flush, 3)
     rows["a6_prep_bwd_weight"] = _hbm_row(N * K + N * 4 + K * N + K * 4, ms, pk,
                                           "C4 Wq [16384,4096] -> WtQ [4096,16384] (one-off, via a double-float workspace)")
-    del WtQ, ws
+    del ws
     # next row 1: the bf16 backward mode (transient dequantization + bf16 tcgen05 GEMM), C4 shapes
     M = wl["M"]
     weff_t = torch.empty((K, N), dtype=torch.bfloat16, device=dev)
@@ -365,7 +365,22 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
     rows["n1_bf16_bwd_gemm"] = _tc_row(2.0 * M * N * K, ms, pk, "C4 dY [20480,16384] . W_eff -> dX bf16 [20480,4096]")
     rows["n1_bf16_bwd_gemm"].update({"traffic": gemm_traffic_per_launch("bf16_bwd"),
                                      "algorithmic_bytes": M * N * 2 + K * N * 2 + M * K * 2})
-    del W, Wq, weff_t, dY, dX
+    # next row 3: the second reading of the int8 backward (no prepared weight copy), and the accuracy of the
+    # two int8 readings against the bf16 mode on this workload
+    ws3 = torch.empty(cr.convrot_bwd_x_r2_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
+    dX3 = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+    ms = _time(torch, lambda i: cr.convrot_linear_bwd_x_r2(dY, Wq, sw, b, dX3, ws3), flush, 5)
+    rows["n3_int8_bwd_second_reading"] = _tc_row(2.0 * M * N * K, ms, pk,
+                                                 "C4 dY [20480,16384] -> dX [20480,4096], scale-folded unrotated "
+                                                 "codes, Wq as stored, rotation of the product (whole call)")
+    dX1 = cr.convrot_linear_bwd_x(dY, WtQ, swt, b)
+    cr.convrot_gemm_bf16(dY, cr.convrot_dequant_weight_t(Wq, sw, b), dX)
+
+    def rel(a):
+        return round(float(torch.linalg.vector_norm((a.float() - dX.float())) / torch.linalg.vector_norm(dX.float())), 5)
+    rows["n3_int8_bwd_second_reading"].update({"rel_fro_vs_bf16_mode": rel(dX3),
+                                               "first_reading_rel_fro_vs_bf16_mode": rel(dX1)})
+    del W, Wq, weff_t, dY, dX, dX1, dX3, ws3, WtQ
     # a1 + a2: LoRA merge fused into the weight quantizer, C3 qkv weight
     wl3 = synth.WORKLOADS["qkv_lora"]
     N3, K3, r = wl3["N"], wl3["K"], wl3["lora_rank"]

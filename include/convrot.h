@@ -230,6 +230,21 @@ CONVROT_API int convrot_linear_bwd_x(const uint16_t *dY, int64_t M, int64_t N, c
                          const float *scale_wt, int64_t K, int block, uint16_t *dX,
                          void *workspace, size_t ws_bytes, convrot_stream_t stream);
 
+/* Bytes of workspace convrot_linear_bwd_x_r2 needs: dY codes (fp16-held) and
+ * scales, the transient fp16 transpose of Wq and the fp32 product [M, K]. */
+CONVROT_API size_t convrot_bwd_x_r2_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/* Input gradient through the int8 GEMM, second reading (the pages leave the
+ * operand open; this reading keeps Wq as stored and needs no prepared copy):
+ *   D   = fp32(dY[m,n] * scale_w[n]);  Dq, s_d = per-row absmax codes of D, no rotation
+ *   dX  = bf16( (s_d[m] * sum_n Dq[m,n] Wq[n,k]) R )   R along K in blocks of `block`
+ * dY bf16 [M, N]; Wq int8 [N, K] with scale_w fp32 [N] (from convrot_quantize_weight);
+ * dX out bf16 [M, K]; N and K multiples of 32 and of 16, at most 32768; dY and dX
+ * 32-byte aligned; workspace >= convrot_bwd_x_r2_workspace_bytes(M, N, K), 256-byte aligned. */
+CONVROT_API int convrot_linear_bwd_x_r2(const uint16_t *dY, int64_t M, int64_t N, const int8_t *Wq,
+                            const float *scale_w, int64_t K, int block, uint16_t *dX,
+                            void *workspace, size_t ws_bytes, convrot_stream_t stream);
+
 /* ------------------------------------------------- bf16 frozen backward -- */
 
 /* The default backward mode of the layer (guide 4.1: the backward option

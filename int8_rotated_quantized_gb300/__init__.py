@@ -63,6 +63,8 @@ def lib():
                 "convrot_widen_codes": ([P, I64, P, P], I),
                 "convrot_gemm_dequant_w16": ([P, P, I64, I64, P, P, I64, P, P, P], I),
                 "convrot_gemm_bf16": ([P, I64, I64, P, I64, P, P], I),
+                "convrot_bwd_x_r2_workspace_bytes": ([I64, I64, I64], S),
+                "convrot_linear_bwd_x_r2": ([P, I64, I64, P, P, I64, I, P, P, S, P], I),
                 "convrot_bwd_x_bf16_workspace_bytes": ([I64, I64], S),
                 "convrot_linear_bwd_x_bf16": ([P, I64, I64, P, P, I64, I, P, P, S, P], I),
                 "convrot_gemm_s32_workspace_bytes": ([I64, I64], S),
@@ -360,6 +362,28 @@ def convrot_linear_bwd_x_bf16(dY, Wq, scale_w, block, dX=None, workspace=None, s
     ws = _workspace(nbytes, dY.device, workspace)
     _check(lib().convrot_linear_bwd_x_bf16(_ptr(dY), M, N, _ptr(Wq), _ptr(scale_w), K, block, _ptr(dX), _ptr(ws),
                                            nbytes, _stream(stream)), "convrot_linear_bwd_x_bf16")
+    return dX
+
+
+def convrot_bwd_x_r2_workspace_bytes(M: int, N: int, K: int) -> int:
+    return lib().convrot_bwd_x_r2_workspace_bytes(M, N, K)
+
+
+def convrot_linear_bwd_x_r2(dY, Wq, scale_w, block, dX=None, workspace=None, stream=None):
+    """Input gradient through the int8 GEMM, second reading: dY bf16 [M, N], Wq int8 [N, K] -> dX bf16 [M, K]."""
+    _need(dY, torch.bfloat16, "dY", 2)
+    _need(Wq, torch.int8, "Wq", 2)
+    _need(scale_w, torch.float32, "scale_w", 1)
+    M, N = dY.shape
+    if Wq.shape[0] != N:
+        raise ValueError("shape mismatch")
+    K = Wq.shape[1]
+    if dX is None:
+        dX = torch.empty((M, K), dtype=torch.bfloat16, device=dY.device)
+    nbytes = convrot_bwd_x_r2_workspace_bytes(M, N, K)
+    ws = _workspace(nbytes, dY.device, workspace)
+    _check(lib().convrot_linear_bwd_x_r2(_ptr(dY), M, N, _ptr(Wq), _ptr(scale_w), K, block, _ptr(dX), _ptr(ws),
+                                         nbytes, _stream(stream)), "convrot_linear_bwd_x_r2")
     return dX
 
 

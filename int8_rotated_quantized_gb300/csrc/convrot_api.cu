@@ -271,6 +271,39 @@ int convrot_linear_bwd_x(const uint16_t *dY, int64_t M, int64_t N, const int8_t 
     return convrot_linear_fwd(dY, M, N, WtQ, scale_wt, K, block, nullptr, dX, workspace, ws_bytes, stream);
 }
 
+size_t convrot_bwd_x_r2_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || K < 0) return 0;
+    return convrot_act_workspace_bytes(M, N) + align256((size_t)K * (size_t)N * 2) +
+           align256((size_t)M * (size_t)K * sizeof(float));
+}
+
+int convrot_linear_bwd_x_r2(const uint16_t *dY, int64_t M, int64_t N, const int8_t *Wq, const float *scale_w,
+                            int64_t K, int block, uint16_t *dX, void *workspace, size_t ws_bytes,
+                            convrot_stream_t stream) {
+    CHECK(block_ok(block) && row_ok(K, block) && row_ok(N, 16) && M >= 0 && M <= INT32_MAX);
+    CHECK(M == 0 || (dY && Wq && scale_w && dX && workspace && aligned16(Wq) && aligned16(scale_w) &&
+                     ((uintptr_t)workspace & 255u) == 0 && convrot::bwd_r2_ok(N, K, dY, dX)));
+    CHECK(M == 0 || ws_bytes >= convrot_bwd_x_r2_workspace_bytes(M, N, K));
+    unsigned *err = nullptr;
+    int rc = device_setup(&err);
+    if (rc != CONVROT_OK) return rc;
+    if (M == 0) return CONVROT_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    char *ws = static_cast<char *>(workspace);
+    uint16_t *dq = reinterpret_cast<uint16_t *>(ws);
+    float *sd = reinterpret_cast<float *>(ws + align256((size_t)M * (size_t)N * 2));
+    uint16_t *wt16 = reinterpret_cast<uint16_t *>(ws + convrot_act_workspace_bytes(M, N));
+    float *P = reinterpret_cast<float *>(ws + convrot_act_workspace_bytes(M, N) + align256((size_t)K * (size_t)N * 2));
+    rc = cuda_status(convrot::launch_scaleq(dY, M, N, scale_w, dq, sd, st));
+    if (rc != CONVROT_OK) return rc;
+    rc = cuda_status(convrot::launch_transpose_widen(Wq, N, K, wt16, st));
+    if (rc != CONVROT_OK) return rc;
+    // P [M, K] = float(Dq [M, N] . (Wt16 [K, N])^T) * s_d
+    rc = cuda_status(convrot::launch_gemm_w16_scale_f32(dq, sd, wt16, M, K, N, P, err, st));
+    if (rc != CONVROT_OK) return rc;
+    return cuda_status(convrot::launch_rot_rows_f32(P, M, K, block, dX, st));
+}
+
 int convrot_dequant_weight_t(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K, int block,
                              uint16_t *WeffT, convrot_stream_t stream) {
     CHECK(block_ok(block) && row_ok(K, block) && N >= 0 && N % 16 == 0 && N <= INT32_MAX);

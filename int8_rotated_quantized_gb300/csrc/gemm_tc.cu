@@ -71,9 +71,13 @@ constexpr int kModeS32 = 0, kModeDequant = 1, kModeBf16 = 2, kModeDequantW16 = 3
 // The widened-weight dequantization mode plus a LoRA bypass term in the
 // epilogue: y += sum_j xa[m, j] * B[n, j] (xa already scaled, stored transposed).
 constexpr int kModeDequantW16Lora = 4;
+// Widened weight codes, exact integer chunks, and an fp32 result scaled by the
+// token's scale only: P[m, n] = float(acc) * sa[m] (the second reading of the
+// int8 backward rotates P afterwards).
+constexpr int kModeScaleF32 = 5;
 // modes whose weight tiles arrive by TMA already in the MMA's format
 constexpr bool weight_direct(int mode) {
-    return mode == kModeBf16 || mode == kModeDequantW16 || mode == kModeDequantW16Lora;
+    return mode == kModeBf16 || mode == kModeDequantW16 || mode == kModeDequantW16Lora || mode == kModeScaleF32;
 }
 
 // Stages of the rings when the weight tiles arrive ready by TMA (widened-weight
@@ -510,6 +514,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (full || i < mlim) *out = acc[i];
                         out += p.N;
                     }
+                } else if constexpr (MODE == kModeScaleF32) {
+                    float *out = static_cast<float *>(p.out) + (int64_t)m0 * p.N + n;
+#pragma unroll
+                    for (int i4 = 0; i4 < 128; i4 += 4) {
+                        float sx[4];
+                        if (full) {
+                            const float4 v = __ldg(reinterpret_cast<const float4 *>(p.sa + m0 + i4));
+                            sx[0] = v.x, sx[1] = v.y, sx[2] = v.z, sx[3] = v.w;
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) sx[j] = i4 + j < mlim ? __ldg(p.sa + m0 + i4 + j) : 0.f;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            if (full || i4 + j < mlim) *out = __fmul_rn(__int2float_rn(acc[i4 + j]), sx[j]);
+                            out += p.N;
+                        }
+                    }
                 } else if constexpr (MODE == kModeBf16) {
                     uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)m0 * p.N + n;
 #pragma unroll
@@ -723,6 +745,24 @@ cudaError_t launch_gemm_w16_lora(const uint16_t *A, const float *sa, const uint1
     GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, sa, sb, bias, out, err, xa, lora_b, rank,
                lora_xa_ld(M)};
     return launch_mode<kModeDequantW16Lora>(tmX, tmW, p, num_t * num_w, st);
+}
+
+cudaError_t launch_gemm_w16_scale_f32(const uint16_t *A, const float *sa, const uint16_t *B16, int64_t M, int64_t N,
+                                      int64_t K, float *out, unsigned *err, cudaStream_t st) {
+    if (M == 0 || N == 0) return cudaSuccess;
+    cudaError_t e = get_encoder();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tmX, tmW;
+    if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, (uint64_t)K, (uint64_t)M, BK, TT,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B16, (uint64_t)K, (uint64_t)N, BK, TW,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    const int64_t num_t = (M + TT - 1) / TT, num_w = (N + TW - 1) / TW;
+    int group, group_weight;
+    choose_raster(num_t, num_w, K, 2, group, group_weight);
+    GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, sa, nullptr, nullptr, out, err};
+    return launch_mode<kModeScaleF32>(tmX, tmW, p, num_t * num_w, st);
 }
 
 cudaError_t launch_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t M, int64_t N, int64_t K, uint16_t *out,

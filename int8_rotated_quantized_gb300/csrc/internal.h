@@ -64,6 +64,16 @@ cudaError_t launch_lora_down(const uint16_t *x, int64_t M, int64_t K, const floa
 // int8 codes -> fp16 values holding the same integers, 32 per thread (rotq_wide.cu).
 cudaError_t launch_widen_codes(const int8_t *A, int64_t count, uint16_t *out, cudaStream_t st);
 
+// P[M,N] = float(A[M,K] . B16[N,K]^T) * sa[m] in fp32 (exact integer sums).
+cudaError_t launch_gemm_w16_scale_f32(const uint16_t *A, const float *sa, const uint16_t *B16, int64_t M, int64_t N,
+                                      int64_t K, float *out, unsigned *err, cudaStream_t st);
+// Second reading of the int8 backward (bwd_r2.cu).
+bool bwd_r2_ok(int64_t N, int64_t K, const void *dY, const void *dX);
+cudaError_t launch_scaleq(const uint16_t *dY, int64_t M, int64_t N, const float *colscale, uint16_t *q, float *scale,
+                          cudaStream_t st);
+cudaError_t launch_transpose_widen(const int8_t *W, int64_t N, int64_t K, uint16_t *T, cudaStream_t st);
+cudaError_t launch_rot_rows_f32(const float *P, int64_t rows, int64_t L, int block, uint16_t *out, cudaStream_t st);
+
 // C[M,N] = bf16(A[M,K] . B[N,K]^T) with bf16 operands, fp32 accumulation.
 cudaError_t launch_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t M, int64_t N, int64_t K, uint16_t *out,
                              unsigned *err, cudaStream_t st);

@@ -31,7 +31,8 @@ def test_header_declares_the_boundary():
                  "convrot_linear_fwd_noalloc", "convrot_selftest_wait_timeout", "convrot_dequant_weight_t",
                  "convrot_gemm_bf16", "convrot_linear_bwd_x_bf16", "convrot_bwd_x_bf16_workspace_bytes",
                  "convrot_linear_workspace_bytes", "convrot_widen_codes", "convrot_gemm_dequant_w16",
-                 "convrot_linear_fwd_lora", "convrot_linear_lora_workspace_bytes"]:
+                 "convrot_linear_fwd_lora", "convrot_linear_lora_workspace_bytes", "convrot_linear_bwd_x_r2",
+                 "convrot_bwd_x_r2_workspace_bytes"]:
         assert must in names
 
 
@@ -101,6 +102,10 @@ def test_bad_shapes_are_rejected(L):
     assert L.convrot_linear_fwd_lora(FAKE, 8, 256, FAKE, FAKE, 32, 32, None, FAKE, FAKE, 4, 1.0, 1.0, FAKE, FAKE,
                                      need_l - 1, None) == 1
     assert L.convrot_widen_codes(FAKE, 24, FAKE, None) == 1
+    # second reading of the int8 backward: N not a multiple of 32, workspace too small
+    need_r2 = L.convrot_bwd_x_r2_workspace_bytes(8, 512, 256)
+    assert L.convrot_linear_bwd_x_r2(FAKE, 8, 48, FAKE, FAKE, 256, 32, FAKE, FAKE, 1 << 30, None) == 1
+    assert L.convrot_linear_bwd_x_r2(FAKE, 8, 512, FAKE, FAKE, 256, 32, FAKE, FAKE, need_r2 - 1, None) == 1
     need = L.convrot_bwd_x_bf16_workspace_bytes(64, 256)
     assert need == 64 * 256 * 2
     assert L.convrot_linear_bwd_x_bf16(FAKE, 8, 64, FAKE, FAKE, 256, 32, FAKE, FAKE, need - 1, None) == 1

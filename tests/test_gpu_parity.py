@@ -385,6 +385,25 @@ def test_linear_bwd_x_bf16_parity(block):
     assert rel_fro(f64(got), f64(dY) @ f64(W)) <= REL_FRO_BF16
 
 
+@pytest.mark.parametrize("M,N,K,block", [(150, 768, 256, 32), (300, 512, 384, 128), (37, 1024, 256, 256)])
+def test_linear_bwd_x_second_reading_parity(M, N, K, block):
+    W = synth.normal_bf16(23, synth.STREAM_W, N, K, 0.02)
+    wq, sw = oracle.quantize_weight(W, block)
+    dY = synth.normal_bf16(23, synth.STREAM_DY, M, N, 1e-3)
+    ws = torch.empty(cr.convrot_bwd_x_r2_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    dX = cr.convrot_linear_bwd_x_r2(torch_bf16(dY), _i8(wq), _f32(sw), block, workspace=ws)
+    assert cr.convrot_get_error() == cr.OK
+    ref, dq_ref, sd_ref = oracle.linear_bwd_x_r2(dY, wq, sw, block)
+    # the unrotated codes and scales are decided in the same fp32 arithmetic: identical
+    dq = ws[:M * N * 2].view(torch.float16).view(M, N)
+    np.testing.assert_array_equal(codes_of(dq), dq_ref)
+    off = (M * N * 2 + 255) // 256 * 256
+    np.testing.assert_array_equal(ws[off:off + 4 * M].view(torch.float32).cpu().numpy(), sd_ref)
+    got = bits_of(dX)
+    _check_bf16_sums(got, ref, K)
+    assert rel_fro(f64(got), f64(dY) @ f64(W)) <= REL_FRO_BF16
+
+
 # ------------------------------------------------------------------ embedding
 
 
