@@ -27,6 +27,7 @@
 // than 8 spread over b/8 consecutive lanes.
 #include "common.cuh"
 #include "internal.h"
+#include "launch_cache.h"
 #include "wide.cuh"
 
 namespace convrot {
@@ -332,8 +333,8 @@ cudaError_t launch_bwd_prep_df(const int8_t *Wq, const float *scale_w, int64_t N
     const float ch = (float)c;
     const float cl = (float)(c - (double)ch);
     const size_t smem = sizeof(float2) * (size_t)block * kPrepRows;
-    cudaError_t e = cudaFuncSetAttribute(prep_transpose_df_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(sizeof(float2) * 256 * kPrepRows));
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(prep_transpose_df_kernel),
+                                     (int)(sizeof(float2) * 256 * kPrepRows));
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((N + kPrepRows - 1) / kPrepRows), (unsigned)(K / block));
     prep_transpose_df_kernel<<<grid, 256, smem, st>>>(Wq, scale_w, N, K, block, ch, cl, T);
@@ -342,9 +343,7 @@ cudaError_t launch_bwd_prep_df(const int8_t *Wq, const float *scale_w, int64_t N
     // rows of T: length N, 8 elements per thread, 512 threads, S slots
     const int64_t chunks = N / 8;
     const int S = chunks <= kThreads ? 1 : chunks <= 2 * kThreads ? 2 : chunks <= 4 * kThreads ? 4 : 8;
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = sm_count();
     const int64_t g = K < (int64_t)sms * 2 ? K : (int64_t)sms * 2;
     const float denom = (float)(127.0 * sqrt((double)block));
     const int lanes = block / 8;

@@ -15,6 +15,7 @@
 #include "common.cuh"
 #include "fwht.cuh"
 #include "internal.h"
+#include "launch_cache.h"
 #include "wide.cuh"
 
 namespace convrot {
@@ -168,10 +169,7 @@ void shape32(int64_t len, int &G, int &S) {
 }
 
 int64_t grid_for(int64_t nblocks) {
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t cap = (int64_t)sms * 2;
+    const int64_t cap = (int64_t)sm_count() * 2;
     return nblocks < cap ? nblocks : cap;
 }
 

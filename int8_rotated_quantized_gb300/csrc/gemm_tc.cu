@@ -49,6 +49,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "launch_cache.h"
 #include "mbar.cuh"
 #include "wide.cuh"
 
@@ -645,18 +646,6 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, size_t esize, const voi
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int sm_count_of_current_device() {
-    static int cached[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cached[dev] == 0) {
-        int n = 0;
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = n;
-    }
-    return cached[dev];
-}
-
 // Raster choice.  The tiles of the grouped dimension are read from DRAM once
 // if `group` of them (plus the streaming tiles of one wave) stay in L2; the
 // swept operand is then read once per group.  Measured on GB300, groups whose
@@ -678,10 +667,10 @@ void choose_raster(int64_t num_t, int64_t num_w, int64_t K, int64_t w_elem, int 
 template <int MODE>
 cudaError_t launch_mode(const CUtensorMap &tmX, const CUtensorMap &tmW, const GemmArgs &p, int64_t tiles,
                         cudaStream_t st) {
-    const int sms = sm_count_of_current_device();
+    const int sms = sm_count();
     const int grid = (int)(tiles < sms ? tiles : sms);
     constexpr int kSmem = Layout<MODE>::SMEM_BYTES;
-    cudaError_t e = cudaFuncSetAttribute(gemm_s8_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_s8_tc_kernel<MODE>), kSmem);
     if (e != cudaSuccess) return e;
     gemm_s8_tc_kernel<MODE><<<grid, NUM_THREADS, kSmem, st>>>(tmX, tmW, p);
     return cudaGetLastError();

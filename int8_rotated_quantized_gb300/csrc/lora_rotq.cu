@@ -36,6 +36,7 @@
 #include "common.cuh"
 #include "fwht.cuh"
 #include "internal.h"
+#include "launch_cache.h"
 #include "mbar.cuh"
 #include "wide.cuh"
 
@@ -317,7 +318,7 @@ template <int LOGB, int RB>
 cudaError_t launch_lora_t(const LoraArgs &a, int cs, cudaStream_t st) {
     auto kernel = lora_rotq_kernel<LOGB, RB>;
     const size_t sm = smem_bytes(a.KS);
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kernel), (int)sm);
     if (e != cudaSuccess) return e;
     const int threads = (int)(a.KS / 4);
     const int64_t ntiles = (a.rows + kRowsPerTile - 1) / kRowsPerTile;
@@ -333,13 +334,24 @@ cudaError_t launch_lora_t(const LoraArgs &a, int cs, cudaStream_t st) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3(cs, 1, 1);
+    // resident clusters of this configuration, queried once per device and shape
+    static std::map<std::tuple<int, int, size_t>, int> cluster_cache;
+    static std::mutex cluster_mu;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters <= 0) {
-        (void)cudaGetLastError();
-        int dev = 0, sms = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        clusters = sms / cs > 0 ? sms / cs : 1;
+    {
+        std::lock_guard<std::mutex> lock(cluster_mu);
+        const auto key = std::make_tuple(current_device(), cs, sm);
+        auto it = cluster_cache.find(key);
+        if (it != cluster_cache.end()) {
+            clusters = it->second;
+        } else {
+            if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters <= 0) {
+                (void)cudaGetLastError();
+                const int sms = sm_count();
+                clusters = sms / cs > 0 ? sms / cs : 1;
+            }
+            cluster_cache[key] = clusters;
+        }
     }
     cfg.gridDim = dim3(cs, (unsigned)(ntiles < clusters ? ntiles : clusters), 1);
     return cudaLaunchKernelEx(&cfg, kernel, a);

@@ -24,6 +24,7 @@
 #include "common.cuh"
 #include "fwht.cuh"
 #include "internal.h"
+#include "launch_cache.h"
 
 namespace convrot {
 namespace {
@@ -374,12 +375,7 @@ cudaError_t launch_rotq_t(const RotqArgs &base, int64_t rows, int64_t K, cudaStr
     auto go = [&](auto kernel, int rpt) -> cudaError_t {
         const int64_t per_cta = (int64_t)groups * rpt;
         const int64_t nblocks = (rows + per_cta - 1) / per_cta;
-        int dev = 0, sms = 0, per_sm = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
-        if (e != cudaSuccess) return e;
-        const int64_t resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+        const int64_t resident = (int64_t)sm_count() * blocks_per_sm(reinterpret_cast<const void *>(kernel), threads, 0);
         const int64_t grid = nblocks < resident ? nblocks : resident;
         kernel<<<(unsigned)grid, threads, 0, st>>>(a);
         return cudaGetLastError();
@@ -542,12 +538,7 @@ cudaError_t launch_emb_lookup(const int64_t *ids, int64_t n, const int8_t *Eq, c
     auto go = [&](auto kernel, int rpt) -> cudaError_t {
         const int64_t per_cta = (int64_t)groups * rpt;
         const int64_t nblocks = (n + per_cta - 1) / per_cta;
-        int dev = 0, sms = 0, per_sm = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
-        if (e != cudaSuccess) return e;
-        const int64_t resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+        const int64_t resident = (int64_t)sm_count() * blocks_per_sm(reinterpret_cast<const void *>(kernel), threads, 0);
         const int64_t grid = nblocks < resident ? nblocks : resident;
         kernel<<<(unsigned)grid, threads, 0, st>>>(ids, n, Eq, scale_e, V, D, lanes, G, inv_sqrt_b, out, err);
         return cudaGetLastError();

@@ -21,6 +21,7 @@
 #include "common.cuh"
 #include "fwht.cuh"
 #include "internal.h"
+#include "launch_cache.h"
 #include "wide.cuh"
 
 namespace convrot {
@@ -203,12 +204,7 @@ void shape_for(int64_t len, int &G, int &S) {
 
 template <typename Kernel, typename... Args>
 cudaError_t launch_persistent(Kernel kernel, int threads, int64_t nblocks, cudaStream_t st, Args... args) {
-    int dev = 0, sms = 0, per_sm = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0);
-    if (e != cudaSuccess) return e;
-    const int64_t resident = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+    const int64_t resident = (int64_t)sm_count() * blocks_per_sm(reinterpret_cast<const void *>(kernel), threads, 0);
     const int64_t grid = nblocks < resident ? nblocks : resident;
     kernel<<<(unsigned)grid, threads, 0, st>>>(args...);
     return cudaGetLastError();
@@ -277,9 +273,7 @@ cudaError_t launch_widen_codes(const int8_t *A, int64_t count, uint16_t *out, cu
     if (count == 0) return cudaSuccess;
     if (count % 32 != 0 || !a32(A) || !a32(out)) return launch_widen_i8(A, count, out, st);
     const int64_t n32 = count / 32;
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = sm_count();
     const int64_t want = (n32 + kThreads - 1) / kThreads;
     const int64_t grid = want < (int64_t)sms * 4 ? want : (int64_t)sms * 4;
     widen_codes_kernel<<<(unsigned)grid, kThreads, 0, st>>>(A, n32, out);
