@@ -438,7 +438,27 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
     rows["a8_embedding_lookup"] = _hbm_row(n_ids * 8 + n_ids * D + n_ids * 4 + n_ids * D * 2, ms, pk,
                                            "C5 8192 ids -> bf16 [8192,4096]")
     assert cr.convrot_get_error() == cr.OK
+    del Eq, se, out, id_sets
+    add_same_size_copy(torch, dev, flush, rows)
     return rows
+
+
+def add_same_size_copy(torch, dev, flush, rows):
+    """Context for the memory-bound rows: a device-to-device copy (torch) that moves the
+    same number of bytes, timed the same way.  Launch and ramp cost a visible share of
+    kernels of a few tens of microseconds, which the large-copy peak does not show."""
+    for row in rows.values():
+        nbytes = row.get("algorithmic_bytes")
+        if not nbytes or "GB/s" not in row:
+            continue
+        half = max(int(nbytes // 2) // 256 * 256, 256)
+        a = torch.empty(half, dtype=torch.uint8, device=dev)
+        c = torch.empty_like(a)
+        ms = _time(torch, lambda i: c.copy_(a), flush, 9)
+        copy_gbs = 2 * half / (ms * 1e-3) / 1e9
+        row["same_size_copy_GB/s"] = round(copy_gbs, 1)
+        row["frac_of_same_size_copy"] = round(row["GB/s"] / copy_gbs, 4)
+        del a, c
 
 
 def measure_e2e(cr, torch, dev, x, dY, Wq, sw, WtQ, swt, b, ops_step, steps=4):

@@ -282,6 +282,33 @@ def test_linear_fwd_lora_bypass_parity(M, K, N, rank, with_bias):
     assert rel_fro(f64(yb), full) <= REL_FRO_BF16
 
 
+@pytest.mark.parametrize("case", range(8))
+def test_randomized_small_shapes(case):
+    """Seeded random shapes: M not a multiple of the tile, N a multiple of 16, every block size,
+    an all-zero activation row and an all-zero weight row."""
+    rng = np.random.default_rng(1000 + case)
+    b = int(rng.choice([32, 64, 128, 256]))
+    K = b * int(rng.integers(1, 1024 // b + 1))
+    if K % 16:
+        K = b * 2
+    M = int(rng.integers(1, 700))
+    N = 16 * int(rng.integers(1, 40))
+    x = synth.activations_bf16(2000 + case, M, K, int(rng.integers(0, 8)), 25.0)
+    W = synth.normal_bf16(2000 + case, synth.STREAM_W, N, K, 0.02)
+    x[rng.integers(0, M)] = 0
+    W[rng.integers(0, N)] = 0
+    wq_ref, sw_ref = oracle.quantize_weight(W, b)
+    Wq, sw = cr.convrot_quantize_weight(torch_bf16(W), b)
+    check_codes(codes_of(Wq), wq_ref, f64(W), b)
+    check_scales(sw.cpu().numpy(), sw_ref)
+    y = cr.convrot_linear_fwd(torch_bf16(x), Wq, sw, b)
+    small = torch.empty(cr.convrot_act_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
+    assert torch.equal(y, cr.convrot_linear_fwd(torch_bf16(x), Wq, sw, b, workspace=small))
+    y_ref, _, _ = oracle.linear_fwd(x, codes_of(Wq), sw.cpu().numpy(), b)
+    assert rel_fro(f64(bits_of(y)), f64(y_ref)) <= REL_FRO_ORACLE
+    assert cr.convrot_get_error() == cr.OK
+
+
 def test_linear_fwd_tiny_workload():
     wl = synth.WORKLOADS["tiny"]
     M, K, N, b = wl["M"], wl["K"], wl["N"], wl["block"]
