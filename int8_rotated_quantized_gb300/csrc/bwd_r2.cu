@@ -24,11 +24,18 @@ namespace {
 constexpr int kThreads = 512;
 
 // Codes of D = dY * colscale per row, without rotation: one row per group of
-// G threads, 32 consecutive elements per thread.
+// G threads, 32 consecutive elements per thread.  A thread keeps the same
+// columns for every row, so the block stages its column scales once in shared
+// memory, laid out [s][v][t] as float4 so that a warp's read of them is
+// contiguous.  The next row's loads are issued before this row's reduction,
+// and the partial maxima alternate between two shared arrays so one barrier
+// per row suffices.
 template <int S>
-__global__ void __launch_bounds__(kThreads) scaleq_kernel(const uint16_t *x, int64_t rows, int64_t L,
-                                                          const float *colscale, int G, __half *q, float *scale) {
-    __shared__ float red[kThreads / 32];
+__global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) scaleq_kernel(const uint16_t *x, int64_t rows, int64_t L,
+                                                                          const float *colscale, int G, __half *q,
+                                                                          float *scale) {
+    extern __shared__ float4 cs_s[];  // [S][8][G]
+    __shared__ float red[2][kThreads / 32];
     const int g = threadIdx.x / G;
     const int t = threadIdx.x - g * G;
     const int lane = threadIdx.x & 31;
@@ -36,40 +43,60 @@ __global__ void __launch_bounds__(kThreads) scaleq_kernel(const uint16_t *x, int
     const int groups = blockDim.x / G;
     const int wpg = G >> 5;
     const int64_t chunks = L >> 5;
-    for (int64_t blk = blockIdx.x; blk * groups < rows; blk += gridDim.x) {
+    const int64_t nblocks = (rows + groups - 1) / groups;
+
+    for (int i = threadIdx.x; i < S * 8 * G; i += blockDim.x) {
+        const int s = i / (8 * G), v = (i / G) & 7, tt = i % G;
+        const int64_t c = (int64_t)s * G + tt;
+        cs_s[i] = c < chunks ? __ldg(reinterpret_cast<const float4 *>(colscale + 32 * c) + v)
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+
+    uint32_t raw[S][16];
+    auto fetch = [&](int64_t blk) {
         const int64_t row = blk * groups + g;
-        float e[S][32];
-        float amax = 0.f;
 #pragma unroll
         for (int s = 0; s < S; ++s) {
             const int64_t c = (int64_t)s * G + t;
             if (c < chunks && row < rows) {
-                uint32_t raw[16];
-                ld256(x + row * L + 32 * c, raw);
-                ld256(x + row * L + 32 * c + 16, raw + 8);
-                unpack_bf16x32(raw, e[s]);
-                const float4 *cs = reinterpret_cast<const float4 *>(colscale + 32 * c);
-#pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                    const float4 f = __ldg(cs + v);
-                    e[s][4 * v] = __fmul_rn(e[s][4 * v], f.x);
-                    e[s][4 * v + 1] = __fmul_rn(e[s][4 * v + 1], f.y);
-                    e[s][4 * v + 2] = __fmul_rn(e[s][4 * v + 2], f.z);
-                    e[s][4 * v + 3] = __fmul_rn(e[s][4 * v + 3], f.w);
-                }
+                ld256(x + row * L + 32 * c, raw[s]);
+                ld256(x + row * L + 32 * c + 16, raw[s] + 8);
             } else {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) e[s][i] = 0.f;
+                for (int i = 0; i < 16; ++i) raw[s][i] = 0u;
+            }
+        }
+    };
+
+    int par = 0;
+    int64_t blk = blockIdx.x;
+    if (blk < nblocks) fetch(blk);
+    for (; blk < nblocks; blk += gridDim.x, par ^= 1) {
+        const int64_t row = blk * groups + g;
+        float e[S][32];
+#pragma unroll
+        for (int s = 0; s < S; ++s) unpack_bf16x32(raw[s], e[s]);
+        if (blk + gridDim.x < nblocks) fetch(blk + gridDim.x);
+        float amax = 0.f;
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const float4 f = cs_s[(s * 8 + v) * G + t];
+                e[s][4 * v] = __fmul_rn(e[s][4 * v], f.x);
+                e[s][4 * v + 1] = __fmul_rn(e[s][4 * v + 1], f.y);
+                e[s][4 * v + 2] = __fmul_rn(e[s][4 * v + 2], f.z);
+                e[s][4 * v + 3] = __fmul_rn(e[s][4 * v + 3], f.w);
             }
             amax = fmaxf(amax, amax32(e[s]));
         }
 #pragma unroll
         for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, m));
-        if (lane == 0) red[warp] = amax;
+        if (lane == 0) red[par][warp] = amax;
         __syncthreads();
         float m = 0.f;
-        for (int w = 0; w < wpg; ++w) m = fmaxf(m, red[g * wpg + w]);
-        __syncthreads();  // red is rewritten by the next rows
+        for (int w = 0; w < wpg; ++w) m = fmaxf(m, red[par][g * wpg + w]);
         if (row < rows) {
             const float inv = m > 0.f ? __fdiv_rn(127.f, m) : 0.f;
             if (t == 0) scale[row] = __fdiv_rn(m, 127.f);
@@ -130,12 +157,11 @@ __global__ void __launch_bounds__(kThreads) rot_rows_f32_kernel(const float *P, 
             const int64_t c = (int64_t)s * G + t;
             float e[32];
             if (c < chunks && row < rows) {
-                const float4 *src = reinterpret_cast<const float4 *>(P + row * L + 32 * c);
+                uint32_t raw[32];
 #pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                    const float4 f = src[v];
-                    e[4 * v] = f.x, e[4 * v + 1] = f.y, e[4 * v + 2] = f.z, e[4 * v + 3] = f.w;
-                }
+                for (int v = 0; v < 4; ++v) ld256(P + row * L + 32 * c + 8 * v, raw + 8 * v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) e[i] = __uint_as_float(raw[i]);
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) e[i] = 0.f;
@@ -201,10 +227,14 @@ cudaError_t launch_scaleq(const uint16_t *dY, int64_t M, int64_t N, const float 
     const int groups = G >= kThreads ? 1 : kThreads / G;
     const int64_t grid = grid_for((M + groups - 1) / groups);
     __half *qh = reinterpret_cast<__half *>(q);
+    const int smem = S * 8 * G * (int)sizeof(float4);
+    const void *fn = S == 1 ? (const void *)scaleq_kernel<1> : (const void *)scaleq_kernel<2>;
+    const cudaError_t e = ensure_smem_attr(fn, smem);
+    if (e != cudaSuccess) return e;
     if (S == 1)
-        scaleq_kernel<1><<<(unsigned)grid, groups * G, 0, st>>>(dY, M, N, colscale, G, qh, scale);
+        scaleq_kernel<1><<<(unsigned)grid, groups * G, smem, st>>>(dY, M, N, colscale, G, qh, scale);
     else
-        scaleq_kernel<2><<<(unsigned)grid, groups * G, 0, st>>>(dY, M, N, colscale, G, qh, scale);
+        scaleq_kernel<2><<<(unsigned)grid, groups * G, smem, st>>>(dY, M, N, colscale, G, qh, scale);
     return cudaGetLastError();
 }
 

@@ -6,6 +6,7 @@ profilers (ncu) and quick timing.
     python -m int8_rotated_quantized_gb300.profile_case lookup --V 248000 --D 4096 --n 8192
     python -m int8_rotated_quantized_gb300.profile_case lora --N 12288 --K 4096
     python -m int8_rotated_quantized_gb300.profile_case prep --N 16384 --K 4096
+    python -m int8_rotated_quantized_gb300.profile_case bwd_r2 --M 20480 --N 16384 --K 4096
 
 Each case does one warm-up launch and `--reps` measured launches (CUDA events,
 L2 flushed before each) and prints the median time.
@@ -31,7 +32,7 @@ import synth.gpu as sg  # noqa: E402
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["gemm", "gemm_w16", "gemm_bf16", "widen", "rotq", "lookup", "lora", "prep",
-                                     "dequant", "wquant"])
+                                     "dequant", "wquant", "bwd_r2"])
     ap.add_argument("--M", type=int, default=8192)
     ap.add_argument("--N", type=int, default=16384)
     ap.add_argument("--K", type=int, default=4096)
@@ -117,6 +118,16 @@ def main():
         fn = lambda i: cr.convrot_dequant_weight_t(Wq, sw, b, T)  # noqa: E731
         work = a.N * a.K + a.N * 4 + 2 * a.N * a.K
         unit = "GB/s"
+    elif a.case == "bwd_r2":
+        # --N out features (dY width), --K in features
+        dY = sg.normal_bf16(0, synth.STREAM_DY, a.M, a.N, 1e-3, dev)
+        W = sg.normal_bf16(0, synth.STREAM_W, a.N, a.K, 0.02, dev)
+        Wq, sw = cr.convrot_quantize_weight(W, b)
+        dX = torch.empty((a.M, a.K), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(cr.convrot_bwd_x_r2_workspace_bytes(a.M, a.N, a.K), dtype=torch.uint8, device=dev)
+        fn = lambda i: cr.convrot_linear_bwd_x_r2(dY, Wq, sw, b, dX, ws)  # noqa: E731
+        work = 2.0 * a.M * a.N * a.K
+        unit = "TOPS"
     else:
         T = sg.normal_bf16(0, synth.STREAM_TABLE, a.V, a.D, 0.02, dev)
         Eq, se = cr.convrot_quantize_weight(T, b)
