@@ -69,15 +69,29 @@ __global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) rotq_wide_kernel(con
         }
     };
 
+    // The row after the next one is asked into L2 (one request per 128-byte
+    // line), so the register loads of the next iteration find it there.
+    auto prefetch_l2 = [&](int64_t blk) {
+        const int64_t row = blk * groups + g;
+        if (blk >= nblocks || row >= a.rows || (t & 1)) return;
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            const int64_t c = (int64_t)s * G + t;
+            if (c < chunks) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.x + row * a.ldx + 32 * c));
+        }
+    };
+
     int par = 0;
     int64_t blk = blockIdx.x;
     if (blk < nblocks) fetch(blk);
+    prefetch_l2(blk + gridDim.x);
     for (; blk < nblocks; blk += gridDim.x, par ^= 1) {
         const int64_t row = blk * groups + g;
         float e[S][32];
 #pragma unroll
         for (int s = 0; s < S; ++s) unpack_bf16x32(raw[s], e[s]);
         if (blk + gridDim.x < nblocks) fetch(blk + gridDim.x);
+        prefetch_l2(blk + 2 * (int64_t)gridDim.x);
         float amax = 0.f;
 #pragma unroll
         for (int s = 0; s < S; ++s) {
@@ -105,7 +119,9 @@ __global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) rotq_wide_kernel(con
 }
 
 // out[t] = bf16((scale[id] * Eq[id,:]) R): the transform of the integer codes
-// is exact in fp32; one scaling after it.
+// is exact in fp32; one scaling after it.  The ids run one row ahead of the
+// code loads, which run one row ahead of the arithmetic, so no load waits on
+// the id load issued in the same iteration.
 template <int S, int LOGB>
 __global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) lookup_wide_kernel(const int64_t *ids, int64_t n, const int8_t *Eq,
                                                                const float *scale_e, int64_t V, int64_t D, int G,
@@ -117,12 +133,14 @@ __global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) lookup_wide_kernel(c
     const int64_t chunks = D >> 5;
     const int64_t nblocks = (n + groups - 1) / groups;
 
+    auto load_id = [&](int64_t blk) -> int64_t {
+        const int64_t tok = blk * groups + g;
+        return blk < nblocks && tok < n ? __ldg(ids + tok) : int64_t(-1);
+    };
     uint32_t raw[S][8];
     float sc = 0.f;
-    auto fetch = [&](int64_t blk) {
+    auto fetch = [&](int64_t blk, int64_t id) {
         const int64_t tok = blk * groups + g;
-        int64_t id = -1;
-        if (tok < n) id = __ldg(ids + tok);
         const bool ok = tok < n && id >= 0 && id < V;
         if (tok < n && !ok && t == 0) atomicOr(err, DEVERR_INDEX);
         sc = ok ? __ldg(scale_e + id) : 0.f;
@@ -139,16 +157,21 @@ __global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) lookup_wide_kernel(c
     };
 
     int64_t blk = blockIdx.x;
-    if (blk < nblocks) fetch(blk);
+    int64_t id_next = load_id(blk + gridDim.x);
+    if (blk < nblocks) fetch(blk, load_id(blk));
     for (; blk < nblocks; blk += gridDim.x) {
         const int64_t tok = blk * groups + g;
         float e[S][32];
 #pragma unroll
         for (int s = 0; s < S; ++s)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) e[s][i] = (float)(int8_t)((raw[s][i >> 2] >> (8 * (i & 3))) & 0xff);
+            for (int k = 0; k < 8; ++k) codes_to_f32x4(raw[s][k], &e[s][4 * k]);
         const float s_cur = sc;
-        if (blk + gridDim.x < nblocks) fetch(blk + gridDim.x);
+        if (blk + gridDim.x < nblocks) {
+            const int64_t id = id_next;
+            id_next = load_id(blk + 2 * (int64_t)gridDim.x);
+            fetch(blk + gridDim.x, id);
+        }
 #pragma unroll
         for (int s = 0; s < S; ++s) fwht32<LOGB>(e[s], lane);
         if (tok >= n) continue;
@@ -159,8 +182,9 @@ __global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) lookup_wide_kernel(c
             uint32_t w[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const float y0 = __fmul_rn(__fmul_rn(e[s][2 * i], s_cur), inv_sqrt_b);
-                const float y1 = __fmul_rn(__fmul_rn(e[s][2 * i + 1], s_cur), inv_sqrt_b);
+                float y0 = e[s][2 * i], y1 = e[s][2 * i + 1];
+                mul2c(y0, y1, s_cur);  // (e * s) * (1 / sqrt(b)), two roundings per lane
+                mul2c(y0, y1, inv_sqrt_b);
                 __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
                 w[i] = *reinterpret_cast<uint32_t *>(&h);
             }

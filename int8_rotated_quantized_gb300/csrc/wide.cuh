@@ -111,6 +111,19 @@ __device__ __forceinline__ float amax32(const float (&e)[32]) {
     return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
 }
 
+// int8 x 4 -> four fp32 values of the same integers: bias each byte by 128
+// (xor 0x80), splice it under the exponent of 2^23 (0x4B000000, where the fp32
+// spacing is 1), and subtract 2^23 + 128 exactly.
+__device__ __forceinline__ void codes_to_f32x4(uint32_t w, float *e) {
+    const uint32_t x = w ^ 0x80808080u;
+    e[0] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7540));
+    e[1] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7541));
+    e[2] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7542));
+    e[3] = __uint_as_float(__byte_perm(x, 0x4B000000u, 0x7543));
+    add2c(e[0], e[1], -8388736.0f);
+    add2c(e[2], e[3], -8388736.0f);
+}
+
 // int8 x 4 -> two fp16x2 words holding the same integers: bias each byte by
 // 128 (xor 0x80), splice it under the fp16 exponent of 1024 (0x64), and
 // subtract 1152 = 1024 + 128 exactly.
