@@ -69,29 +69,15 @@ __global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) rotq_wide_kernel(con
         }
     };
 
-    // The row after the next one is asked into L2 (one request per 128-byte
-    // line), so the register loads of the next iteration find it there.
-    auto prefetch_l2 = [&](int64_t blk) {
-        const int64_t row = blk * groups + g;
-        if (blk >= nblocks || row >= a.rows || (t & 1)) return;
-#pragma unroll
-        for (int s = 0; s < S; ++s) {
-            const int64_t c = (int64_t)s * G + t;
-            if (c < chunks) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.x + row * a.ldx + 32 * c));
-        }
-    };
-
     int par = 0;
     int64_t blk = blockIdx.x;
     if (blk < nblocks) fetch(blk);
-    prefetch_l2(blk + gridDim.x);
     for (; blk < nblocks; blk += gridDim.x, par ^= 1) {
         const int64_t row = blk * groups + g;
         float e[S][32];
 #pragma unroll
         for (int s = 0; s < S; ++s) unpack_bf16x32(raw[s], e[s]);
         if (blk + gridDim.x < nblocks) fetch(blk + gridDim.x);
-        prefetch_l2(blk + 2 * (int64_t)gridDim.x);
         float amax = 0.f;
 #pragma unroll
         for (int s = 0; s < S; ++s) {
