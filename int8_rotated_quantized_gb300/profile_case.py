@@ -32,7 +32,7 @@ import synth.gpu as sg  # noqa: E402
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case", choices=["gemm", "gemm_w16", "gemm_bf16", "widen", "rotq", "lookup", "lora", "prep",
-                                     "dequant", "wquant", "bwd_r2"])
+                                     "dequant", "wquant", "bwd_r2", "fwd_lora"])
     ap.add_argument("--M", type=int, default=8192)
     ap.add_argument("--N", type=int, default=16384)
     ap.add_argument("--K", type=int, default=4096)
@@ -126,6 +126,17 @@ def main():
         dX = torch.empty((a.M, a.K), dtype=torch.bfloat16, device=dev)
         ws = torch.empty(cr.convrot_bwd_x_r2_workspace_bytes(a.M, a.N, a.K), dtype=torch.uint8, device=dev)
         fn = lambda i: cr.convrot_linear_bwd_x_r2(dY, Wq, sw, b, dX, ws)  # noqa: E731
+        work = 2.0 * a.M * a.N * a.K
+        unit = "TOPS"
+    elif a.case == "fwd_lora":
+        # forward with an unmerged rank-16 adapter as a bypass in the GEMM epilogue
+        x = sg.activations_bf16(0, a.M, a.K, 41, 30.0, dev)
+        W = sg.normal_bf16(0, synth.STREAM_W, a.N, a.K, 0.02, dev)
+        Wq, sw = cr.convrot_quantize_weight(W, b)
+        A, B = sg.lora_pair(0, a.N, a.K, 16, 0.01, dev)
+        y = torch.empty((a.M, a.N), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(cr.convrot_linear_lora_workspace_bytes(a.M, a.K, a.N), dtype=torch.uint8, device=dev)
+        fn = lambda i: cr.convrot_linear_fwd_lora(x, Wq, sw, b, A, B, 16.0, 1.0, None, y, ws)  # noqa: E731
         work = 2.0 * a.M * a.N * a.K
         unit = "TOPS"
     else:
