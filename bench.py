@@ -16,12 +16,14 @@ bounded sample of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import statistics
 import subprocess
 import sys
 import tempfile
+import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -78,22 +80,82 @@ def peaks():
 
 # ---------------------------------------------------------------- clocks ----
 
+class NvmlSampler:
+    """The SM clock and the clock-event reasons of one GPU, read through NVML
+    (the driver's libnvidia-ml, read-only queries) every 2 ms on a background
+    thread, so a timed region of tens of milliseconds still gets many samples."""
+
+    NVML_CLOCK_SM = 1
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, uuid, index: int):
+        self.samples, self.reasons, self.max_mhz, self.lib = [], 0, None, None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            found = bool(uuid) and lib.nvmlDeviceGetHandleByUUID(("GPU-" + uuid).encode(), ctypes.byref(h)) == 0
+            if not found and lib.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self.reason_fn = (getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+                              or getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons", None))
+            self.lib, self.h = lib, h
+        except (OSError, AttributeError):
+            self.lib = None
+            return
+        self.stop_evt = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def _run(self):
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop_evt.is_set():
+            if self.lib.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, ctypes.byref(mhz)) == 0:
+                self.samples.append(float(mhz.value))
+            if self.reason_fn is not None and self.reason_fn(self.h, ctypes.byref(rs)) == 0:
+                self.reasons |= int(rs.value)
+            time.sleep(0.002)
+
+    def stop(self):
+        if self.lib is None:
+            return None
+        self.stop_evt.set()
+        self.thread.join(timeout=5)
+        names = sorted(n for bit, n in self.REASON_BITS.items() if self.reasons & bit)
+        return {"samples": list(self.samples), "max_mhz": self.max_mhz, "reasons": names}
+
+
+def gpu_uuid(torch, dev):
+    u = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    return str(u) if u is not None else None
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 100 ms in the background."""
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms in the background,
+    plus the in-process NVML sampler for short regions."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, uuid=None):
         self.file = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
         self.proc = None
+        self.nvml = None
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", ("GPU-" + uuid) if uuid else str(gpu_index),
+                                          f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.file, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+
+    def start_fine(self, gpu_index: int, uuid=None):
+        """Begin the 2 ms NVML sampling (call right before the timed region)."""
+        self.nvml = NvmlSampler(uuid, gpu_index)
 
     def stop(self):
         if self.proc is not None:
@@ -117,9 +179,18 @@ class ClockSampler:
                         reasons.add(name)
             except (ValueError, IndexError):
                 continue
+        source = "nvidia-smi every 100 ms"
+        fine = self.nvml.stop() if self.nvml is not None else None
+        if fine and fine["samples"]:
+            # the median comes from the timed region alone; reasons from both samplers
+            sm = fine["samples"]
+            mx = max(mx, fine["max_mhz"] or 0.0)
+            reasons |= set(fine["reasons"])
+            source = "NVML every 2 ms during the timed region (reasons also from nvidia-smi every 100 ms)"
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "source": source}
 
 
 # ------------------------------------------------------------ our kernels ----
@@ -192,6 +263,8 @@ def run_gpu(args):
         mark(6)
 
     launches_per_step = 6
+    uuid = gpu_uuid(torch, dev)
+    sampler = ClockSampler(local, uuid) if rank == 0 else None
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -199,7 +272,8 @@ def run_gpu(args):
     assert cr.convrot_get_error() == cr.OK
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
-    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler is not None:
+        sampler.start_fine(local, uuid)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
