@@ -211,7 +211,9 @@ int convrot_linear_fwd(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq
 
 size_t convrot_linear_lora_workspace_bytes(int64_t M, int64_t K, int64_t N) {
     if (M < 0 || K < 0 || N < 0) return 0;
-    return convrot_linear_workspace_bytes(M, K, N) + align256((size_t)convrot::lora_xa_ld(M) * 16 * sizeof(float));
+    const int splits = convrot::lora_down_splits(M, K);
+    const size_t xa_bytes = align256((size_t)convrot::lora_xa_ld(M) * 16 * sizeof(float));
+    return convrot_linear_workspace_bytes(M, K, N) + xa_bytes + (splits > 1 ? (size_t)splits * xa_bytes : 0);
 }
 
 int convrot_linear_fwd_lora(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq, const float *scale_w,
@@ -238,7 +240,9 @@ int convrot_linear_fwd_lora(const uint16_t *x, int64_t M, int64_t K, const int8_
     const float coef = (float)((double)scale * (double)alpha / (double)rank);
     rc = quantize_act_impl(x, M, K, K, block, xq, sx, st);
     if (rc != CONVROT_OK) return rc;
-    rc = cuda_status(convrot::launch_lora_down(x, M, K, lora_A, rank, coef, xa, st));
+    float *part = reinterpret_cast<float *>(reinterpret_cast<char *>(xa) +
+                                            align256((size_t)convrot::lora_xa_ld(M) * 16 * sizeof(float)));
+    rc = cuda_status(convrot::launch_lora_down(x, M, K, lora_A, rank, coef, xa, part, st));
     if (rc != CONVROT_OK) return rc;
     rc = cuda_status(convrot::launch_widen_codes(Wq, N * K, w16, st));
     if (rc != CONVROT_OK) return rc;

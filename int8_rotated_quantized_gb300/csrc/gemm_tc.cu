@@ -147,6 +147,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// (a0, a1) <- (x0 * k + a0, x1 * k + a1) on fp32 values held as int bits: one
+// rounding per lane, bit-identical to two fmaf.
+__device__ __forceinline__ void fma2_acc(int &a0, int &a1, float x0, float x1, float k) {
+    asm("{\n .reg .b64 ra, rx, rk;\n mov.b64 ra, {%0, %1};\n mov.b64 rx, {%2, %3};\n mov.b64 rk, {%4, %4};\n"
+        " fma.rn.f32x2 ra, rx, rk, ra;\n mov.b64 {%0, %1}, ra;\n}"
+        : "+r"(a0), "+r"(a1)
+        : "f"(x0), "f"(x1), "f"(k));
+}
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -572,10 +581,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                         for (int i4 = 0; i4 < 128; i4 += 4) {
                             const float4 v = row[i4 >> 2];  // every lane reads the same 16 bytes
-                            acc[i4] = __float_as_int(__fmaf_rn(v.x, bj, __int_as_float(acc[i4])));
-                            acc[i4 + 1] = __float_as_int(__fmaf_rn(v.y, bj, __int_as_float(acc[i4 + 1])));
-                            acc[i4 + 2] = __float_as_int(__fmaf_rn(v.z, bj, __int_as_float(acc[i4 + 2])));
-                            acc[i4 + 3] = __float_as_int(__fmaf_rn(v.w, bj, __int_as_float(acc[i4 + 3])));
+                            // y += xa * b on packed pairs (one rounding per lane, as fmaf)
+                            fma2_acc(acc[i4], acc[i4 + 1], v.x, v.y, bj);
+                            fma2_acc(acc[i4 + 2], acc[i4 + 3], v.z, v.w, bj);
                         }
                     }
                     // pass 3: round and store

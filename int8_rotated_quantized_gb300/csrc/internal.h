@@ -59,8 +59,11 @@ cudaError_t launch_gemm_w16_lora(const uint16_t *A, const float *sa, const uint1
 // so the epilogue's 128-token halves never leave the rows.
 __host__ __device__ inline int64_t lora_xa_ld(int64_t M) { return (M + 255) / 256 * 256; }
 // xa^T[j, m] = coef * sum_k x[m, k] A[j, k] for j < rank (lora_rotq.cu); K % 32 == 0.
+// When lora_down_splits(M, K) > 1 the column spans' partial sums go to `part`
+// ([splits][16][lora_xa_ld(M)] floats) and a second kernel adds them in span order.
+int lora_down_splits(int64_t M, int64_t K);
 cudaError_t launch_lora_down(const uint16_t *x, int64_t M, int64_t K, const float *A, int rank, float coef, float *xa,
-                             cudaStream_t st);
+                             float *part, cudaStream_t st);
 // int8 codes -> fp16 values holding the same integers, 32 per thread (rotq_wide.cu).
 cudaError_t launch_widen_codes(const int8_t *A, int64_t count, uint16_t *out, cudaStream_t st);
 
