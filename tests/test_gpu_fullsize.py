@@ -45,6 +45,19 @@ def _normal_rows(stream, rows, cols, sigma):
     return np.concatenate([synth.normal_bf16(0, stream, 1, cols, sigma, row0=int(r)) for r in rows])
 
 
+def _oracle_weight(W_gpu, Wq, sw, b):
+    """The oracle's quantization of the whole weight (its input: the bits of the shared
+    seeded generator), checked against the GPU's, and uploaded so that the GPU's
+    backward runs on exactly the codes the oracle's reference uses."""
+    w_np = bits_of(W_gpu)
+    wq_ref, sw_ref = oracle.quantize_rows_bf16(w_np, b)
+    check_codes(codes_of(Wq), wq_ref, f64(w_np), b, "weight codes (all rows)")
+    check_scales(sw.cpu().numpy(), sw_ref, "weight scales (all rows)")
+    wq_dev = torch.from_numpy(wq_ref).cuda()
+    sw_dev = torch.from_numpy(sw_ref).cuda()
+    return wq_ref, sw_ref, wq_dev, sw_dev
+
+
 def _check_fwd(wl, x_gpu, W_gpu, Wq, sw, y, rng):
     M, K = x_gpu.shape
     N = W_gpu.shape[0]
@@ -123,13 +136,14 @@ def test_qkv_lora_bypass_forward_full_size():
     A_np, B_np = synth.lora_pair(0, N, K, r, wl["lora_sigma"])
     x_rows = _act_rows(wl, ms, K)
     assert np.array_equal(bits_of(x[torch.from_numpy(ms).cuda()]), x_rows)
-    wq_s = codes_of(Wq[torch.from_numpy(ns).cuda()])
-    sw_s = sw.cpu().numpy()[ns]
+    w_rows = _normal_rows(synth.STREAM_W, ns, K, wl["w_sigma"])
+    wq_s, sw_s = oracle.quantize_rows_bf16(w_rows, b)
+    check_codes(codes_of(Wq[torch.from_numpy(ns).cuda()]), wq_s, f64(w_rows), b, "weight codes")
+    check_scales(sw.cpu().numpy()[ns], sw_s, "weight scales")
     ref = oracle.linear_fwd_lora(x_rows, wq_s, sw_s, b, A_np, B_np[ns], alpha, scale)
     got = bits_of(y[torch.from_numpy(ms).cuda()][:, torch.from_numpy(ns).cuda()])
     assert rel_fro(f64(got), f64(ref)) <= REL_FRO_ORACLE
     assert np.mean(got == ref) > 0.9
-    w_rows = _normal_rows(synth.STREAM_W, ns, K, wl["w_sigma"])
     merged = oracle.lora_merge(w_rows, A_np, B_np[ns], alpha, scale)
     assert rel_fro(f64(got), f64(x_rows) @ f64(merged).T) <= REL_FRO_BF16
 
@@ -144,13 +158,13 @@ def test_train20k_forward_and_backward_full_size():
     rng = np.random.default_rng(4)
     _check_fwd(wl, x, W, Wq, sw, y, rng)
     del y
-    # backward: the prepared weight on two Hadamard blocks along K, then grad_x
-    WtQ, swt = cr.convrot_prepare_bwd_weight(Wq, sw, b)
+    # backward: the prepared weight on two Hadamard blocks along K, then grad_x, on the
+    # oracle's weight codes (checked against the GPU's on every row)
+    wq_np, sw_np, Wq_o, sw_o = _oracle_weight(W, Wq, sw, b)
+    WtQ, swt = cr.convrot_prepare_bwd_weight(Wq_o, sw_o, b)
     dY = sg.normal_bf16(0, synth.STREAM_DY, M, N, wl["dy_sigma"], "cuda")
     dX = cr.convrot_linear_bwd_x(dY, WtQ, swt, b)
     assert cr.convrot_get_error() == cr.OK
-    wq_np = codes_of(Wq)
-    sw_np = sw.cpu().numpy()
     kblocks = np.sort(rng.choice(K // b, size=2, replace=False))
     ks = np.concatenate([np.arange(kb * b, (kb + 1) * b) for kb in kblocks])
     wtq_ref = np.empty((len(ks), N), dtype=np.int8)
@@ -177,14 +191,14 @@ def test_train20k_bf16_backward_full_size():
     M, K, N, b = wl["M"], wl["K"], wl["N"], wl["block"]
     W = sg.normal_bf16(0, synth.STREAM_W, N, K, wl["w_sigma"], "cuda")
     Wq, sw = cr.convrot_quantize_weight(W, b)
+    wq_np, sw_np, Wq_o, sw_o = _oracle_weight(W, Wq, sw, b)
     dY = sg.normal_bf16(0, synth.STREAM_DY, M, N, wl["dy_sigma"], "cuda")
     ws = torch.empty(cr.convrot_bwd_x_bf16_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
-    dX = cr.convrot_linear_bwd_x_bf16(dY, Wq, sw, b, workspace=ws)
+    dX = cr.convrot_linear_bwd_x_bf16(dY, Wq_o, sw_o, b, workspace=ws)
     assert cr.convrot_get_error() == cr.OK
     rng = np.random.default_rng(6)
     kblocks = np.sort(rng.choice(K // b, size=2, replace=False))
     ks = np.concatenate([np.arange(kb * b, (kb + 1) * b) for kb in kblocks])
-    wq_np, sw_np = codes_of(Wq), sw.cpu().numpy()
     weff_ref = np.concatenate([oracle.dequant_weight_t(np.ascontiguousarray(wq_np[:, kb * b:(kb + 1) * b]), sw_np, b)
                                for kb in kblocks])                      # [len(ks), N]
     weff_dev = ws[:K * N * 2].view(torch.int16).view(K, N)[torch.from_numpy(ks).cuda()].cpu().numpy().view(np.uint16)
@@ -200,6 +214,34 @@ def test_train20k_bf16_backward_full_size():
     assert np.mean(dx_s == dx_ref) > 0.98
     w_cols = bits_of(W[:, torch.from_numpy(ks).cuda()])
     assert rel_fro(g, f64(dy_rows) @ f64(w_cols)) <= REL_FRO_BF16
+
+
+def test_train20k_int8_backward_second_reading_full_size():
+    wl = synth.WORKLOADS["train20k"]
+    M, K, N, b = wl["M"], wl["K"], wl["N"], wl["block"]
+    W = sg.normal_bf16(0, synth.STREAM_W, N, K, wl["w_sigma"], "cuda")
+    Wq, sw = cr.convrot_quantize_weight(W, b)
+    wq_np, sw_np, Wq_o, sw_o = _oracle_weight(W, Wq, sw, b)
+    dY = sg.normal_bf16(0, synth.STREAM_DY, M, N, wl["dy_sigma"], "cuda")
+    ws = torch.empty(cr.convrot_bwd_x_r2_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    dX = cr.convrot_linear_bwd_x_r2(dY, Wq_o, sw_o, b, workspace=ws)
+    assert cr.convrot_get_error() == cr.OK
+    rng = np.random.default_rng(9)
+    ms = _rows(rng, M, 16)
+    dy_rows = _normal_rows(synth.STREAM_DY, ms, N, wl["dy_sigma"])
+    assert np.array_equal(bits_of(dY[torch.from_numpy(ms).cuda()]), dy_rows)
+    dx_ref, dq_ref, sd_ref = oracle.linear_bwd_x_r2(dy_rows, wq_np, sw_np, b)
+    # the unrotated codes and the row scales are decided in the same fp32 arithmetic: identical
+    dq = ws[:M * N * 2].view(torch.float16).view(M, N)[torch.from_numpy(ms).cuda()]
+    np.testing.assert_array_equal(codes_of(dq), dq_ref)
+    off = (M * N * 2 + 255) // 256 * 256
+    np.testing.assert_array_equal(ws[off:off + 4 * M].view(torch.float32).cpu().numpy()[ms], sd_ref)
+    got = bits_of(dX[torch.from_numpy(ms).cuda()])
+    g, r = f64(got), f64(dx_ref)
+    # one bf16 step, plus an allowance for the fp32 scaling and rotation near zero (as the parity tests)
+    assert np.all(np.abs(g - r) <= np.abs(r) * 2.0 ** -7 + 64 * 2.0 ** -24 * np.sqrt(K) * np.sqrt(np.mean(r * r)))
+    assert np.mean(got == dx_ref) > 0.98
+    assert rel_fro(g, f64(dy_rows) @ f64(bits_of(W))) <= REL_FRO_BF16
 
 
 def test_embed_table_and_lookup_full_size():

@@ -235,6 +235,8 @@ def test_widened_weight_path_is_bit_identical(M, K, N):
     x = synth.activations_bf16(19, M, K, 8, 30.0)
     W = synth.normal_bf16(19, synth.STREAM_W, N, K, 0.02)
     Wq, sw = cr.convrot_quantize_weight(torch_bf16(W), b)
+    wq_ref, sw_ref = oracle.quantize_weight(W, b)
+    check_codes(codes_of(Wq), wq_ref, f64(W), b)
     w16 = cr.convrot_widen_codes(Wq)
     assert torch.equal(w16.float(), Wq.float())
     fast = cr.convrot_linear_fwd(torch_bf16(x), Wq, sw, b)
@@ -243,18 +245,24 @@ def test_widened_weight_path_is_bit_identical(M, K, N):
     assert torch.equal(fast, fused)
     xq, sx = cr.convrot_quantize_activation(torch_bf16(x), b)
     assert torch.equal(cr.convrot_gemm_dequant_w16(xq, sx, w16, sw), cr.convrot_gemm_dequant(xq, sx, Wq, sw))
-    y_ref, _, _ = oracle.linear_fwd(x, codes_of(Wq), sw.cpu().numpy(), b)
+    # against the oracle, every oracle input from the oracle: the GPU runs on the oracle's codes
+    y_ref, _, _ = oracle.linear_fwd(x, wq_ref, sw_ref, b)
+    y_o = cr.convrot_linear_fwd(torch_bf16(x), _i8(wq_ref), _f32(sw_ref), b)
+    assert rel_fro(f64(bits_of(y_o)), f64(y_ref)) <= REL_FRO_ORACLE
     assert rel_fro(f64(bits_of(fast)), f64(y_ref)) <= REL_FRO_ORACLE
     # int32 path of the widened operand: exact integer sums
     A = np.random.default_rng(19).integers(-127, 128, size=(M, K), dtype=np.int8)
-    acc = cr.convrot_gemm_s32(_i8(A), Wq)
-    np.testing.assert_array_equal(acc.cpu().numpy(), oracle.gemm_s32(A, codes_of(Wq)))
+    acc = cr.convrot_gemm_s32(_i8(A), _i8(wq_ref))
+    np.testing.assert_array_equal(acc.cpu().numpy(), oracle.gemm_s32(A, wq_ref))
 
 
 @pytest.mark.parametrize("M,K,N,rank,with_bias", [(300, 1024, 272, 16, False), (65, 512, 128, 5, True),
-                                                   (513, 4096, 400, 16, True)])
+                                                   (513, 4096, 400, 16, True), (65, 256, 128, 8, False),
+                                                   (40, 1056, 96, 16, True)])
 def test_linear_fwd_lora_bypass_parity(M, K, N, rank, with_bias):
-    b = 128
+    """Shapes cover one column span (K = 256), 2, 4 and 8 spans, and spans that do not
+    divide K (K = 1056: the last span is empty)."""
+    b = 128 if K % 128 == 0 else 32
     x = synth.activations_bf16(21, M, K, 8, 30.0)
     W = synth.normal_bf16(21, synth.STREAM_W, N, K, 0.02)
     A, B = synth.lora_pair(21, N, K, rank, 0.05)
@@ -304,8 +312,10 @@ def test_randomized_small_shapes(case):
     y = cr.convrot_linear_fwd(torch_bf16(x), Wq, sw, b)
     small = torch.empty(cr.convrot_act_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
     assert torch.equal(y, cr.convrot_linear_fwd(torch_bf16(x), Wq, sw, b, workspace=small))
-    y_ref, _, _ = oracle.linear_fwd(x, codes_of(Wq), sw.cpu().numpy(), b)
+    y_ref, _, _ = oracle.linear_fwd(x, wq_ref, sw_ref, b)
     assert rel_fro(f64(bits_of(y)), f64(y_ref)) <= REL_FRO_ORACLE
+    y_o = cr.convrot_linear_fwd(torch_bf16(x), _i8(wq_ref), _f32(sw_ref), b)
+    assert rel_fro(f64(bits_of(y_o)), f64(y_ref)) <= REL_FRO_ORACLE
     assert cr.convrot_get_error() == cr.OK
 
 
