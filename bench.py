@@ -78,6 +78,22 @@ def peaks():
         return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
+# ------------------------------------------------------------- multi-rank ----
+
+def max_over_ranks(torch, dist, ms, device):
+    """The job's time: the slowest rank's (all-reduce MAX; a no-op on one process)."""
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(world, ops_per_step, steps, job_ms):
+    """Whole-job TOPS: every rank runs its own batch (no data-path collective), so the
+    work is world x steps x ops_per_step over the slowest rank's time."""
+    return world * ops_per_step * steps / (job_ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- clocks ----
 
 class NvmlSampler:
@@ -294,15 +310,11 @@ def run_gpu(args):
     k1d = [e[3].elapsed_time(e[4]) for e in evs]
     wb = [e[4].elapsed_time(e[5]) for e in evs]
     gb = [e[5].elapsed_time(e[6]) for e in evs]
-    total_ms = sum(step_ms)
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(torch, dist, sum(step_ms), dev)
     assert cr.convrot_get_error() == cr.OK
 
     ops_step = 2.0 * 2.0 * M * N * K           # fwd + grad_x GEMMs
-    value = world * ops_step * args.steps / (total_ms * 1e-3) / 1e12
+    value = weak_scaling_value(world, ops_step, args.steps, total_ms)
     gemm_ms = statistics.mean(gf + gb)
     gemm_tflops = 2.0 * M * N * K / (gemm_ms * 1e-3) / 1e12
 

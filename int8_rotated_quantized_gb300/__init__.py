@@ -156,6 +156,17 @@ def convrot_quantize_weight(W, block, lora_A=None, lora_B=None, alpha=1.0, scale
     return Wq, scale_w
 
 
+def shard_rows(M: int, world: int, rank: int):
+    """Token rows [start, start + count) of one data-parallel rank.  Every step of the
+    layer is independent per token row (the rotation and the scale act within a row,
+    the GEMM's rows are independent), so ranks run their shards with no exchange."""
+    if world < 1 or not 0 <= rank < world or M < 0:
+        raise ValueError("bad shard")
+    base, extra = divmod(M, world)
+    start = rank * base + min(rank, extra)
+    return start, base + (1 if rank < extra else 0)
+
+
 def convrot_quantize_activation(x, block, xq=None, scale_x=None, stream=None):
     """Rotate + quantize the rows of x (bf16 [M, K]).  Returns (codes as fp16 [M, K], scale fp32 [M])."""
     _need(x, torch.bfloat16, "x", 2)
