@@ -157,7 +157,9 @@ CONVROT_API int convrot_linear_fwd(const uint16_t *x, int64_t M, int64_t K, cons
                        uint16_t *y, void *workspace, size_t ws_bytes, convrot_stream_t stream);
 
 /* Bytes of workspace convrot_linear_fwd_lora needs: those of the widened-weight
- * path plus the scaled down-projection (16 rows of M rounded up to 256, fp32). */
+ * path plus the scaled down-projection (16 rows of M rounded up to 256, fp32)
+ * and, when the down-projection splits K into column spans (few rows), one
+ * partial-sum array of that size per span (at most 8). */
 CONVROT_API size_t convrot_linear_lora_workspace_bytes(int64_t M, int64_t K, int64_t N);
 
 /* Forward with an unmerged LoRA adapter as a bypass (the LoRA branch of a
