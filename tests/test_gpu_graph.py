@@ -1,0 +1,57 @@
+"""The layer's calls inside a captured CUDA graph.
+
+Every entry point only enqueues work on the caller's stream (no allocation, no
+synchronisation), so a training step of the layer can be captured once and
+replayed; the replay must give exactly the bits of the eager calls."""
+import pytest
+
+import synth
+from helpers import torch_bf16
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import int8_rotated_quantized_gb300 as cr  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    cr._build.build()
+    cr.lib()
+
+
+def test_step_replays_from_a_cuda_graph():
+    M, K, N, b = 300, 512, 384, 128
+    x = torch_bf16(synth.activations_bf16(31, M, K, 4, 20.0))
+    W = torch_bf16(synth.normal_bf16(31, synth.STREAM_W, N, K, 0.02))
+    dY = torch_bf16(synth.normal_bf16(31, synth.STREAM_DY, M, N, 1e-3))
+    Wq, sw = cr.convrot_quantize_weight(W, b)
+    WtQ, swt = cr.convrot_prepare_bwd_weight(Wq, sw, b)
+    ws = torch.empty(max(cr.convrot_linear_workspace_bytes(M, K, N), cr.convrot_linear_workspace_bytes(M, N, K)),
+                     dtype=torch.uint8, device="cuda")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    dX = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # eager calls first: per-device launch parameters are cached before capture
+        cr.convrot_linear_fwd(x, Wq, sw, b, y=y, workspace=ws, stream=s)
+        cr.convrot_linear_bwd_x(dY, WtQ, swt, b, dX=dX, workspace=ws, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    y_eager, dx_eager = y.clone(), dX.clone()
+    y.zero_()
+    dX.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st = torch.cuda.current_stream()
+        cr.convrot_linear_fwd(x, Wq, sw, b, y=y, workspace=ws, stream=st)
+        cr.convrot_linear_bwd_x(dY, WtQ, swt, b, dX=dX, workspace=ws, stream=st)
+    for _ in range(2):
+        y.zero_()
+        dX.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_eager) and torch.equal(dX, dx_eager)
+    assert cr.convrot_get_error() == cr.OK
