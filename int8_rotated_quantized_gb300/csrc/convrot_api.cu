@@ -68,6 +68,13 @@ int gemm_impl(const uint16_t *xq, const float *sx, int64_t M, int64_t K, const i
 
 }  // namespace
 
+namespace convrot {
+unsigned *current_error_word() {
+    unsigned *err = nullptr;
+    return device_setup(&err) == CONVROT_OK ? err : nullptr;
+}
+}  // namespace convrot
+
 extern "C" {
 
 const char *convrot_status_string(int status) {

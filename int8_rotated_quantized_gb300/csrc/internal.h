@@ -21,6 +21,8 @@ bool lora_cluster_ok(const void *W, int64_t K, int64_t ldw, int block, const flo
 cudaError_t launch_lora_cluster(const uint16_t *W, int64_t rows, int64_t K, int64_t ldw, int block, const float *A,
                                 const float *B, int rank, float coef, int8_t *q, float *scale, unsigned *err,
                                 cudaStream_t st);
+// The device error word of the current device (convrot_api.cu), or null.
+unsigned *current_error_word();
 bool lookup_wide_ok(const void *Eq, int64_t D, const void *out);
 cudaError_t launch_lookup_wide(const int64_t *ids, int64_t n, const int8_t *Eq, const float *scale_e, int64_t V,
                                int64_t D, int block, uint16_t *out, unsigned *err, cudaStream_t st);

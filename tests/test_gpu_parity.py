@@ -91,15 +91,20 @@ def test_quantize_weight_parity(block, K):
     assert float(sw[5]) == 0.0 and int(Wq[5].abs().max()) == 0
 
 
-@pytest.mark.parametrize("K", [12288, 16384, 32768])
-def test_quantize_long_rows_parity(K):
-    """Rows longer than one CTA pass (several 8-element slots per thread, partly masked)."""
+@pytest.mark.parametrize("K,block", [(12288, 128), (16384, 128), (32768, 128), (8192, 64), (12288, 256), (8256, 64)])
+def test_quantize_long_rows_parity(K, block):
+    """Long rows: the TMA-staged kernel (multiples of 64 from 8192 to 16384 elements, including a
+    row group narrower than the CTA) and rows longer than one CTA pass; fp16-held and int8 codes."""
     M = 9
     x = synth.activations_bf16(2, M, K, 41, 30.0)
-    q_ref, s_ref = oracle.quantize_rows_bf16(x, 128)
-    xq, sx = cr.convrot_quantize_activation(torch_bf16(x), 128)
-    check_codes(codes_of(xq), q_ref, f64(x), 128)
+    q_ref, s_ref = oracle.quantize_rows_bf16(x, block)
+    xq, sx = cr.convrot_quantize_activation(torch_bf16(x), block)
+    check_codes(codes_of(xq), q_ref, f64(x), block)
     check_scales(sx.cpu().numpy(), s_ref)
+    Wq, sw = cr.convrot_quantize_weight(torch_bf16(x), block)
+    check_codes(codes_of(Wq), q_ref, f64(x), block)
+    check_scales(sw.cpu().numpy(), s_ref)
+    assert cr.convrot_get_error() == cr.OK
 
 
 @pytest.mark.parametrize("block", [32, 128])
