@@ -211,6 +211,11 @@ __global__ void __launch_bounds__(kThreads, 2) rotq_tma_kernel(const __grid_cons
             if (t < chunks) store_codes32(e, inv, static_cast<OutT *>(a.q) + row * a.K + 32 * t);
         }
     }
+    if (abort_flag && threadIdx.x == 0) {  // a wait gave up: give copies still in flight time to land
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 200000ull) {
+        }
+    }
 }
 
 // out[t] = bf16((scale[id] * Eq[id,:]) R): the transform of the integer codes
