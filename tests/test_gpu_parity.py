@@ -118,18 +118,21 @@ def test_quantize_activation_parity(block):
     check_scales(sx.cpu().numpy(), s_ref)
 
 
-def test_quantize_weight_with_row_stride():
-    N, K, ld = 40, 256, 384
+@pytest.mark.parametrize("N,K,ld,block", [(40, 256, 384, 32), (7, 8192, 8320, 128)])
+def test_quantize_weight_with_row_stride(N, K, ld, block):
+    """Rows with a stride larger than their length (the second case goes through the
+    TMA-staged kernel, whose tensor map carries the stride)."""
     Wfull = synth.normal_bf16(4, synth.STREAM_W, N, ld, 0.02)
-    q_ref, s_ref = oracle.quantize_weight(np.ascontiguousarray(Wfull[:, :K]), 32)
+    q_ref, s_ref = oracle.quantize_weight(np.ascontiguousarray(Wfull[:, :K]), block)
     t = torch_bf16(Wfull)
     Wq = torch.empty((N, K), dtype=torch.int8, device="cuda")
     sw = torch.empty((N,), dtype=torch.float32, device="cuda")
-    rc = cr.lib().convrot_quantize_weight(cr._ptr(t), N, K, ld, 32, None, None, 0, 1.0, 1.0, cr._ptr(Wq), cr._ptr(sw),
-                                          cr._stream(None))
+    rc = cr.lib().convrot_quantize_weight(cr._ptr(t), N, K, ld, block, None, None, 0, 1.0, 1.0, cr._ptr(Wq),
+                                          cr._ptr(sw), cr._stream(None))
     assert rc == cr.OK
-    check_codes(codes_of(Wq), q_ref, f64(Wfull[:, :K]), 32)
+    check_codes(codes_of(Wq), q_ref, f64(Wfull[:, :K]), block)
     check_scales(sw.cpu().numpy(), s_ref)
+    assert cr.convrot_get_error() == cr.OK
 
 
 # Cases of the cluster kernel (rank <= 16 padded to 4, 8 or 16; K split into
