@@ -439,7 +439,7 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
     rows["a6_prep_bwd_weight"] = _hbm_row(N * K + N * 4 + K * N + K * 4, ms, pk,
                                           "C4 Wq [16384,4096] -> WtQ [4096,16384] (one-off, via a double-float workspace)")
     del ws
-    # next row 1: the bf16 backward mode (transient dequantization + bf16 tcgen05 GEMM), C4 shapes
+    # the bf16 backward mode (transient dequantization + bf16 tcgen05 GEMM), on the 20k-token shapes
     M = wl["M"]
     weff_t = torch.empty((K, N), dtype=torch.bfloat16, device=dev)
     ms = _time(torch, lambda i: cr.convrot_dequant_weight_t(Wq, sw, b, weff_t), flush, reps)
@@ -451,7 +451,7 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
     rows["n1_bf16_bwd_gemm"] = _tc_row(2.0 * M * N * K, ms, pk, "C4 dY [20480,16384] . W_eff -> dX bf16 [20480,4096]")
     rows["n1_bf16_bwd_gemm"].update({"traffic": gemm_traffic_per_launch("bf16_bwd"),
                                      "algorithmic_bytes": M * N * 2 + K * N * 2 + M * K * 2})
-    # next row 3: the second reading of the int8 backward (no prepared weight copy), and the accuracy of the
+    # the second reading of the int8 backward (no prepared weight copy), and the accuracy of the
     # two int8 readings against the bf16 mode on this workload
     ws3 = torch.empty(cr.convrot_bwd_x_r2_workspace_bytes(M, N, K), dtype=torch.uint8, device=dev)
     dX3 = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
@@ -484,7 +484,7 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
     rows["a1a2_lora_merge_quant"].update({"fma_per_s_T": round(fma / (ms * 1e-3) / 1e12, 2),
                                           "fma_peak_T": round(fma_peak / 1e12, 2),
                                           "fma_frac": round(fma / (ms * 1e-3) / fma_peak, 4)})
-    # next row 2: the same adapter as an unmerged bypass in the forward (x [4096,4096] of the qkv workload)
+    # the same adapter as an unmerged bypass in the forward (x [4096,4096] of the qkv workload)
     M3 = wl3["M"]
     x3 = sg.activations_bf16(0, M3, K3, wl3["x_outliers"], wl3["x_factor"], dev)
     Wq3p, sw3p = cr.convrot_quantize_weight(W3, b)
