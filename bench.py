@@ -322,13 +322,13 @@ def run_gpu(args):
     if rank == 0:
         rows = measure_rows(cr, synth, sg, torch, dev, flush, pk) if not args.no_rows else {}
         rows["a3_x_rotate_quant"] = _hbm_row(M * K * 2 + M * K * 2 + M * 4, statistics.median(k1x), pk,
-                                             "C4 x [20480,4096] bf16 -> fp16-held codes + fp32 scales")
+                                             "train20k x [20480,4096] bf16 -> fp16-held codes + fp32 scales")
         rows["a6_dy_rotate_quant"] = _hbm_row(M * N * 2 + M * N * 2 + M * 4, statistics.median(k1d), pk,
-                                              "C4 dY [20480,16384] bf16 -> fp16-held codes + fp32 scales")
+                                              "train20k dY [20480,16384] bf16 -> fp16-held codes + fp32 scales")
         rows["a4_widen_weight_codes"] = _hbm_row(3 * N * K, statistics.median(wf + wb), pk,
-                                                 "C4 int8 codes [16384,4096] -> transient fp16 operand (fwd and bwd)")
-        rows["a4a5_fwd_gemm"] = _tc_row(2.0 * M * N * K, statistics.median(gf), pk, "C4 20480x16384x4096")
-        rows["a6_bwd_gemm"] = _tc_row(2.0 * M * N * K, statistics.median(gb), pk, "C4 20480x4096x16384")
+                                                 "train20k int8 codes [16384,4096] -> transient fp16 operand (fwd and bwd)")
+        rows["a4a5_fwd_gemm"] = _tc_row(2.0 * M * N * K, statistics.median(gf), pk, "train20k 20480x16384x4096")
+        rows["a6_bwd_gemm"] = _tc_row(2.0 * M * N * K, statistics.median(gb), pk, "train20k 20480x4096x16384")
         e2e = measure_e2e(cr, torch, dev, x, dY, Wq, sw, WtQ, swt, b, ops_step, steps=max(4, args.steps))
         cpu = None
         if world == 1 and not args.no_cpu:
@@ -423,32 +423,32 @@ def _time(torch, fn, flush, reps, pre=None):
 def measure_rows(cr, synth, sg, torch, dev, flush, pk):
     rows = {}
     reps = 10
-    # a2: weight rotate + quantize, C4 weight
+    # a2: weight rotate + quantize, the 20k-token workload's weight
     wl = synth.WORKLOADS["train20k"]
     N, K, b = wl["N"], wl["K"], wl["block"]
     W = sg.normal_bf16(0, synth.STREAM_W, N, K, wl["w_sigma"], dev)
     Wq = torch.empty((N, K), dtype=torch.int8, device=dev)
     sw = torch.empty((N,), dtype=torch.float32, device=dev)
     ms = _time(torch, lambda i: cr.convrot_quantize_weight(W, b, Wq=Wq, scale_w=sw), flush, reps)
-    rows["a2_weight_rotate_quant"] = _hbm_row(N * K * 2 + N * K + N * 4, ms, pk, "C4 W [16384,4096] bf16 -> int8")
+    rows["a2_weight_rotate_quant"] = _hbm_row(N * K * 2 + N * K + N * 4, ms, pk, "train20k W [16384,4096] bf16 -> int8")
     # a6 prep (one-off): int8 backward weight
     WtQ = torch.empty((K, N), dtype=torch.int8, device=dev)
     swt = torch.empty((K,), dtype=torch.float32, device=dev)
     ws = torch.empty(cr.convrot_bwd_weight_workspace_bytes(N, K), dtype=torch.uint8, device=dev)
     ms = _time(torch, lambda i: cr.convrot_prepare_bwd_weight(Wq, sw, b, WtQ, swt, ws), flush, 3)
     rows["a6_prep_bwd_weight"] = _hbm_row(N * K + N * 4 + K * N + K * 4, ms, pk,
-                                          "C4 Wq [16384,4096] -> WtQ [4096,16384] (one-off, via a double-float workspace)")
+                                          "train20k Wq [16384,4096] -> WtQ [4096,16384] (one-off, via a double-float workspace)")
     del ws
     # the bf16 backward mode (transient dequantization + bf16 tcgen05 GEMM), on the 20k-token shapes
     M = wl["M"]
     weff_t = torch.empty((K, N), dtype=torch.bfloat16, device=dev)
     ms = _time(torch, lambda i: cr.convrot_dequant_weight_t(Wq, sw, b, weff_t), flush, reps)
     rows["n1_bf16_bwd_dequant"] = _hbm_row(N * K + N * 4 + K * N * 2, ms, pk,
-                                           "C4 Wq [16384,4096] -> W_eff^T bf16 [4096,16384] (per backward)")
+                                           "train20k Wq [16384,4096] -> W_eff^T bf16 [4096,16384] (per backward)")
     dY = sg.normal_bf16(0, synth.STREAM_DY, M, N, wl["dy_sigma"], dev)
     dX = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
     ms = _time(torch, lambda i: cr.convrot_gemm_bf16(dY, weff_t, dX), flush, 5)
-    rows["n1_bf16_bwd_gemm"] = _tc_row(2.0 * M * N * K, ms, pk, "C4 dY [20480,16384] . W_eff -> dX bf16 [20480,4096]")
+    rows["n1_bf16_bwd_gemm"] = _tc_row(2.0 * M * N * K, ms, pk, "train20k dY [20480,16384] . W_eff -> dX bf16 [20480,4096]")
     rows["n1_bf16_bwd_gemm"].update({"traffic": gemm_traffic_per_launch("bf16_bwd"),
                                      "algorithmic_bytes": M * N * 2 + K * N * 2 + M * K * 2})
     # the second reading of the int8 backward (no prepared weight copy), and the accuracy of the
@@ -457,7 +457,7 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
     dX3 = torch.empty((M, K), dtype=torch.bfloat16, device=dev)
     ms = _time(torch, lambda i: cr.convrot_linear_bwd_x_r2(dY, Wq, sw, b, dX3, ws3), flush, 5)
     rows["n3_int8_bwd_second_reading"] = _tc_row(2.0 * M * N * K, ms, pk,
-                                                 "C4 dY [20480,16384] -> dX [20480,4096], scale-folded unrotated "
+                                                 "train20k dY [20480,16384] -> dX [20480,4096], scale-folded unrotated "
                                                  "codes, Wq as stored, rotation of the product (whole call)")
     dX1 = cr.convrot_linear_bwd_x(dY, WtQ, swt, b)
     cr.convrot_gemm_bf16(dY, cr.convrot_dequant_weight_t(Wq, sw, b), dX)
@@ -467,7 +467,7 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
     rows["n3_int8_bwd_second_reading"].update({"rel_fro_vs_bf16_mode": rel(dX3),
                                                "first_reading_rel_fro_vs_bf16_mode": rel(dX1)})
     del W, Wq, weff_t, dY, dX, dX1, dX3, ws3, WtQ
-    # a1 + a2: LoRA merge fused into the weight quantizer, C3 qkv weight
+    # a1 + a2: LoRA merge fused into the weight quantizer, the qkv weight
     wl3 = synth.WORKLOADS["qkv_lora"]
     N3, K3, r = wl3["N"], wl3["K"], wl3["lora_rank"]
     W3 = sg.normal_bf16(0, synth.STREAM_W, N3, K3, wl3["w_sigma"], dev)
@@ -477,7 +477,7 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
     ms = _time(torch, lambda i: cr.convrot_quantize_weight(W3, b, A, B, wl3["lora_alpha"], wl3["lora_scale"], Wq3,
                                                            sw3), flush, reps)
     rows["a1a2_lora_merge_quant"] = _hbm_row(N3 * K3 * 2 + N3 * K3 + N3 * 4 + r * K3 * 4 + N3 * r * 4, ms, pk,
-                                             "C3 W [12288,4096] + LoRA r16 -> int8")
+                                             "qkv W [12288,4096] + LoRA r16 -> int8")
     # the merge is r + 1 fp32 fused multiply-adds per element in a fixed order: its ALU roofline
     fma = N3 * K3 * (r + 1)
     fma_peak = fp32_fma_peak(torch, dev)
@@ -495,7 +495,7 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
                                                              wl3["lora_scale"], y=y3, workspace=wsl), flush, reps)
     ms_p = _time(torch, lambda i: cr.convrot_linear_fwd(x3, Wq3p, sw3p, b, y=y3, workspace=wsp), flush, reps)
     rows["n2_lora_bypass_fwd"] = _tc_row(2.0 * M3 * N3 * K3, ms_l, pk,
-                                         "C3 x [4096,4096] . W [12288,4096] + LoRA r16 bypass, whole forward call")
+                                         "qkv x [4096,4096] . W [12288,4096] + LoRA r16 bypass, whole forward call")
     rows["n2_lora_bypass_fwd"].update({"plain_fwd_ms": round(ms_p, 4),
                                        "bypass_overhead_frac": round(ms_l / ms_p - 1.0, 4)})
     del W3, Wq3, A, B, x3, Wq3p, sw3p, y3, wsl, wsp
@@ -514,7 +514,7 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
 
     ms = _time(torch, quant_table, flush, 5)
     rows["a7_table_rotate_quant"] = _hbm_row(V * D * 2 + V * D + V * 4, ms, pk,
-                                             "C5 table [248000,4096] bf16 -> int8, 8 row slabs")
+                                             "embed table [248000,4096] bf16 -> int8, 8 row slabs")
     del T
     # a8: lookup of 8192 ids, rotating over 8 id sets
     n_ids = wl5["n_ids"]
@@ -522,7 +522,7 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
     out = torch.empty((n_ids, D), dtype=torch.bfloat16, device=dev)
     ms = _time(torch, lambda i: cr.convrot_embedding_lookup(id_sets[i % len(id_sets)], Eq, se, b, out), flush, 16)
     rows["a8_embedding_lookup"] = _hbm_row(n_ids * 8 + n_ids * D + n_ids * 4 + n_ids * D * 2, ms, pk,
-                                           "C5 8192 ids -> bf16 [8192,4096]")
+                                           "embed 8192 ids -> bf16 [8192,4096]")
     assert cr.convrot_get_error() == cr.OK
     del Eq, se, out, id_sets
     add_same_size_copy(torch, dev, flush, rows)
