@@ -13,7 +13,8 @@ import pytest
 
 import oracle
 import synth
-from helpers import REL_FRO_BF16, REL_FRO_ORACLE, bits_of, check_codes, check_scales, codes_of, f64, rel_fro
+from helpers import (REL_FRO_BF16, REL_FRO_ORACLE, bits_of, check_codes, check_dequant_elementwise, check_scales,
+                     codes_of, f64, rel_fro)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -70,10 +71,19 @@ def _check_fwd(wl, x_gpu, W_gpu, Wq, sw, y, rng):
     wq_ref, sw_ref = oracle.quantize_rows_bf16(w_rows, b)
     check_codes(codes_of(Wq[torch.from_numpy(ns).cuda()]), wq_ref, f64(w_rows), b, "weight codes")
     check_scales(sw.cpu().numpy()[ns], sw_ref, "weight scales")
-    y_ref, _, _ = oracle.linear_fwd(x_rows, wq_ref, sw_ref, b)
+    y_ref, xq_ref, _ = oracle.linear_fwd(x_rows, wq_ref, sw_ref, b)
     y_s = bits_of(y[torch.from_numpy(ms).cuda()][:, torch.from_numpy(ns).cuda()])
     assert rel_fro(f64(y_s), f64(y_ref)) <= REL_FRO_ORACLE
     assert rel_fro(f64(y_s), f64(x_rows) @ f64(w_rows).T) <= REL_FRO_BF16
+    # element by element on the sampled outputs whose activation and weight code rows agree
+    # with the oracle's (the forward's own quantizer kernel gives the GPU's activation codes)
+    xq, _ = cr.convrot_quantize_activation(x_gpu, b)
+    rows_ok = np.all(codes_of(xq[torch.from_numpy(ms).cuda()]) == xq_ref, axis=1)
+    cols_ok = np.all(codes_of(Wq[torch.from_numpy(ns).cuda()]) == wq_ref, axis=1)
+    mask = rows_ok[:, None] & cols_ok[None, :]
+    assert mask.mean() > 0.9
+    check_dequant_elementwise(y_s, y_ref, mask=mask, what="full-size forward (sampled)")
+    del xq
 
 
 def test_img1024_forward_full_size():

@@ -8,8 +8,8 @@ import pytest
 
 import oracle
 import synth
-from helpers import (REL_FRO_BF16, REL_FRO_ORACLE, bits_of, check_codes, check_scales, codes_of, f64, rel_fro,
-                     torch_bf16)
+from helpers import (REL_FRO_BF16, REL_FRO_ORACLE, bits_of, check_codes, check_dequant_elementwise, check_scales,
+                     codes_of, f64, rel_fro, torch_bf16)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -36,6 +36,16 @@ def _f32(a):
 
 def _rand_codes(rng, shape):
     return rng.integers(-127, 128, size=shape, dtype=np.int8)
+
+
+def _agreeing_codes(x_t, xq_ref, Wq_t, wq_ref, b):
+    """Masks [M, N] of the outputs whose activation row (first mask), and also whose
+    weight row (second mask), have the same codes on the GPU (the forward's own
+    quantizer kernel) as in the oracle."""
+    xq, _ = cr.convrot_quantize_activation(x_t, b)
+    rows = np.all(codes_of(xq) == xq_ref, axis=1)
+    cols = np.all(codes_of(Wq_t) == wq_ref, axis=1)
+    return rows[:, None] & np.ones(len(cols), dtype=bool)[None, :], rows[:, None] & cols[None, :]
 
 
 # ------------------------------------------------------------------ GEMM (int32)
@@ -320,10 +330,15 @@ def test_randomized_small_shapes(case):
     y = cr.convrot_linear_fwd(torch_bf16(x), Wq, sw, b)
     small = torch.empty(cr.convrot_act_workspace_bytes(M, K), dtype=torch.uint8, device="cuda")
     assert torch.equal(y, cr.convrot_linear_fwd(torch_bf16(x), Wq, sw, b, workspace=small))
-    y_ref, _, _ = oracle.linear_fwd(x, wq_ref, sw_ref, b)
+    y_ref, xq_ref, _ = oracle.linear_fwd(x, wq_ref, sw_ref, b)
     assert rel_fro(f64(bits_of(y)), f64(y_ref)) <= REL_FRO_ORACLE
     y_o = cr.convrot_linear_fwd(torch_bf16(x), _i8(wq_ref), _f32(sw_ref), b)
     assert rel_fro(f64(bits_of(y_o)), f64(y_ref)) <= REL_FRO_ORACLE
+    # element by element wherever the code rows agree (all but near-tie rows)
+    xrows, mask = _agreeing_codes(torch_bf16(x), xq_ref, Wq, wq_ref, b)
+    assert mask.mean() > 0.9
+    check_dequant_elementwise(bits_of(y), y_ref, mask=mask, what="forward on the GPU's codes")
+    check_dequant_elementwise(bits_of(y_o), y_ref, mask=xrows, what="forward on the oracle's weight codes")
     assert cr.convrot_get_error() == cr.OK
 
 
@@ -340,6 +355,11 @@ def test_linear_fwd_tiny_workload():
     yb = f64(bits_of(y))
     assert rel_fro(yb, f64(y_ref)) <= REL_FRO_ORACLE
     assert rel_fro(yb, f64(x) @ f64(W).T) <= REL_FRO_BF16
+    xrows, mask = _agreeing_codes(torch_bf16(x), xq_ref, Wq, wq_ref, b)
+    assert mask.mean() > 0.9
+    check_dequant_elementwise(bits_of(y), y_ref, mask=mask, what="tiny forward")
+    y_o = cr.convrot_linear_fwd(torch_bf16(x), _i8(wq_ref), _f32(sw_ref), b)
+    check_dequant_elementwise(bits_of(y_o), y_ref, mask=xrows, what="tiny forward on the oracle's weight codes")
     assert cr.convrot_get_error() == cr.OK
 
 
@@ -355,6 +375,10 @@ def test_linear_fwd_ragged_multi_tile():
     yb = f64(bits_of(y))
     assert rel_fro(yb, f64(y_ref)) <= REL_FRO_ORACLE
     assert rel_fro(yb, f64(x) @ f64(W).T + f64(bias)) <= REL_FRO_BF16
+    _, xq_ref, _ = oracle.linear_fwd(x, wq_ref, sw_ref, b, bias)
+    _, mask = _agreeing_codes(torch_bf16(x), xq_ref, Wq, wq_ref, b)
+    assert mask.mean() > 0.9
+    check_dequant_elementwise(bits_of(y), y_ref, bias_bits=bias, mask=mask, what="ragged forward with bias")
 
 
 # ------------------------------------------------------------------ backward

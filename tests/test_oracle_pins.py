@@ -176,6 +176,31 @@ def test_quantizer_brute_force_fp64_definition(b):
     assert diff.sum() == 0 or np.all(_near_tie(ratio[diff]))
 
 
+@pytest.mark.parametrize("b", [8, 16, 32, 64, 128, 256])
+def test_quantizer_exact_ties_round_half_to_even_in_bulk(b):
+    """Rows built as x = H_b w per block (integer w, one block +-254 e_i per row) rotate
+    exactly to u = b w, so the codes are rne(127 w / 254) = rne(w / 2): every odd w is an
+    exact tie and must go to the even neighbour (1.5 -> 2, 2.5 -> 2, -0.5 -> 0), and the
+    scale is 254 sqrt(b) / 127 = 2 sqrt(b).  A quantizer that rounded ties away from zero
+    or truncated would fail on hundreds of elements here."""
+    from helpers import tie_rows
+    x, want, nties = tie_rows(b, 12, 2048, b)
+    assert nties > 100
+    q, s = oracle.quantize_rows_bf16(x, b)
+    np.testing.assert_array_equal(q, want)
+    np.testing.assert_array_equal(s, np.float32(2.0 * math.sqrt(b)))
+
+
+@pytest.mark.parametrize("b", [16, 64, 256])
+def test_bwd_weight_exact_ties_round_half_to_even(b):
+    """The backward weight of a constructed base (one +-1 code per block of K, row scales
+    (H_b w) 2^-16 along N) transforms along N to exact ties; its codes are tau_k rne(w / 2)."""
+    from helpers import tie_bwd_weight
+    Wq, s, want = tie_bwd_weight(b, 2 * b, 2 * b, b)
+    q, _ = oracle.prepare_bwd_weight(Wq, s, b)
+    np.testing.assert_array_equal(q, want)
+
+
 def test_quantizer_zero_row_and_ldx():
     x = np.zeros((3, 64), dtype=np.uint16)
     x[1] = _bf16(synth.normal(1, 0, 0, 64))
