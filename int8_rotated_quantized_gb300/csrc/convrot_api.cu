@@ -397,6 +397,25 @@ int convrot_gemm_s32(const int8_t *A, const int8_t *B, int64_t M, int64_t N, int
     return cuda_status(convrot::launch_gemm(a16, nullptr, B, nullptr, nullptr, M, N, K, C, true, err, st));
 }
 
+int convrot_selftest_gemm_fault(int widened, const uint16_t *xq, const float *scale_x, int64_t M, int64_t K,
+                                const void *Wq, const float *scale_w, int64_t N, uint16_t *y, uint64_t limit_ns,
+                                int64_t skip_iteration, int producer, convrot_stream_t stream) {
+    CHECK(limit_ns > 0 && limit_ns <= 10000000000ull && (producer == 0 || producer == 1));
+    CHECK(skip_iteration >= 0 && skip_iteration <= INT32_MAX && (widened == 0 || widened == 1));
+    CHECK(M >= 0 && N >= 0 && K > 0 && K % 16 == 0 && K <= (1 << 20) && N % 16 == 0);
+    CHECK(M <= INT32_MAX && N <= INT32_MAX);
+    CHECK(M == 0 || N == 0 ||
+          (xq && scale_x && Wq && scale_w && y && aligned16(xq) && aligned16(Wq) && aligned16(y) &&
+           aligned16(scale_x) && aligned16(scale_w)));
+    unsigned *err = nullptr;
+    int rc = device_setup(&err);
+    if (rc != CONVROT_OK) return rc;
+    if (M == 0 || N == 0) return CONVROT_OK;
+    return cuda_status(convrot::launch_gemm_fault_selftest(widened != 0, xq, scale_x, Wq, scale_w, M, N, K, y, err,
+                                                           limit_ns, (int)skip_iteration, producer,
+                                                           (cudaStream_t)stream));
+}
+
 int convrot_selftest_wait_timeout(uint64_t limit_ns, convrot_stream_t stream) {
     CHECK(limit_ns > 0 && limit_ns <= 10000000000ull);
     unsigned *err = nullptr;

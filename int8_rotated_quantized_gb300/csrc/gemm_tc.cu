@@ -135,6 +135,13 @@ struct GemmArgs {
     const float *lora_b;   // [N, lora_rank] (bypass mode)
     int lora_rank;
     int64_t lora_ld;       // row stride of lora_xa: M rounded up to 256
+    uint64_t wait_limit_ns = kWaitLimitNs;  // bound of every pipeline wait
+    // Failure-path self-test only: the producer named by fault_role (0 the
+    // activation producer, 1 the weight producer) issues no copy at its
+    // iteration fault_skip_it, so the stage it feeds never fills and the
+    // consumer's bounded wait must end the kernel.  -1 outside the self-test.
+    int fault_skip_it = -1;
+    int fault_role = -1;
 };
 
 // ------------------------------------------------------------- PTX wrappers --
@@ -234,9 +241,8 @@ __device__ __forceinline__ void tile_coords(int tile, int num_t, int num_w, int 
 // rest parked in __syncwarp measured 2x slower); the result is made
 // warp-uniform so no lane runs ahead on an abort.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *err,
-                                          int lane) {
-    (void)lane;
-    const bool got = mbar_wait(bar, parity, abort_flag, err);
+                                          uint64_t limit_ns) {
+    const bool got = mbar_wait(bar, parity, abort_flag, err, limit_ns);
     return __all_sync(0xffffffffu, got);
 }
 
@@ -316,16 +322,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int empty0 = is_x ? L::BAR_X_EMPTY : w_direct ? L::BAR_CONV_EMPTY : L::BAR_W_EMPTY;
             const CUtensorMap *map = is_x ? &tmX : &tmW;
             asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
-            int it = 0;
+            int it = 0, skipped = -1;
             bool ok = true;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
                 int tb, wb;
                 tile_coords(tile, num_t, num_w, p.group, p.group_weight != 0, tb, wb);
                 for (int kb = 0; kb < num_kb; ++kb, ++it) {
                     const int s = it % nst;
-                    if (!mbar_wait(bar(empty0 + s), ((it / nst) & 1) ^ 1, abort_flag, p.err)) {
+                    if (!mbar_wait(bar(empty0 + s), ((it / nst) & 1) ^ 1, abort_flag, p.err, p.wait_limit_ns)) {
                         ok = false;
                         break;
+                    }
+                    if (it == p.fault_skip_it && p.fault_role == (is_x ? 0 : 1)) {
+                        skipped = it;  // self-test: this stage is never filled
+                        continue;
                     }
                     if (is_x) {
                         mbar_expect_tx(bar(full0 + s), X_STAGE);
@@ -339,9 +349,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
-            if (!ok) {  // let the copies already issued land before the CTA exits
+            if (!ok || skipped >= 0) {  // let the copies already issued land before the CTA exits
                 for (int j = it - 1; j >= 0 && j >= it - nst; --j)
-                    mbar_wait_drain(bar(full0 + j % nst), (j / nst) & 1);
+                    if (j != skipped) mbar_wait_drain(bar(full0 + j % nst), (j / nst) & 1, p.wait_limit_ns);
             }
         } else if (warp == 1 && lane == 0) {
             // --------------------------------------------------------- MMA
@@ -353,7 +363,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const int kc = kb % chunk_kb;
                     if (kc == 0) {
                         const int buf = g & 1;
-                        if (!mbar_wait(bar(L::BAR_ACC_EMPTY + buf), ((g >> 1) & 1) ^ 1, abort_flag, p.err)) {
+                        if (!mbar_wait(bar(L::BAR_ACC_EMPTY + buf), ((g >> 1) & 1) ^ 1, abort_flag, p.err,
+                                       p.wait_limit_ns)) {
                             ok = false;
                             break;
                         }
@@ -362,8 +373,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     const int s = it % L::XS;
                     const int c = it % L::CS;
-                    if (!mbar_wait(bar(L::BAR_X_FULL + s), (it / L::XS) & 1, abort_flag, p.err) ||
-                        !mbar_wait(bar(L::BAR_CONV_FULL + c), (it / L::CS) & 1, abort_flag, p.err)) {
+                    if (!mbar_wait(bar(L::BAR_X_FULL + s), (it / L::XS) & 1, abort_flag, p.err, p.wait_limit_ns) ||
+                        !mbar_wait(bar(L::BAR_CONV_FULL + c), (it / L::CS) & 1, abort_flag, p.err, p.wait_limit_ns)) {
                         ok = false;
                         break;
                     }
@@ -385,7 +396,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             // All MMAs issued by this thread have completed once this fires.
             umma_commit(bar(L::BAR_DRAIN));
-            mbar_wait_drain(bar(L::BAR_DRAIN), 0);
+            mbar_wait_drain(bar(L::BAR_DRAIN), 0, p.wait_limit_ns);
         }
         __syncwarp();
         end_barrier();
@@ -404,8 +415,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int kb = 0; kb < num_kb; ++kb, ++it) {
                 const int s = it % L::WS;
                 const int c = it % L::CS;
-                if (!warp_wait(bar(L::BAR_W_FULL + s), (it / L::WS) & 1, abort_flag, p.err, lane) ||
-                    !warp_wait(bar(L::BAR_CONV_EMPTY + c), ((it / L::CS) & 1) ^ 1, abort_flag, p.err, lane)) {
+                if (!warp_wait(bar(L::BAR_W_FULL + s), (it / L::WS) & 1, abort_flag, p.err, p.wait_limit_ns) ||
+                    !warp_wait(bar(L::BAR_CONV_EMPTY + c), ((it / L::CS) & 1) ^ 1, abort_flag, p.err, p.wait_limit_ns)) {
                     ok = false;
                     break;
                 }
@@ -458,7 +469,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // stage this half-tile's bypass rows (rank x 128 tokens) in shared memory
                 // while the chunks accumulate, once the four warps of this half have read
                 // the previous tile's rows (bounded waits, like every pipeline wait)
-                if (u > 0 && !warp_wait(bar(L::BAR_XS_FREE + h), (u - 1) & 1, abort_flag, p.err, lane)) {
+                if (u > 0 && !warp_wait(bar(L::BAR_XS_FREE + h), (u - 1) & 1, abort_flag, p.err, p.wait_limit_ns)) {
                     ok = false;
                     break;
                 }
@@ -480,7 +491,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
             for (int ch = 0; ch < nchunks; ++ch, ++g) {
                 const int buf = g & 1;
-                if (!warp_wait(bar(L::BAR_ACC_FULL + buf), (g >> 1) & 1, abort_flag, p.err, lane)) {
+                if (!warp_wait(bar(L::BAR_ACC_FULL + buf), (g >> 1) & 1, abort_flag, p.err, p.wait_limit_ns)) {
                     ok = false;
                     break;
                 }
@@ -511,7 +522,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int mlim = p.M - m0;  // tokens of this column half that exist
             const bool full = mlim >= 128;
             if constexpr (MODE == kModeDequantW16Lora) {  // every thread of the half takes part
-                if (!warp_wait(bar(L::BAR_XS_READY + h), u & 1, abort_flag, p.err, lane)) {
+                if (!warp_wait(bar(L::BAR_XS_READY + h), u & 1, abort_flag, p.err, p.wait_limit_ns)) {
                     ok = false;
                     break;
                 }
@@ -760,6 +771,31 @@ cudaError_t launch_gemm_w16_scale_f32(const uint16_t *A, const float *sa, const 
     choose_raster(num_t, num_w, K, 2, group, group_weight);
     GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, sa, nullptr, nullptr, out, err};
     return launch_mode<kModeScaleF32>(tmX, tmW, p, num_t * num_w, st);
+}
+
+cudaError_t launch_gemm_fault_selftest(bool widened, const uint16_t *A, const float *sa, const void *B,
+                                      const float *sb, int64_t M, int64_t N, int64_t K, uint16_t *out, unsigned *err,
+                                      uint64_t limit_ns, int skip_it, int role, cudaStream_t st) {
+    if (M == 0 || N == 0) return cudaSuccess;
+    cudaError_t e = get_encoder();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tmX, tmW;
+    const bool okw = widened ? encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B, (uint64_t)K, (uint64_t)N, BK, TW,
+                                         CU_TENSOR_MAP_SWIZZLE_128B)
+                             : encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, B, (uint64_t)K, (uint64_t)N, BK, TW,
+                                         CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!okw || !encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, (uint64_t)K, (uint64_t)M, BK, TT,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    const int64_t num_t = (M + TT - 1) / TT, num_w = (N + TW - 1) / TW;
+    int group, group_weight;
+    choose_raster(num_t, num_w, K, widened ? 2 : 1, group, group_weight);
+    GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, sa, sb, nullptr, out, err};
+    p.wait_limit_ns = limit_ns;
+    p.fault_skip_it = skip_it;
+    p.fault_role = role;
+    return widened ? launch_mode<kModeDequantW16>(tmX, tmW, p, num_t * num_w, st)
+                   : launch_mode<kModeDequant>(tmX, tmW, p, num_t * num_w, st);
 }
 
 cudaError_t launch_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t M, int64_t N, int64_t K, uint16_t *out,

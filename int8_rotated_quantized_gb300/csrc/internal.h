@@ -83,6 +83,14 @@ cudaError_t launch_rot_rows_f32(const float *P, int64_t rows, int64_t L, int blo
 cudaError_t launch_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t M, int64_t N, int64_t K, uint16_t *out,
                              unsigned *err, cudaStream_t st);
 
+// Failure-path self-test of the GEMM itself: the dequantization GEMM (int8
+// weight codes widened in the loop, or already widened to fp16 values) with
+// every pipeline wait bounded by limit_ns, and the copy of producer `role` at
+// its iteration `skip_it` never issued (gemm_tc.cu).
+cudaError_t launch_gemm_fault_selftest(bool widened, const uint16_t *A, const float *sa, const void *B,
+                                      const float *sb, int64_t M, int64_t N, int64_t K, uint16_t *out, unsigned *err,
+                                      uint64_t limit_ns, int skip_it, int role, cudaStream_t st);
+
 // Self-test of the bounded-wait failure path (selftest.cu).
 cudaError_t launch_wait_timeout(uint64_t limit_ns, unsigned *err, cudaStream_t st);
 

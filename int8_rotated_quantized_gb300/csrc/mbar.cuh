@@ -51,10 +51,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // Bounded wait that ignores the abort flag: used while draining in-flight work.
-__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) return;
+        if (global_timer_ns() - t0 > limit_ns) return;
     }
 }
 
