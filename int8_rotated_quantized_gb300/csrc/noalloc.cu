@@ -22,9 +22,10 @@
 
 namespace {
 
-// 64 MiB: M * K * 2 bytes of codes plus M * 4 bytes of scales (each region
-// 256-byte aligned) must fit, e.g. M = 8192 tokens at K = 4096.
-constexpr size_t kScratchBytes = size_t(64) << 20;
+// 64 MiB + 256 KiB: M * K * 2 bytes of codes plus M * 4 bytes of scales (each
+// region rounded up to 256 bytes) must fit.  M = 8192 tokens at K = 4096 take
+// 64 MiB of codes and 32 KiB of scales; the largest M at K = 4096 is 8219.
+constexpr size_t kScratchBytes = (size_t(64) << 20) + (size_t(256) << 10);
 
 static __device__ __align__(256) unsigned char g_fwd_scratch[kScratchBytes];
 
@@ -36,14 +37,20 @@ size_t round256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 // Device address of the scratch array on the current device.  In host code
 // the name g_fwd_scratch is only a host-side stand-in, so the address is
-// looked up once per device with that device current and cached.
+// looked up once per device with that device current and cached.  The cache
+// is keyed by the device index alone: the library must not be used across a
+// cudaDeviceReset (or any other replacement of the device's primary context),
+// after which the cached address would no longer belong to the context.
 int scratch_of_current_device(unsigned char **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CONVROT_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
     if (g_scratch_ptr[dev] == nullptr) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_fwd_scratch) != cudaSuccess || p == nullptr) return CONVROT_ERR_CUDA;
+        if (cudaGetSymbolAddress(&p, g_fwd_scratch) != cudaSuccess || p == nullptr) {
+            (void)cudaGetLastError();  // leave no error behind for the caller's next check
+            return CONVROT_ERR_CUDA;
+        }
         g_scratch_ptr[dev] = p;
     }
     *out = static_cast<unsigned char *>(g_scratch_ptr[dev]);

@@ -62,13 +62,29 @@ def test_noalloc_matches_regular_forward_on_two_calls():
         assert torch.equal(y, ref)  # same kernels, same inputs: identical results
 
 
-def test_noalloc_refuses_problems_beyond_its_array():
+def _need(M, K):
+    r = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    return r(M * K * 2) + r(M * 4)
+
+
+def test_noalloc_accepts_the_largest_problem_and_refuses_the_next():
+    """The limit follows from convrot_linear_fwd_noalloc_max_bytes(): the largest M that
+    fits at K = 4096 runs (and equals the regular forward), one row more is refused."""
     limit = cr.convrot_linear_fwd_noalloc_max_bytes()
-    K = 4096
-    M = limit // (2 * K) + 1
-    x = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
-    Wq = torch.zeros((16, K), dtype=torch.int8, device="cuda")
-    sw = torch.zeros((16,), dtype=torch.float32, device="cuda")
-    y = torch.empty((M, 16), dtype=torch.bfloat16, device="cuda")
-    assert _call_noalloc(x, Wq, sw, 128, y) == cr.ERR_UNSUPPORTED
+    K, N, b = 4096, 16, 128
+    M = limit // (2 * K)
+    while _need(M + 1, K) <= limit:
+        M += 1
+    while _need(M, K) > limit:
+        M -= 1
+    assert M >= 8192  # 8192 tokens at K = 4096 fit, scales included
+    x = torch_bf16(synth.activations_bf16(24, M + 1, K, 10, 30.0))
+    W = synth.normal_bf16(24, synth.STREAM_W, N, K, 0.02)
+    Wq, sw = cr.convrot_quantize_weight(torch_bf16(W), b)
+    y = torch.empty((M + 1, N), dtype=torch.bfloat16, device="cuda")
+    assert _call_noalloc(x[:M], Wq, sw, b, y[:M]) == cr.OK
+    torch.cuda.synchronize()
+    assert cr.convrot_get_error() == cr.OK
+    assert torch.equal(y[:M], cr.convrot_linear_fwd(x[:M], Wq, sw, b))
+    assert _call_noalloc(x, Wq, sw, b, y) == cr.ERR_UNSUPPORTED
     assert cr.convrot_get_error() == cr.OK
