@@ -320,15 +320,24 @@ def run_gpu(args):
 
     result = None
     if rank == 0:
-        rows = measure_rows(cr, synth, sg, torch, dev, flush, pk) if not args.no_rows else {}
-        rows["a3_x_rotate_quant"] = _hbm_row(M * K * 2 + M * K * 2 + M * 4, statistics.median(k1x), pk,
-                                             "train20k x [20480,4096] bf16 -> fp16-held codes + fp32 scales")
-        rows["a6_dy_rotate_quant"] = _hbm_row(M * N * 2 + M * N * 2 + M * 4, statistics.median(k1d), pk,
-                                              "train20k dY [20480,16384] bf16 -> fp16-held codes + fp32 scales")
-        rows["a4_widen_weight_codes"] = _hbm_row(3 * N * K, statistics.median(wf + wb), pk,
-                                                 "train20k int8 codes [16384,4096] -> transient fp16 operand (fwd and bwd)")
-        rows["a4a5_fwd_gemm"] = _tc_row(2.0 * M * N * K, statistics.median(gf), pk, "train20k 20480x16384x4096")
-        rows["a6_bwd_gemm"] = _tc_row(2.0 * M * N * K, statistics.median(gb), pk, "train20k 20480x4096x16384")
+        int8_peak = measure_int8_mma_peak(cr, torch, dev)
+        rows = measure_rows(cr, synth, sg, torch, dev, flush, pk, int8_peak) if not args.no_rows else {}
+        # the method's own output is 1-byte codes (+ fp32 scales): those are the algorithmic bytes;
+        # the fp16 container the GEMM reads is reported beside them
+        rows["a3_x_rotate_quant"] = _hbm_row(M * K * 2 + M * K + M * 4, statistics.median(k1x), pk,
+                                             "train20k x [20480,4096] bf16 -> codes (held as fp16) + fp32 scales",
+                                             container_bytes=M * K * 2 + M * K * 2 + M * 4)
+        rows["a6_dy_rotate_quant"] = _hbm_row(M * N * 2 + M * N + M * 4, statistics.median(k1d), pk,
+                                              "train20k dY [20480,16384] bf16 -> codes (held as fp16) + fp32 scales",
+                                              container_bytes=M * N * 2 + M * N * 2 + M * 4)
+        rows["overhead_widen_weight_codes"] = _overhead_row(
+            3 * N * K, statistics.median(wf + wb), 2, statistics.median(step_ms),
+            "train20k: int8 weight codes [16384,4096] -> transient fp16 operand, once before each GEMM (forward "
+            "and grad_x); work the method does not have, the price of the fp16 tensor-core route")
+        rows["a4a5_fwd_gemm"] = _tc_row(2.0 * M * N * K, statistics.median(gf), pk, "train20k 20480x16384x4096",
+                                        int8_peak)
+        rows["a6_bwd_gemm"] = _tc_row(2.0 * M * N * K, statistics.median(gb), pk, "train20k 20480x4096x16384",
+                                      int8_peak)
         e2e = measure_e2e(cr, torch, dev, x, dY, Wq, sw, WtQ, swt, b, ops_step, steps=max(4, args.steps))
         cpu = None
         if world == 1 and not args.no_cpu:
@@ -358,6 +367,11 @@ def run_gpu(args):
                 "frac": round(gemm_tflops / pk["bf16"], 4),
                 "peak_note": f"{pk['source']} dense bf16 burst (the kind::f16 MMA that carries the int8 codes runs at the "
                              "bf16/fp16 rate; tcgen05 kind::i8 does not exist on sm_103a)",
+                "int8_peak": int8_peak["TOPS"],
+                "frac_of_int8_peak": round(gemm_tflops / int8_peak["TOPS"], 3),
+                "int8_peak_note": "measured in this run: dense int8 through the only int8 MMA of sm_103a, the legacy "
+                                  "warp-level mma.sync m16n8k32 s8 (convrot_probe_mma_s8_rate, "
+                                  f"{int8_peak['ms']} ms for {int8_peak['ops']:.3e} ops, 4 CTAs x 8 warps per SM)",
                 "traffic": gemm_traffic_per_launch(),
                 "traffic_note": "mean DRAM bytes per launch over the forward and grad_x shapes (ncu, one pass); "
                                 "algorithmic bytes per launch 973225984 for both (fp16 activation and weight "
@@ -389,16 +403,60 @@ def fp32_fma_peak(torch, dev):
     return props.multi_processor_count * 128 * mhz * 1e6
 
 
-def _hbm_row(nbytes, ms, pk, what):
+def _hbm_row(nbytes, ms, pk, what, container_bytes=None):
+    """An HBM-bound row: GB/s and frac on the algorithmic bytes (the compulsory reads and
+    writes of the method's own data: bf16 in, 1-byte codes, fp32 scales); where the kernel
+    writes a wider container (fp16-held codes), its bytes and rate are reported beside."""
     gbs = nbytes / (ms * 1e-3) / 1e9
-    return {"what": what, "ms": round(ms, 4), "algorithmic_bytes": int(nbytes), "GB/s": round(gbs, 1),
-            "peak_GB/s": pk["hbm"], "frac": round(gbs / pk["hbm"], 4)}
+    row = {"what": what, "ms": round(ms, 4), "algorithmic_bytes": int(nbytes), "GB/s": round(gbs, 1),
+           "peak_GB/s": pk["hbm"], "frac": round(gbs / pk["hbm"], 4)}
+    if container_bytes is not None:
+        cgbs = container_bytes / (ms * 1e-3) / 1e9
+        row.update({"container_bytes": int(container_bytes), "container_GB/s": round(cgbs, 1),
+                    "container_frac": round(cgbs / pk["hbm"], 4)})
+    return row
 
 
-def _tc_row(ops, ms, pk, what):
+def _overhead_row(nbytes, ms, launches, step_ms, what):
+    """Work the method does not have (no roofline achievement): its time and share of the step."""
+    return {"what": what, "overhead": True, "ms_per_launch": round(ms, 4), "launches_per_step": launches,
+            "ms_per_step": round(ms * launches, 4), "share_of_step": round(ms * launches / step_ms, 4),
+            "bytes_moved_per_launch": int(nbytes), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+
+
+def _tc_row(ops, ms, pk, what, int8_peak=None):
     tops = ops / (ms * 1e-3) / 1e12
-    return {"what": what, "ms": round(ms, 4), "ops": ops, "TOPS": round(tops, 1), "peak_TFLOP/s": pk["bf16"],
-            "frac": round(tops / pk["bf16"], 4)}
+    row = {"what": what, "ms": round(ms, 4), "ops": ops, "TOPS": round(tops, 1), "peak_TFLOP/s": pk["bf16"],
+           "frac": round(tops / pk["bf16"], 4)}
+    if int8_peak is not None:
+        row.update({"int8_peak_TOPS": int8_peak["TOPS"], "frac_of_int8_peak": round(tops / int8_peak["TOPS"], 3)})
+    return row
+
+
+def measure_int8_mma_peak(cr, torch, dev, reps=5):
+    """Dense int8 rate of the legacy warp-level MMA (the only int8 MMA on sm_103a), timed
+    with CUDA events around the library's probe kernel; the median of `reps` launches."""
+    sink = torch.empty(1 << 16, dtype=torch.int32, device=dev)
+    ops = ctypes.c_double()
+    stream = torch.cuda.current_stream()
+
+    def launch(iters):
+        rc = cr.lib().convrot_probe_mma_s8_rate(iters, cr._ptr(sink), sink.numel() * 4, ctypes.byref(ops),
+                                                cr._stream(None))
+        assert rc == cr.OK
+    launch(64)
+    torch.cuda.synchronize()
+    iters, ms = 4096, []
+    for _ in range(reps + 1):
+        a = torch.cuda.Event(enable_timing=True)
+        z = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        launch(iters)
+        z.record(stream)
+        torch.cuda.synchronize()
+        ms.append(a.elapsed_time(z))
+    t = statistics.median(ms[1:])
+    return {"TOPS": round(ops.value / (t * 1e-3) / 1e12, 1), "ms": round(t, 3), "ops": ops.value}
 
 
 def _time(torch, fn, flush, reps, pre=None):
@@ -420,9 +478,41 @@ def _time(torch, fn, flush, reps, pre=None):
     return statistics.median(out)
 
 
-def measure_rows(cr, synth, sg, torch, dev, flush, pk):
+def measure_rows(cr, synth, sg, torch, dev, flush, pk, int8_peak=None):
     rows = {}
     reps = 10
+    # the single 1024^2-image forward: x [4096,4096] (4096 image tokens), W [4096,4096]
+    wl2 = synth.WORKLOADS["img1024"]
+    M2, K2, N2, b2 = wl2["M"], wl2["K"], wl2["N"], wl2["block"]
+    x2 = sg.activations_bf16(0, M2, K2, wl2["x_outliers"], wl2["x_factor"], dev)
+    W2 = sg.normal_bf16(0, synth.STREAM_W, N2, K2, wl2["w_sigma"], dev)
+    xq2 = torch.empty((M2, K2), dtype=torch.float16, device=dev)
+    sx2 = torch.empty((M2,), dtype=torch.float32, device=dev)
+    Wq2 = torch.empty((N2, K2), dtype=torch.int8, device=dev)
+    sw2 = torch.empty((N2,), dtype=torch.float32, device=dev)
+    ms = _time(torch, lambda i: cr.convrot_quantize_activation(x2, b2, xq2, sx2), flush, reps)
+    rows["c2_a3_x_rotate_quant"] = _hbm_row(M2 * K2 * 3 + M2 * 4, ms, pk,
+                                            "img1024 x [4096,4096] bf16 -> codes (held as fp16) + fp32 scales",
+                                            container_bytes=M2 * K2 * 4 + M2 * 4)
+    ms = _time(torch, lambda i: cr.convrot_quantize_weight(W2, b2, Wq=Wq2, scale_w=sw2), flush, reps)
+    rows["c2_a2_weight_rotate_quant"] = _hbm_row(N2 * K2 * 3 + N2 * 4, ms, pk, "img1024 W [4096,4096] bf16 -> int8")
+    w16 = cr.convrot_widen_codes(Wq2)
+    y2 = torch.empty((M2, N2), dtype=torch.bfloat16, device=dev)
+    ms = _time(torch, lambda i: cr.convrot_gemm_dequant_w16(xq2, sx2, w16, sw2, None, y2), flush, reps)
+    tiles = -(-M2 // 256) * -(-N2 // 128)
+    rows["c2_a4a5_gemm"] = _tc_row(2.0 * M2 * N2 * K2, ms, pk,
+                                   f"img1024 4096x4096x4096 GEMM + dequant (widened-weight mode; {tiles} tiles of "
+                                   "256 tokens x 128 weight rows on the SMs)", int8_peak)
+    ws2 = torch.empty(cr.convrot_linear_workspace_bytes(M2, K2, N2), dtype=torch.uint8, device=dev)
+    ms = _time(torch, lambda i: cr.convrot_linear_fwd(x2, Wq2, sw2, b2, y=y2, workspace=ws2), flush, reps)
+    rows["c2_fwd_call"] = _tc_row(2.0 * M2 * N2 * K2, ms, pk,
+                                  "img1024 whole forward call (rotate+quantize x, widen W codes, GEMM + dequant)",
+                                  int8_peak)
+    ms = _time(torch, lambda i: cr.convrot_linear_fwd_noalloc(x2, Wq2, sw2, b2, y=y2), flush, reps)
+    rows["c2_fwd_noalloc_call"] = _tc_row(2.0 * M2 * N2 * K2, ms, pk,
+                                          "img1024 forward without a workspace (library-owned code array; the GEMM "
+                                          "widens the int8 weight codes in its loop)", int8_peak)
+    del x2, W2, xq2, sx2, Wq2, sw2, w16, y2, ws2
     # a2: weight rotate + quantize, the 20k-token workload's weight
     wl = synth.WORKLOADS["train20k"]
     N, K, b = wl["N"], wl["K"], wl["block"]
@@ -498,7 +588,15 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk):
                                          "qkv x [4096,4096] . W [12288,4096] + LoRA r16 bypass, whole forward call")
     rows["n2_lora_bypass_fwd"].update({"plain_fwd_ms": round(ms_p, 4),
                                        "bypass_overhead_frac": round(ms_l / ms_p - 1.0, 4)})
-    del W3, Wq3, A, B, x3, Wq3p, sw3p, y3, wsl, wsp
+    rows["c3_fwd_call"] = _tc_row(2.0 * M3 * N3 * K3, ms_p, pk,
+                                  "qkv x [4096,4096] . W [12288,4096] (LoRA merged at load), whole forward call "
+                                  "(rotate+quantize x, widen W codes, GEMM + dequant)", int8_peak)
+    xq3, sx3 = cr.convrot_quantize_activation(x3, b)
+    w16_3 = cr.convrot_widen_codes(Wq3)
+    ms = _time(torch, lambda i: cr.convrot_gemm_dequant_w16(xq3, sx3, w16_3, sw3, None, y3), flush, reps)
+    rows["c3_a4a5_gemm"] = _tc_row(2.0 * M3 * N3 * K3, ms, pk,
+                                   "qkv 4096x12288x4096 GEMM + dequant (widened-weight mode, merged weight)", int8_peak)
+    del W3, Wq3, A, B, x3, Wq3p, sw3p, y3, wsl, wsp, xq3, sx3, w16_3
     # a7: embedding table quantization (row-chunked: 8 slabs of 31000 rows)
     wl5 = synth.WORKLOADS["embed"]
     V, D = wl5["V"], wl5["D"]

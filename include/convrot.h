@@ -184,13 +184,19 @@ CONVROT_API int convrot_linear_fwd_lora(const uint16_t *x, int64_t M, int64_t K,
  * it computes exactly what convrot_linear_fwd computes, with the activation
  * codes and scales kept in one fixed device array inside the library instead
  * of a caller workspace.
- *   - The array is convrot_linear_fwd_noalloc_max_bytes() bytes (64 MiB) on
- *     every GPU that loads the library, held until the process exits.
- *     Problems needing more (M*K*2 + M*4 bytes, each part rounded up to 256)
- *     return CONVROT_ERR_UNSUPPORTED and enqueue nothing.
+ *   - The array is convrot_linear_fwd_noalloc_max_bytes() bytes (64 MiB +
+ *     256 KiB) on every GPU that loads the library, held until the process
+ *     exits.  Problems needing more (M*K*2 + M*4 bytes, each part rounded up
+ *     to 256; at K = 4096 at most M = 8219 rows) return
+ *     CONVROT_ERR_UNSUPPORTED and enqueue nothing.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     stream capture.  Do not use the library across a cudaDeviceReset: the
+ *     cached address belongs to the context that was reset.
+ *   - The GEMM of this entry point widens the int8 weight codes inside its
+ *     loop (there is no workspace for a widened copy): the speed of
+ *     convrot_linear_fwd with a small workspace, below that of its
+ *     widened-weight path.
  *   - All calls share the array: calls whose kernels can overlap on the GPU
  *     (other streams, other host threads) race and must be serialised by the
  *     caller.  Nothing needs clearing between calls: each call rewrites all
@@ -310,6 +316,33 @@ CONVROT_API int convrot_gemm_s32(const int8_t *A, const int8_t *B, int64_t M, in
  * the next convrot_get_error() returns CONVROT_ERR_TIMEOUT and the context
  * remains usable.  (The GEMM's own waits use a 2 s limit.) */
 CONVROT_API int convrot_selftest_wait_timeout(uint64_t limit_ns, convrot_stream_t stream);
+
+/* Measurement entry for a roofline denominator: launches a kernel of four
+ * 256-thread CTAs per SM whose warps issue only dense int8 MMAs through the
+ * legacy warp-level path (mma.sync m16n8k32 s8 x s8 -> s32; tcgen05 has no
+ * int8 kind on this GPU), `iters` rounds of 8 independent MMAs per warp.
+ * *ops (host pointer) receives the operation count of the launch (2 per
+ * multiply-add); time the launch on `stream` to get the rate.  sink: device
+ * int32 buffer of at least 4 * (number of SMs) entries, overwritten. */
+CONVROT_API int convrot_probe_mma_s8_rate(int iters, int32_t *sink, size_t sink_bytes, double *ops,
+                              convrot_stream_t stream);
+
+/* Test entry for the GEMM's own failure path: convrot_gemm_dequant (widened =
+ * 0: Wq int8 [N, K], widened inside the GEMM loop) or convrot_gemm_dequant_w16
+ * (widened = 1: Wq fp16-held codes [N, K]) with two changes made for the test:
+ * every pipeline wait of the GEMM gives up after `limit_ns` (1 ns .. 10 s)
+ * instead of 2 s, and the copy that `producer` (0: the activation tiles,
+ * 1: the weight tiles) would issue at its iteration `skip_iteration` (counted
+ * over the K blocks of the tiles a CTA processes, from 0) is never issued.  The
+ * stage it would fill stays empty, so a consumer's bounded wait expires: every
+ * role of the CTA then stops, copies and MMAs in flight are drained, the
+ * tensor memory is freed and the kernel returns.  The next convrot_get_error()
+ * returns CONVROT_ERR_TIMEOUT; y is partly written; the context stays usable.
+ * Arguments as in convrot_gemm_dequant (no bias). */
+CONVROT_API int convrot_selftest_gemm_fault(int widened, const uint16_t *xq, const float *scale_x, int64_t M,
+                                int64_t K, const void *Wq, const float *scale_w, int64_t N, uint16_t *y,
+                                uint64_t limit_ns, int64_t skip_iteration, int producer,
+                                convrot_stream_t stream);
 
 #ifdef __cplusplus
 }

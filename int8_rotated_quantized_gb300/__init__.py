@@ -72,6 +72,8 @@ def lib():
                 "convrot_linear_fwd_noalloc": ([P, I64, I64, P, P, I64, I, P, P, P], I),
                 "convrot_linear_fwd_noalloc_max_bytes": ([], S),
                 "convrot_selftest_wait_timeout": ([ctypes.c_uint64, P], I),
+                "convrot_probe_mma_s8_rate": ([I, P, S, ctypes.POINTER(ctypes.c_double), P], I),
+                "convrot_selftest_gemm_fault": ([I, P, P, I64, I64, P, P, I64, P, ctypes.c_uint64, I64, I, P], I),
             }
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
@@ -437,7 +439,7 @@ def convrot_linear_fwd_noalloc_max_bytes() -> int:
 
 def convrot_linear_fwd_noalloc(x, Wq, scale_w, block, bias=None, y=None, stream=None):
     """Forward without a caller workspace, for callers that cannot allocate on
-    this path (the library keeps the activation codes in a fixed 64 MiB device
+    this path (the library keeps the activation codes in a fixed 64.25 MiB device
     array; calls that overlap on the GPU must be serialised by the caller).
     `y` must be given by such callers; it is allocated here only for
     convenience when omitted."""

@@ -15,7 +15,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libconvrot.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
-SOURCES = ["rotq.cu", "rotq_wide.cu", "lora_rotq.cu", "bwd_prep.cu", "bwd_r2.cu", "gemm_tc.cu", "convrot_api.cu", "noalloc.cu", "selftest.cu"]
+SOURCES = ["rotq.cu", "rotq_wide.cu", "lora_rotq.cu", "bwd_prep.cu", "bwd_r2.cu", "gemm_tc.cu", "convrot_api.cu",
+           "noalloc.cu", "selftest.cu", "peak_probe.cu"]
 HEADERS = ["common.cuh", "fwht.cuh", "mbar.cuh", "wide.cuh", "internal.h", "launch_cache.h"]
 
 NVCC_FLAGS = [

@@ -32,7 +32,8 @@ def test_header_declares_the_boundary():
                  "convrot_gemm_bf16", "convrot_linear_bwd_x_bf16", "convrot_bwd_x_bf16_workspace_bytes",
                  "convrot_linear_workspace_bytes", "convrot_widen_codes", "convrot_gemm_dequant_w16",
                  "convrot_linear_fwd_lora", "convrot_linear_lora_workspace_bytes", "convrot_linear_bwd_x_r2",
-                 "convrot_bwd_x_r2_workspace_bytes"]:
+                 "convrot_bwd_x_r2_workspace_bytes", "convrot_selftest_gemm_fault",
+                 "convrot_probe_mma_s8_rate"]:
         assert must in names
 
 
