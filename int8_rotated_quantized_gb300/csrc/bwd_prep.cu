@@ -241,12 +241,23 @@ __device__ __forceinline__ uint16_t df_to_bf16(float hi, float lo) {
 }
 
 // A CTA takes 64 weight rows and KT = max(128, B) columns; each thread owns
-// 32 consecutive codes of one row (two 16-byte loads), transforms them in
-// registers (packed fp32 butterflies, log2(B / 32) stages across lanes), forms
-// every value as a double-float product with the row's double-float scale
-// s * (1/sqrt(B)), rounds it to bf16 and writes it into a shared tile
-// [KT][64] whose 8-column groups are xor-swizzled by the writer's 32-column
-// chunk; the tile leaves as 16-byte stores (128-byte row segments of T).
+// 32 consecutive codes of one row (two 16-byte loads), turns them into exact
+// fp32 values (byte splice), transforms them in registers (packed fp32
+// butterflies, log2(B / 32) stages across lanes; integer sums below 2^15, so
+// exact), rounds every value s * u / sqrt(B) to bf16 and writes it into a
+// shared tile [KT][64] whose 8-column groups are xor-swizzled by the writer's
+// 32-column chunk; the tile leaves as 16-byte stores (128-byte row segments of
+// T).  (A persistent form of this kernel, loading the next tile's codes while
+// transforming the current one, measured slower: 64-68 us against 58 us.)
+//
+// Rounding.  With (sh, sl) the row factor s / sqrt(B) as a double-float, the
+// value is v = u (sh + sl).  The fp32 product p = u * sh differs from it by
+// less than 2.5 fp32 steps of p (half a step from the product's rounding,
+// under two from u * sl, since |sl| <= one step of sh), so the bf16 rounding
+// of p is already the correct rounding of v unless p's low 16 bits lie within
+// that distance of 0x8000, a bf16 rounding midpoint.  Groups of 8 values with
+// such a p (about 1 in 900 per thread) are rounded again from the exact
+// double-float value hi + lo; the rest keep the rounding of p.
 template <int B>
 __global__ void __launch_bounds__(512) dequant_t_kernel(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K,
                                                         float ch, float cl, uint16_t *T) {
@@ -274,17 +285,45 @@ __global__ void __launch_bounds__(512) dequant_t_kernel(const int8_t *Wq, const 
     const float sl = __fmaf_rn(s, cl, __fmaf_rn(s, ch, -sh));
     float e[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) e[i] = (float)(int8_t)((w[i >> 2] >> (8 * (i & 3))) & 0xff);
+    for (int k = 0; k < 8; ++k) codes_to_f32x4(w[k], &e[4 * k]);
     fwht32<LOGB>(e, lane);  // exact: integer sums below 2^15
+    uint32_t pk[16];
+    // per group of 8 values, the smallest distance (mod 2^16) of a low half
+    // above 0x7ffc, kept per 16-bit lane: the low halves of p0 and p1 are
+    // packed into one word and 0x7ffc7ffc is subtracted from it as a 32-bit
+    // number; a borrow out of the lower lane shifts the upper lane's window by
+    // one step, so a lane value <= 8 covers every low half within 2.5 steps
+    // of 0x8000 either way
+    uint32_t near[4] = {~0u, ~0u, ~0u, ~0u};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float p0 = e[2 * i], p1 = e[2 * i + 1];
+        mul2c(p0, p1, sh);
+        const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+        pk[i] = *reinterpret_cast<const uint32_t *>(&h);
+        const uint32_t d = __byte_perm(__float_as_uint(p0), __float_as_uint(p1), 0x5410) - 0x7ffc7ffcu;
+        asm("min.u16x2 %0, %0, %1;" : "+r"(near[i >> 2]) : "r"(d));
+    }
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        if ((near[g] & 0xffffu) <= 8u || (near[g] >> 16) <= 8u) {
+#pragma unroll
+            for (int i = 8 * g; i < 8 * g + 8; ++i) {
+                // u * (sh + sl) as hi + lo: the product u * sh exactly, plus u * sl
+                const float hi = __fmul_rn(e[i], sh);
+                const float lo = __fmaf_rn(e[i], sl, __fmaf_rn(e[i], sh, -hi));
+                float rh, rlo;
+                fast_two_sum(hi, lo, rh, rlo);
+                const uint32_t b = df_to_bf16(rh, rlo);
+                pk[i >> 1] = (i & 1) ? ((pk[i >> 1] & 0xffffu) | (b << 16)) : ((pk[i >> 1] & 0xffff0000u) | b);
+            }
+        }
+    }
     const int slot = rl ^ (8 * (c & 7));
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        // u * (sh + sl) as hi + lo: the product u * sh exactly, plus u * sl
-        const float hi = __fmul_rn(e[i], sh);
-        const float lo = __fmaf_rn(e[i], sl, __fmaf_rn(e[i], sh, -hi));
-        float rh, rlo;
-        fast_two_sum(hi, lo, rh, rlo);
-        dtile[(32 * c + i) * kDeqRows + slot] = df_to_bf16(rh, rlo);
+    for (int i = 0; i < 16; ++i) {
+        dtile[(32 * c + 2 * i) * kDeqRows + slot] = (uint16_t)(pk[i] & 0xffffu);
+        dtile[(32 * c + 2 * i + 1) * kDeqRows + slot] = (uint16_t)(pk[i] >> 16);
     }
     __syncthreads();
     for (int idx = tid; idx < KT * (kDeqRows / 8); idx += blockDim.x) {

@@ -429,6 +429,40 @@ def test_dequant_weight_t_parity(N, K, block):
     np.testing.assert_array_equal(got, ref)
 
 
+def test_dequant_weight_t_rounding_midpoints():
+    """Values on and beside bf16 rounding midpoints.  With b = 64 (1/sqrt(b) = 1/8 exact)
+    and one code q per row, W_eff = s q H[j, k] / 8 = +-s q / 8; the scales are chosen so
+    that s q / 8 lands exactly on a midpoint between two bf16 values (ties go to even), or
+    one and a few fp32 steps beside it, across binades; q in {1, 3, 5, 7, 127} makes the
+    product inexact in fp32 for most rows.  Every value must be the correctly rounded one."""
+    b, K = 64, 128
+    rng = np.random.default_rng(41)
+    qs, ss = [], []
+    for e in range(-12, 3):
+        for mant in (0, 37, 101, 127):
+            mid = (1.0 + (2 * mant + 1) / 256.0) * 2.0 ** e  # halfway between two bf16 neighbours
+            for q in (1, 3, 5, 7, 127):
+                for off in (0, 1, -1, 2, -2, 5):
+                    s = np.float32(8.0 * mid / q)
+                    s = np.nextafter(s, np.float32(np.inf)) if off > 0 else s
+                    for _ in range(max(0, abs(off) - 1)):
+                        s = np.nextafter(s, np.float32(np.inf) if off > 0 else np.float32(-np.inf))
+                    if off < 0:
+                        s = np.nextafter(s, np.float32(-np.inf))
+                    qs.append(q if rng.integers(2) else -q)
+                    ss.append(s)
+    N = (len(qs) + 15) // 16 * 16
+    wq = np.zeros((N, K), dtype=np.int8)
+    sw = np.zeros(N, dtype=np.float32)
+    for n, (q, s) in enumerate(zip(qs, ss)):
+        wq[n, rng.integers(b)] = q
+        wq[n, b + rng.integers(b)] = -q
+        sw[n] = s
+    ref = oracle.dequant_weight_t(wq, sw, b)
+    got = bits_of(cr.convrot_dequant_weight_t(_i8(wq), _f32(sw), b))
+    np.testing.assert_array_equal(got, ref)
+
+
 @pytest.mark.parametrize("M,N,K", [(300, 272, 1008), (64, 128, 64), (513, 400, 4096)])
 def test_gemm_bf16_parity(M, N, K):
     A = synth.normal_bf16(16, synth.STREAM_DY, M, K, 1.0)
