@@ -157,9 +157,10 @@ CONVROT_API int convrot_linear_fwd(const uint16_t *x, int64_t M, int64_t K, cons
                        uint16_t *y, void *workspace, size_t ws_bytes, convrot_stream_t stream);
 
 /* Bytes of workspace convrot_linear_fwd_lora needs: those of the widened-weight
- * path plus the scaled down-projection (16 rows of M rounded up to 256, fp32)
- * and, when the down-projection splits K into column spans (few rows), one
- * partial-sum array of that size per span (at most 8). */
+ * path, the scaled down-projection and the adapter's B as three bf16 parts per
+ * value (128 bytes per row of M and of N), and, when the down-projection
+ * splits K into column spans (few rows), fp32 partial sums (16 x M rounded up
+ * to 256 per span, at most 8 spans). */
 CONVROT_API size_t convrot_linear_lora_workspace_bytes(int64_t M, int64_t K, int64_t N);
 
 /* Forward with an unmerged LoRA adapter as a bypass (the LoRA branch of a
@@ -167,7 +168,10 @@ CONVROT_API size_t convrot_linear_lora_workspace_bytes(int64_t M, int64_t K, int
  * the merge formula of the voxprint-model-forge MOSS page gives the scaling):
  *   y = bf16( acc * scale_x[m] * scale_w[n] + bias[n]
  *             + sum_j (coef * sum_k x[m,k] lora_A[j,k]) * lora_B[n,j] ),
- *   coef = fp32(scale * alpha / rank), the branch summed in fp32.
+ *   coef = fp32(scale * alpha / rank).  The down-projection is summed in fp32;
+ *   the branch runs on the tensor cores with each fp32 factor split into three
+ *   bf16 parts (about 24 bits) and fp32 accumulation, and is added to the
+ *   dequantized product before the rounding.
  * x bf16 [M, K] (K multiple of 32); lora_A fp32 [rank, K] (16-byte aligned); lora_B fp32 [N, rank];
  * 1 <= rank <= 16; workspace >= convrot_linear_lora_workspace_bytes(M, K, N),
  * 256-byte aligned.  Weight codes as in convrot_linear_fwd. */

@@ -218,9 +218,10 @@ int convrot_linear_fwd(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq
 
 size_t convrot_linear_lora_workspace_bytes(int64_t M, int64_t K, int64_t N) {
     if (M < 0 || K < 0 || N < 0) return 0;
-    const int splits = convrot::lora_down_splits(M, K);
-    const size_t xa_bytes = align256((size_t)convrot::lora_xa_ld(M) * 16 * sizeof(float));
-    return convrot_linear_workspace_bytes(M, K, N) + xa_bytes + (splits > 1 ? (size_t)splits * xa_bytes : 0);
+    const size_t parts_row = (size_t)convrot::kLoraPartsRow * 2;
+    return convrot_linear_workspace_bytes(M, K, N) + align256((size_t)M * parts_row) +
+           align256((size_t)N * parts_row) + align256((size_t)48 * (size_t)K * 2) +
+           align256((size_t)convrot::lora_down_spans(M, K) * (size_t)M * 48 * sizeof(float));
 }
 
 int convrot_linear_fwd_lora(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq, const float *scale_w,
@@ -243,18 +244,25 @@ int convrot_linear_fwd_lora(const uint16_t *x, int64_t M, int64_t K, const int8_
     uint16_t *xq = reinterpret_cast<uint16_t *>(ws);
     float *sx = reinterpret_cast<float *>(ws + align256((size_t)M * (size_t)K * 2));
     uint16_t *w16 = reinterpret_cast<uint16_t *>(ws + convrot_act_workspace_bytes(M, K));
-    float *xa = reinterpret_cast<float *>(ws + convrot_linear_workspace_bytes(M, K, N));
+    const size_t parts_row = (size_t)convrot::kLoraPartsRow * 2;
+    char *lw = ws + convrot_linear_workspace_bytes(M, K, N);
+    uint16_t *xa_parts = reinterpret_cast<uint16_t *>(lw);
+    lw += align256((size_t)M * parts_row);
+    uint16_t *b_parts = reinterpret_cast<uint16_t *>(lw);
+    lw += align256((size_t)N * parts_row);
+    uint16_t *ap = reinterpret_cast<uint16_t *>(lw);
+    lw += align256((size_t)48 * (size_t)K * 2);
+    float *part = reinterpret_cast<float *>(lw);
     const float coef = (float)((double)scale * (double)alpha / (double)rank);
     rc = quantize_act_impl(x, M, K, K, block, xq, sx, st);
     if (rc != CONVROT_OK) return rc;
-    float *part = reinterpret_cast<float *>(reinterpret_cast<char *>(xa) +
-                                            align256((size_t)convrot::lora_xa_ld(M) * 16 * sizeof(float)));
-    rc = cuda_status(convrot::launch_lora_down(x, M, K, lora_A, rank, coef, xa, part, st));
+    rc = cuda_status(
+        convrot::launch_lora_operands(x, M, K, lora_A, lora_B, N, rank, coef, ap, xa_parts, b_parts, part, err, st));
     if (rc != CONVROT_OK) return rc;
     rc = cuda_status(convrot::launch_widen_codes(Wq, N * K, w16, st));
     if (rc != CONVROT_OK) return rc;
     return cuda_status(
-        convrot::launch_gemm_w16_lora(xq, sx, w16, scale_w, bias, xa, lora_B, rank, M, N, K, y, err, st));
+        convrot::launch_gemm_w16_lora(xq, sx, w16, scale_w, bias, xa_parts, b_parts, M, N, K, y, err, st));
 }
 
 size_t convrot_bwd_weight_workspace_bytes(int64_t N, int64_t K) {

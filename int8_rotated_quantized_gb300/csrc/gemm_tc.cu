@@ -51,6 +51,7 @@
 #include "internal.h"
 #include "launch_cache.h"
 #include "mbar.cuh"
+#include "tcgen05.cuh"
 #include "wide.cuh"
 
 namespace convrot {
@@ -69,8 +70,12 @@ constexpr int WH_STAGE = TW * BK * 2;  // 16 KB widened weight tile
 // dequantization epilogue on weight codes that a separate pass already
 // widened to fp16 (no converter in the loop, the same exact integer chunks).
 constexpr int kModeS32 = 0, kModeDequant = 1, kModeBf16 = 2, kModeDequantW16 = 3;
-// The widened-weight dequantization mode plus a LoRA bypass term in the
-// epilogue: y += sum_j xa[m, j] * B[n, j] (xa already scaled, stored transposed).
+// The widened-weight dequantization mode plus a LoRA bypass term:
+// y += sum_j xa[m, j] * B[n, j] (xa already scaled).  The term is one more
+// K block per tile on the tensor cores: xa and B enter as three bf16 parts
+// each (hi + mid + lo = the fp32 value to about 24 bits), the six products of
+// parts whose orders add up to at most 2 accumulate in fp32 into the next
+// TMEM chunk buffer, and the epilogue adds that chunk to the dequantized y.
 constexpr int kModeDequantW16Lora = 4;
 // Widened weight codes, exact integer chunks, and an fp32 result scaled by the
 // token's scale only: P[m, n] = float(acc) * sa[m] (the second reading of the
@@ -97,17 +102,11 @@ struct Layout {
     static constexpr int OFF_X = 0;
     static constexpr int OFF_W8 = OFF_X + XS * X_STAGE;
     static constexpr int OFF_WH = OFF_W8 + WS * W8_STAGE;
-    // bypass mode: the down-projection of the tile's tokens, [2 halves][16][128] fp32
-    static constexpr int XA_BYTES = MODE == kModeDequantW16Lora ? 2 * 16 * 128 * 4 : 0;
-    static constexpr int OFF_XA = OFF_WH + CS * WH_STAGE;
-    static constexpr int OFF_BAR = OFF_XA + XA_BYTES;
+    static constexpr int OFF_BAR = OFF_WH + CS * WH_STAGE;
     static constexpr int BAR_X_FULL = 0, BAR_X_EMPTY = XS, BAR_W_FULL = 2 * XS, BAR_W_EMPTY = BAR_W_FULL + WS,
                          BAR_CONV_FULL = BAR_W_EMPTY + WS, BAR_CONV_EMPTY = BAR_CONV_FULL + CS,
                          BAR_ACC_FULL = BAR_CONV_EMPTY + CS, BAR_ACC_EMPTY = BAR_ACC_FULL + 2,
-                         BAR_DRAIN = BAR_ACC_EMPTY + 2,
-                         BAR_XS_READY = BAR_DRAIN + 1,  // bypass rows staged (per half, 128 arrivals)
-                         BAR_XS_FREE = BAR_XS_READY + 2,  // bypass rows read (per half, 4 warp arrivals)
-                         NUM_BARS = BAR_XS_FREE + 2;
+                         BAR_DRAIN = BAR_ACC_EMPTY + 2, NUM_BARS = BAR_DRAIN + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -131,10 +130,6 @@ struct GemmArgs {
     const uint16_t *bias;
     void *out;
     unsigned *err;
-    const float *lora_xa;  // [16][lora_ld], transposed, coef folded in (bypass mode)
-    const float *lora_b;   // [N, lora_rank] (bypass mode)
-    int lora_rank;
-    int64_t lora_ld;       // row stride of lora_xa: M rounded up to 256
     uint64_t wait_limit_ns = kWaitLimitNs;  // bound of every pipeline wait
     // Failure-path self-test only: the producer named by fault_role (0 the
     // activation producer, 1 the weight producer) issues no copy at its
@@ -143,60 +138,6 @@ struct GemmArgs {
     int fault_skip_it = -1;
     int fault_role = -1;
 };
-
-// ------------------------------------------------------------- PTX wrappers --
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
-            dst),
-        "l"(map), "r"(bar), "r"(x), "r"(y)
-        : "memory");
-}
-
-// (a0, a1) <- (x0 * k + a0, x1 * k + a1) on fp32 values held as int bits: one
-// rounding per lane, bit-identical to two fmaf.
-__device__ __forceinline__ void fma2_acc(int &a0, int &a1, float x0, float x1, float k) {
-    asm("{\n .reg .b64 ra, rx, rk;\n mov.b64 ra, {%0, %1};\n mov.b64 rx, {%2, %3};\n mov.b64 rk, {%4, %4};\n"
-        " fma.rn.f32x2 ra, rx, rk, ra;\n mov.b64 {%0, %1}, ra;\n}"
-        : "+r"(a0), "+r"(a1)
-        : "f"(x0), "f"(x1), "f"(k));
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
-        "[%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr)
-        : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Shared-memory matrix descriptor of a K-major operand tile stored in 128-byte
-// swizzle atoms (8 rows x 128 bytes, atoms 1024 bytes apart along M/N):
-// start address >> 4 (bits 0-13), leading byte offset >> 4 (bits 16-29, not
-// used by swizzled K-major layouts), stride byte offset >> 4 (bits 32-45),
-// descriptor version 1 (bit 46), swizzle mode 2 = 128B (bits 61-63).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
-    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
 
 // All 512 threads meet here at the end; each role reaches it from its own
 // branch, so no code runs after a join of regions with different register
@@ -248,7 +189,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_s8_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const GemmArgs p) {
+    gemm_s8_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                      const __grid_constant__ CUtensorMap tmXA, const __grid_constant__ CUtensorMap tmLB,
+                      const GemmArgs p) {
     using L = Layout<MODE>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -281,10 +224,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(bar(L::BAR_ACC_EMPTY + i), 8);
         }
         mbar_init(bar(L::BAR_DRAIN), 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(L::BAR_XS_READY + i), 128);
-            mbar_init(bar(L::BAR_XS_FREE + i), 4);
-        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -306,6 +245,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int num_kb = (p.K + BK - 1) / BK;
     // K blocks per TMEM accumulation: exact-integer chunks, or all of K for bf16
     const int chunk_kb = MODE == kModeBf16 ? num_kb : CHUNK_KB;
+    // the bypass mode's extra K block per tile (the LoRA parts), its own chunk
+    constexpr int kExtra = MODE == kModeDequantW16Lora ? 1 : 0;
 
     if (warp < 4) {
         regs_dec<REGS_WG0>();
@@ -327,7 +268,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
                 int tb, wb;
                 tile_coords(tile, num_t, num_w, p.group, p.group_weight != 0, tb, wb);
-                for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                for (int kb = 0; kb < num_kb + kExtra; ++kb, ++it) {
                     const int s = it % nst;
                     if (!mbar_wait(bar(empty0 + s), ((it / nst) & 1) ^ 1, abort_flag, p.err, p.wait_limit_ns)) {
                         ok = false;
@@ -337,12 +278,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         skipped = it;  // self-test: this stage is never filled
                         continue;
                     }
+                    const bool extra = kExtra && kb == num_kb;  // bypass parts: 128 bytes per row
                     if (is_x) {
                         mbar_expect_tx(bar(full0 + s), X_STAGE);
-                        tma_load_2d(sX + s * X_STAGE, map, bar(full0 + s), kb * BK, tb * TT);
+                        tma_load_2d(sX + s * X_STAGE, extra ? &tmXA : map, bar(full0 + s), extra ? 0 : kb * BK,
+                                    tb * TT);
                     } else if (w_direct) {
                         mbar_expect_tx(bar(full0 + s), WH_STAGE);
-                        tma_load_2d(sWh + s * WH_STAGE, map, bar(full0 + s), kb * BK, wb * TW);
+                        tma_load_2d(sWh + s * WH_STAGE, extra ? &tmLB : map, bar(full0 + s), extra ? 0 : kb * BK,
+                                    wb * TW);
                     } else {
                         mbar_expect_tx(bar(full0 + s), W8_STAGE);
                         tma_load_2d(sW8 + s * W8_STAGE, map, bar(full0 + s), kb * BK, wb * TW);
@@ -359,8 +303,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             uint32_t dcol = 0;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                for (int kb = 0; kb < num_kb; ++kb, ++it) {
-                    const int kc = kb % chunk_kb;
+                for (int kb = 0; kb < num_kb + kExtra; ++kb, ++it) {
+                    const bool extra = kExtra && kb == num_kb;
+                    const int kc = extra ? 0 : kb % chunk_kb;
                     if (kc == 0) {
                         const int buf = g & 1;
                         if (!mbar_wait(bar(L::BAR_ACC_EMPTY + buf), ((g >> 1) & 1) ^ 1, abort_flag, p.err,
@@ -379,16 +324,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
+                    if (extra) {
+                        // parts at byte offsets 0 (hi), 32 (mid), 64 (lo) of each 128-byte row:
+                        // hi*hi, hi*mid, mid*hi, hi*lo, mid*mid, lo*hi
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = sw128_desc(sWh + c * WH_STAGE + kk * 32);
-                        const uint64_t bd = sw128_desc(sX + s * X_STAGE + kk * 32);
-                        umma_f16(tmem + dcol, ad, bd, MODE == kModeBf16 ? kIdescBF16 : kIdescF16,
-                                 (kc > 0 || kk > 0) ? 1u : 0u);
+                        for (int q = 0; q < 6; ++q) {
+                            const int pa = q == 0 ? 0 : q == 1 ? 0 : q == 2 ? 1 : q == 3 ? 0 : q == 4 ? 1 : 2;
+                            const int pb = q == 0 ? 0 : q == 1 ? 1 : q == 2 ? 0 : q == 3 ? 2 : q == 4 ? 1 : 0;
+                            const uint64_t ad = sw128_desc(sWh + c * WH_STAGE + pa * 32);
+                            const uint64_t bd = sw128_desc(sX + s * X_STAGE + pb * 32);
+                            umma_f16(tmem + dcol, ad, bd, kIdescBF16, q > 0 ? 1u : 0u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            const uint64_t ad = sw128_desc(sWh + c * WH_STAGE + kk * 32);
+                            const uint64_t bd = sw128_desc(sX + s * X_STAGE + kk * 32);
+                            umma_f16(tmem + dcol, ad, bd, MODE == kModeBf16 ? kIdescBF16 : kIdescF16,
+                                     (kc > 0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     umma_commit(bar(L::BAR_X_EMPTY + s));
                     umma_commit(bar(L::BAR_CONV_EMPTY + c));
-                    if (kc == chunk_kb - 1 || kb == num_kb - 1) {
+                    if (extra || kc == chunk_kb - 1 || kb == num_kb - 1) {
                         umma_commit(bar(L::BAR_ACC_FULL + (g & 1)));
                         ++g;
                     }
@@ -460,31 +418,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         regs_inc<REGS_EPI>();
         const int q = warp & 3;          // TMEM lane quarter = weight rows 32q .. 32q+31
         const int h = (warp - 8) >> 2;   // token half of the 256-wide tile
-        int g = 0, u = 0;  // u: tiles this CTA has processed
+        int g = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++u) {
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
             int tb, wb;
             tile_coords(tile, num_t, num_w, p.group, p.group_weight != 0, tb, wb);
-            if constexpr (MODE == kModeDequantW16Lora) {
-                // stage this half-tile's bypass rows (rank x 128 tokens) in shared memory
-                // while the chunks accumulate, once the four warps of this half have read
-                // the previous tile's rows (bounded waits, like every pipeline wait)
-                if (u > 0 && !warp_wait(bar(L::BAR_XS_FREE + h), (u - 1) & 1, abort_flag, p.err, p.wait_limit_ns)) {
-                    ok = false;
-                    break;
-                }
-                const float *xt = p.lora_xa + (int64_t)tb * TT + h * 128;
-                float *xs = reinterpret_cast<float *>(smem + L::OFF_XA) + h * 16 * 128;
-                const int ht = threadIdx.x & 127;
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int idx = ht + 128 * r, j = idx >> 5, c4 = idx & 31;
-                    if (j < p.lora_rank)
-                        *reinterpret_cast<float4 *>(xs + j * 128 + 4 * c4) =
-                            __ldg(reinterpret_cast<const float4 *>(xt + (int64_t)j * p.lora_ld + 4 * c4));
-                }
-                mbar_arrive(bar(L::BAR_XS_READY + h));
-            }
             int acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0;
@@ -521,11 +459,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int m0 = tb * TT + h * 128;
             const int mlim = p.M - m0;  // tokens of this column half that exist
             const bool full = mlim >= 128;
-            if constexpr (MODE == kModeDequantW16Lora) {  // every thread of the half takes part
-                if (!warp_wait(bar(L::BAR_XS_READY + h), u & 1, abort_flag, p.err, p.wait_limit_ns)) {
+            if constexpr (MODE == kModeDequantW16Lora) {
+                // y = acc * (sx * sw) + bias in place (the registers now hold fp32), then
+                // + the bypass chunk from TMEM (every thread of the half takes part)
+                const float swn = n < p.N ? __ldg(p.sb + n) : 0.f;
+                const bool has_bias = p.bias != nullptr && n < p.N;
+                const float bn = has_bias ? bf16_bits_to_float(__ldg(p.bias + n)) : 0.f;
+#pragma unroll
+                for (int i4 = 0; i4 < 128; i4 += 4) {
+                    float sx[4];
+                    if (full) {
+                        const float4 v = __ldg(reinterpret_cast<const float4 *>(p.sa + m0 + i4));
+                        sx[0] = v.x, sx[1] = v.y, sx[2] = v.z, sx[3] = v.w;
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) sx[j] = i4 + j < mlim ? __ldg(p.sa + m0 + i4 + j) : 0.f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float y = __fmul_rn(__int2float_rn(acc[i4 + j]), __fmul_rn(sx[j], swn));
+                        if (has_bias) y = __fadd_rn(y, bn);
+                        acc[i4 + j] = __float_as_int(y);
+                    }
+                }
+                const int buf = g & 1;
+                if (!warp_wait(bar(L::BAR_ACC_FULL + buf), (g >> 1) & 1, abort_flag, p.err, p.wait_limit_ns)) {
                     ok = false;
                     break;
                 }
+                tc_fence_after();
+                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * TT + h * 128);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t r[16];
+                    tmem_ld16(taddr + 16 * j, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        acc[16 * j + i] = __float_as_int(__fadd_rn(__int_as_float(acc[16 * j + i]), __uint_as_float(r[i])));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::BAR_ACC_EMPTY + buf));
+                ++g;
             }
             if (n < p.N) {
                 if constexpr (MODE == kModeS32) {
@@ -560,44 +536,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (full || i < mlim) *out = (uint16_t)float_to_bf16_bits(__int_as_float(acc[i]));
                         out += p.N;
                     }
-                } else if constexpr (MODE == kModeDequantW16Lora) {
-                    // pass 1: y = acc * (sx * sw) + bias in place (the registers now hold fp32)
-                    const float swn = __ldg(p.sb + n);
-                    const bool has_bias = p.bias != nullptr;
-                    const float bn = has_bias ? bf16_bits_to_float(__ldg(p.bias + n)) : 0.f;
-#pragma unroll
-                    for (int i4 = 0; i4 < 128; i4 += 4) {
-                        float sx[4];
-                        if (full) {
-                            const float4 v = __ldg(reinterpret_cast<const float4 *>(p.sa + m0 + i4));
-                            sx[0] = v.x, sx[1] = v.y, sx[2] = v.z, sx[3] = v.w;
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) sx[j] = i4 + j < mlim ? __ldg(p.sa + m0 + i4 + j) : 0.f;
-                        }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            float y = __fmul_rn(__int2float_rn(acc[i4 + j]), __fmul_rn(sx[j], swn));
-                            if (has_bias) y = __fadd_rn(y, bn);
-                            acc[i4 + j] = __float_as_int(y);
-                        }
-                    }
-                    // pass 2: the bypass branch on the unrotated input, y += sum_j xa[m, j] B[n, j]
-                    // in j order, from the staged rows (transposed, coef folded in): each load
-                    // brings 4 consecutive tokens of one j and the 128 sums are independent
-                    const float *xs = reinterpret_cast<const float *>(smem + L::OFF_XA) + h * 16 * 128;
-                    for (int j = 0; j < p.lora_rank; ++j) {
-                        const float bj = __ldg(p.lora_b + (int64_t)n * p.lora_rank + j);
-                        const float4 *row = reinterpret_cast<const float4 *>(xs + j * 128);
-#pragma unroll
-                        for (int i4 = 0; i4 < 128; i4 += 4) {
-                            const float4 v = row[i4 >> 2];  // every lane reads the same 16 bytes
-                            // y += xa * b on packed pairs (one rounding per lane, as fmaf)
-                            fma2_acc(acc[i4], acc[i4 + 1], v.x, v.y, bj);
-                            fma2_acc(acc[i4 + 2], acc[i4 + 3], v.z, v.w, bj);
-                        }
-                    }
-                    // pass 3: round and store
+                } else if constexpr (MODE == kModeDequantW16Lora) {  // y (with the bypass) is in the registers
                     uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)m0 * p.N + n;
 #pragma unroll
                     for (int i = 0; i < 128; ++i) {
@@ -629,41 +568,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
-            if constexpr (MODE == kModeDequantW16Lora) {  // this warp is done with the staged rows
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::BAR_XS_FREE + h));
-            }
         }
         end_barrier();
     }
 }
 
 // ------------------------------------------------------------------- host --
-
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-
-cudaError_t get_encoder() {
-    std::call_once(g_encode_once, [] {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    });
-    return g_encode ? cudaSuccess : cudaErrorNotSupported;
-}
-
-bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, size_t esize, const void *ptr, uint64_t inner, uint64_t outer,
-               uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * esize};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    return g_encode(map, dt, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 // Raster choice.  The tiles of the grouped dimension are read from DRAM once
 // if `group` of them (plus the streaming tiles of one wave) stay in L2; the
@@ -683,15 +593,16 @@ void choose_raster(int64_t num_t, int64_t num_w, int64_t K, int64_t w_elem, int 
     group = (int)(group_weight ? gw : gt);
 }
 
+// tmXA / tmLB: the bypass parts (bypass mode only; other modes pass any map, unused).
 template <int MODE>
 cudaError_t launch_mode(const CUtensorMap &tmX, const CUtensorMap &tmW, const GemmArgs &p, int64_t tiles,
-                        cudaStream_t st) {
+                        cudaStream_t st, const CUtensorMap *tmXA = nullptr, const CUtensorMap *tmLB = nullptr) {
     const int sms = sm_count();
     const int grid = (int)(tiles < sms ? tiles : sms);
     constexpr int kSmem = Layout<MODE>::SMEM_BYTES;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_s8_tc_kernel<MODE>), kSmem);
     if (e != cudaSuccess) return e;
-    gemm_s8_tc_kernel<MODE><<<grid, NUM_THREADS, kSmem, st>>>(tmX, tmW, p);
+    gemm_s8_tc_kernel<MODE><<<grid, NUM_THREADS, kSmem, st>>>(tmX, tmW, tmXA ? *tmXA : tmX, tmLB ? *tmLB : tmW, p);
     return cudaGetLastError();
 }
 
@@ -736,23 +647,26 @@ cudaError_t launch_gemm_w16(const uint16_t *A, const float *sa, const uint16_t *
 }
 
 cudaError_t launch_gemm_w16_lora(const uint16_t *A, const float *sa, const uint16_t *B16, const float *sb,
-                                 const uint16_t *bias, const float *xa, const float *lora_b, int rank, int64_t M,
+                                 const uint16_t *bias, const uint16_t *xa_parts, const uint16_t *b_parts, int64_t M,
                                  int64_t N, int64_t K, uint16_t *out, unsigned *err, cudaStream_t st) {
     if (M == 0 || N == 0) return cudaSuccess;
     cudaError_t e = get_encoder();
     if (e != cudaSuccess) return e;
-    CUtensorMap tmX, tmW;
+    CUtensorMap tmX, tmW, tmXA, tmLB;
     if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, (uint64_t)K, (uint64_t)M, BK, TT,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B16, (uint64_t)K, (uint64_t)N, BK, TW,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmXA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xa_parts, kLoraPartsRow, (uint64_t)M, BK, TT,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tmLB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, b_parts, kLoraPartsRow, (uint64_t)N, BK, TW,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const int64_t num_t = (M + TT - 1) / TT, num_w = (N + TW - 1) / TW;
     int group, group_weight;
     choose_raster(num_t, num_w, K, 2, group, group_weight);
-    GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, sa, sb, bias, out, err, xa, lora_b, rank,
-               lora_xa_ld(M)};
-    return launch_mode<kModeDequantW16Lora>(tmX, tmW, p, num_t * num_w, st);
+    GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, sa, sb, bias, out, err};
+    return launch_mode<kModeDequantW16Lora>(tmX, tmW, p, num_t * num_w, st, &tmXA, &tmLB);
 }
 
 cudaError_t launch_gemm_w16_scale_f32(const uint16_t *A, const float *sa, const uint16_t *B16, int64_t M, int64_t N,

@@ -52,20 +52,23 @@ cudaError_t launch_gemm(const uint16_t *A, const float *sa, const int8_t *B, con
 cudaError_t launch_gemm_w16(const uint16_t *A, const float *sa, const uint16_t *B16, const float *sb,
                             const uint16_t *bias, int64_t M, int64_t N, int64_t K, uint16_t *out, unsigned *err,
                             cudaStream_t st);
-// The same with the LoRA bypass term added in the epilogue: y += sum_j xa[m, j]
-// lora_b[n, j], xa from launch_lora_down (transposed, already scaled).
+// The same with the LoRA bypass term y += sum_j xa[m, j] lora_b[n, j]: both
+// operands as three bf16 parts per value (kLoraPartsRow = 64 bf16 per row: hi
+// at columns 0-15, mid at 16-31, lo at 32-47, zeros at 48-63; j >= rank zero),
+// xa_parts [M][64] and b_parts [N][64] from launch_lora_operands.  The GEMM
+// adds the term as one more K block per tile on the tensor cores.
+constexpr int kLoraPartsRow = 64;
 cudaError_t launch_gemm_w16_lora(const uint16_t *A, const float *sa, const uint16_t *B16, const float *sb,
-                                 const uint16_t *bias, const float *xa, const float *lora_b, int rank, int64_t M,
+                                 const uint16_t *bias, const uint16_t *xa_parts, const uint16_t *b_parts, int64_t M,
                                  int64_t N, int64_t K, uint16_t *out, unsigned *err, cudaStream_t st);
-// Row stride of the transposed down-projection [16][ld]: M rounded up to 256,
-// so the epilogue's 128-token halves never leave the rows.
-__host__ __device__ inline int64_t lora_xa_ld(int64_t M) { return (M + 255) / 256 * 256; }
-// xa^T[j, m] = coef * sum_k x[m, k] A[j, k] for j < rank (lora_rotq.cu); K % 32 == 0.
-// When lora_down_splits(M, K) > 1 the column spans' partial sums go to `part`
-// ([splits][16][lora_xa_ld(M)] floats) and a second kernel adds them in span order.
-int lora_down_splits(int64_t M, int64_t K);
-cudaError_t launch_lora_down(const uint16_t *x, int64_t M, int64_t K, const float *A, int rank, float coef, float *xa,
-                             float *part, cudaStream_t st);
+// K spans of the tensor-core down-projection for M rows of length K (lora_down.cu).
+int lora_down_spans(int64_t M, int64_t K);
+// The bypass operands (lora_down.cu): ap [48, K] bf16 (the parts of A's rows),
+// b_parts [N][64], part [spans][M][48] fp32 (scratch), and xa_parts [M][64] =
+// the parts of coef * x A^T computed on the tensor cores.  K % 32 == 0.
+cudaError_t launch_lora_operands(const uint16_t *x, int64_t M, int64_t K, const float *A, const float *B, int64_t N,
+                                 int rank, float coef, uint16_t *ap, uint16_t *xa_parts, uint16_t *b_parts,
+                                 float *part, unsigned *err, cudaStream_t st);
 // int8 codes -> fp16 values holding the same integers, 32 per thread (rotq_wide.cu).
 cudaError_t launch_widen_codes(const int8_t *A, int64_t count, uint16_t *out, cudaStream_t st);
 

@@ -369,165 +369,7 @@ cudaError_t launch_lora_rb(const LoraArgs &a, int cs, int logb, cudaStream_t st)
     }
 }
 
-// ----------------------------------------------------------- LoRA bypass --
-
-// The down-projection of the LoRA bypass on the unrotated input, scaled and
-// transposed: xa^T[j, m] = coef * sum_k x[m, k] * A[j, k] (fp32, j < rank), so
-// the GEMM epilogue reads 4 consecutive tokens of one j per 16-byte load.
-// A CTA of 4 warps takes 16 rows (4 per warp) and one span of the columns
-// (the spans split K when there are too few rows to fill the GPU).  Per
-// 128-column chunk the A slice [16][128] sits in shared memory, double
-// buffered: the next chunk's A slice and x values are loaded while the
-// current chunk is multiplied.  Lane l owns columns 4l .. 4l + 3 of its warp's
-// four rows; each A load feeds 16 fused multiply-adds.  At the end the 64
-// sums of a lane are reduced across the warp by halving exchanges (lane l ends
-// with entries 2l and 2l + 1), and the span's result is written scaled by
-// `scale_out` into out[j][m] (row stride lora_xa_ld(M)).
-constexpr int kDownRowsPerWarp = 4, kDownWarps = 4, kDownRows = kDownRowsPerWarp * kDownWarps, kDownChunk = 128;
-
-__global__ void __launch_bounds__(kDownWarps * 32) lora_down_kernel(const uint16_t *x, int64_t M, int64_t K,
-                                                                    const float *A, int rank, int64_t kspan,
-                                                                    float scale_out, float *out, int64_t out_split) {
-    __shared__ __align__(16) float As[2][kLoraMaxRank][kDownChunk];
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int64_t m0 = (int64_t)blockIdx.x * kDownRows + warp * kDownRowsPerWarp;
-    const int64_t kb = (int64_t)blockIdx.y * kspan;
-    const int64_t ke = kb + kspan < K ? kb + kspan : K;
-    const int nch = ke > kb ? (int)((ke - kb + kDownChunk - 1) / kDownChunk) : 0;
-
-    // A[j, kc + 4 c4 .. + 3] for the 4 (j, c4) items of this thread: 2048 floats per chunk
-    auto load_a = [&](int64_t kc, float4 (&r)[4]) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int i = threadIdx.x + kDownWarps * 32 * e, j = i >> 5, c4 = i & 31;
-            const int64_t k = kc + 4 * c4;
-            r[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (j < rank && k < ke) r[e] = __ldg(reinterpret_cast<const float4 *>(A + (int64_t)j * K + k));
-        }
-    };
-    auto store_a = [&](int buf, const float4 (&r)[4]) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int i = threadIdx.x + kDownWarps * 32 * e, j = i >> 5, c4 = i & 31;
-            *reinterpret_cast<float4 *>(&As[buf][j][4 * c4]) = r[e];
-        }
-    };
-    auto load_x = [&](int64_t kc, uint2 (&w)[kDownRowsPerWarp]) {
-        const int64_t k = kc + 4 * lane;
-#pragma unroll
-        for (int r = 0; r < kDownRowsPerWarp; ++r) {
-            const int64_t m = m0 + r;
-            w[r] = make_uint2(0u, 0u);
-            if (m < M && k < ke) w[r] = __ldg(reinterpret_cast<const uint2 *>(x + m * K + k));
-        }
-    };
-
-    float acc[kDownRowsPerWarp * kLoraMaxRank];
-#pragma unroll
-    for (int i = 0; i < kDownRowsPerWarp * kLoraMaxRank; ++i) acc[i] = 0.f;
-    float4 ar[4];
-    uint2 xw[kDownRowsPerWarp], xn[kDownRowsPerWarp];
-    if (nch > 0) {
-        load_a(kb, ar);
-        store_a(0, ar);
-        load_x(kb, xw);
-    }
-    __syncthreads();
-    for (int c = 0; c < nch; ++c) {
-        const int buf = c & 1;
-        const int64_t kc = kb + (int64_t)c * kDownChunk;
-        const bool more = c + 1 < nch;
-        if (more) {  // in flight while this chunk is multiplied
-            load_a(kc + kDownChunk, ar);
-            load_x(kc + kDownChunk, xn);
-        }
-        float xv[kDownRowsPerWarp][4];
-#pragma unroll
-        for (int r = 0; r < kDownRowsPerWarp; ++r) {
-            xv[r][0] = __uint_as_float(xw[r].x << 16), xv[r][1] = __uint_as_float(xw[r].x & 0xffff0000u);
-            xv[r][2] = __uint_as_float(xw[r].y << 16), xv[r][3] = __uint_as_float(xw[r].y & 0xffff0000u);
-        }
-#pragma unroll
-        for (int j = 0; j < kLoraMaxRank; ++j) {
-            const float4 a4 = *reinterpret_cast<const float4 *>(&As[buf][j][4 * lane]);
-#pragma unroll
-            for (int r = 0; r < kDownRowsPerWarp; ++r) {
-                float &a = acc[r * kLoraMaxRank + j];
-                a = __fmaf_rn(xv[r][0], a4.x, a);
-                a = __fmaf_rn(xv[r][1], a4.y, a);
-                a = __fmaf_rn(xv[r][2], a4.z, a);
-                a = __fmaf_rn(xv[r][3], a4.w, a);
-            }
-        }
-        if (more) store_a(buf ^ 1, ar);  // that buffer was last read in the previous chunk, before its barrier
-        __syncthreads();
-#pragma unroll
-        for (int r = 0; r < kDownRowsPerWarp; ++r) xw[r] = xn[r];
-    }
-    // Halving exchanges: with mask h the lanes whose bit h is set keep the upper
-    // half of their entries and send the lower half; after masks 16 .. 1 lane l
-    // holds the warp sums of entries 2l and 2l + 1 (entry = r * 16 + j).
-#pragma unroll
-    for (int h = 16, n = 32; h >= 1; h >>= 1, n >>= 1) {
-        const bool up = (lane & h) != 0;
-#pragma unroll
-        for (int i = 0; i < n; ++i) {
-            const float send = up ? acc[i] : acc[n + i];
-            const float keep = up ? acc[n + i] : acc[i];
-            acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, h);
-        }
-    }
-    const int64_t ld = lora_xa_ld(M);
-    float *o = out + (int64_t)blockIdx.y * out_split;
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        const int e = 2 * lane + t, r = e >> 4, j = e & 15;
-        if (j < rank && m0 + r < M) o[(int64_t)j * ld + m0 + r] = __fmul_rn(scale_out, acc[t]);
-    }
-}
-
-// xa[j][m] = coef * (part[0][j][m] + part[1][j][m] + ...) in span order.
-__global__ void lora_down_sum_kernel(const float *part, int splits, int64_t split_stride, int64_t count, float coef,
-                                     float *xa) {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count; i += (int64_t)gridDim.x * blockDim.x) {
-        float v = part[i];
-        for (int s = 1; s < splits; ++s) v = __fadd_rn(v, part[(int64_t)s * split_stride + i]);
-        xa[i] = __fmul_rn(coef, v);
-    }
-}
-
 }  // namespace
-
-int lora_down_splits(int64_t M, int64_t K) {
-    // enough CTAs to fill the GPU several times over, spans of at least 256 columns
-    const int64_t ctas = (M + kDownRows - 1) / kDownRows;
-    int ks = 1;
-    while (ks < 8 && ctas * ks < 1024 && K / (2 * ks) >= 256) ks *= 2;
-    return ks;
-}
-
-cudaError_t launch_lora_down(const uint16_t *x, int64_t M, int64_t K, const float *A, int rank, float coef, float *xa,
-                             float *part, cudaStream_t st) {
-    if (M == 0) return cudaSuccess;
-    const int ks = lora_down_splits(M, K);
-    const int64_t span = ((K + ks - 1) / ks + kDownChunk - 1) / kDownChunk * kDownChunk;
-    const int64_t ld = lora_xa_ld(M);
-    const dim3 grid((unsigned)((M + kDownRows - 1) / kDownRows), (unsigned)ks);
-    if (ks == 1) {
-        lora_down_kernel<<<grid, kDownWarps * 32, 0, st>>>(x, M, K, A, rank, span, coef, xa, 0);
-        return cudaGetLastError();
-    }
-    const int64_t stride = (int64_t)kLoraMaxRank * ld;
-    lora_down_kernel<<<grid, kDownWarps * 32, 0, st>>>(x, M, K, A, rank, span, 1.0f, part, stride);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const int64_t count = (int64_t)rank * ld;  // rows j >= rank are never read
-    const int64_t blocks = (count + 255) / 256 < 4096 ? (count + 255) / 256 : 4096;
-    lora_down_sum_kernel<<<(unsigned)blocks, 256, 0, st>>>(part, ks, stride, count, coef, xa);
-    return cudaGetLastError();
-}
-
 
 bool lora_cluster_ok(const void *W, int64_t K, int64_t ldw, int block, const float *A, int rank, const void *q) {
     if (rank < 1 || rank > kLoraMaxRank || block > 256) return false;
