@@ -217,7 +217,8 @@ CONVROT_API size_t convrot_linear_fwd_noalloc_max_bytes(void);
 
 /* -------------------------------------------------------- frozen backward -- */
 
-/* Bytes of workspace convrot_prepare_bwd_weight needs ([K, N] pairs of fp32). */
+/* Bytes of workspace convrot_prepare_bwd_weight needs: two 32-bit words per
+ * column of W_eff^T (K), cleared and used by the call. */
 CONVROT_API size_t convrot_bwd_weight_workspace_bytes(int64_t N, int64_t K);
 
 /* One-off preparation of the int8 backward weight (guide 7.1 and 4.1: the
@@ -225,8 +226,10 @@ CONVROT_API size_t convrot_bwd_weight_workspace_bytes(int64_t N, int64_t K);
  * GEMM as the forward; PR #2461 Summary: the base is frozen, so only grad_x).  The GEMM is reused
  * unchanged, so its weight operand must be a ConvRot quantization along the
  * new contraction dimension N:
- *   W_eff    = (scale_w (.) Wq) R      (the dequantized base in the original basis, kept as
- *              double-float pairs, ~48 significant bits)
+ *   W_eff    = (scale_w (.) Wq) R      (the dequantized base in the original basis; every
+ *              rotated value is the fp32 rounding of the exact one, decided in fp32 where it
+ *              is far from a rounding boundary and in double-float arithmetic, about 48
+ *              significant bits, near one)
  *   WtQ      out int8 [K, N]: codes of the rows of W_eff^T rotated along N
  *   scale_wt out fp32 [K]
  * N and K multiples of block and of 16; workspace >= convrot_bwd_weight_workspace_bytes. */

@@ -16,8 +16,9 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libconvrot.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 SOURCES = ["rotq.cu", "rotq_wide.cu", "lora_rotq.cu", "bwd_prep.cu", "bwd_r2.cu", "gemm_tc.cu", "convrot_api.cu",
-           "noalloc.cu", "selftest.cu", "peak_probe.cu", "lora_down.cu"]
-HEADERS = ["common.cuh", "fwht.cuh", "mbar.cuh", "wide.cuh", "internal.h", "launch_cache.h", "tcgen05.cuh"]
+           "noalloc.cu", "selftest.cu", "peak_probe.cu", "lora_down.cu",
+           "bwd_weight.cu"]
+HEADERS = ["common.cuh", "fwht.cuh", "mbar.cuh", "wide.cuh", "internal.h", "launch_cache.h", "tcgen05.cuh", "dfloat.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

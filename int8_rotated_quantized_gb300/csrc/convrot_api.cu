@@ -267,7 +267,7 @@ int convrot_linear_fwd_lora(const uint16_t *x, int64_t M, int64_t K, const int8_
 
 size_t convrot_bwd_weight_workspace_bytes(int64_t N, int64_t K) {
     if (N < 0 || K < 0) return 0;
-    return align256((size_t)N * (size_t)K * 2 * sizeof(float));
+    return align256(convrot::bwd_weight_work_bytes(N, K));
 }
 
 int convrot_prepare_bwd_weight(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K, int block, int8_t *WtQ,

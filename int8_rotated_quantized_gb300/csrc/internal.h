@@ -31,7 +31,9 @@ cudaError_t launch_lookup_wide(const int64_t *ids, int64_t n, const int8_t *Eq, 
 cudaError_t launch_emb_lookup(const int64_t *ids, int64_t n, const int8_t *Eq, const float *scale_e, int64_t V,
                               int64_t D, int block, uint16_t *out, unsigned *err, cudaStream_t st);
 
-// One-off int8 backward weight (bwd_prep.cu); `work` holds K * N pairs of fp32.
+// One-off int8 backward weight (bwd_weight.cu); `work` holds
+// bwd_weight_work_bytes(N, K) bytes (per-tile column maxima and bounds).
+size_t bwd_weight_work_bytes(int64_t N, int64_t K);
 cudaError_t launch_bwd_prep_df(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K, int block, void *work,
                                int8_t *WtQ, float *scale_wt, cudaStream_t st);
 

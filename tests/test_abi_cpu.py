@@ -55,7 +55,8 @@ def test_workspace_sizes(L):
     assert L.convrot_act_workspace_bytes(4096, 4096) == 4096 * 4096 * 2 + 4096 * 4
     assert L.convrot_act_workspace_bytes(3, 16) % 256 == 0
     assert L.convrot_act_workspace_bytes(3, 16) >= 3 * 16 * 2 + 3 * 4
-    assert L.convrot_bwd_weight_workspace_bytes(16384, 4096) == 16384 * 4096 * 8
+    # two words per column of the backward weight, 256-aligned
+    assert L.convrot_bwd_weight_workspace_bytes(16384, 4096) == 2 * 4096 * 4
     assert L.convrot_gemm_s32_workspace_bytes(64, 256) == 64 * 256 * 2
     assert L.convrot_act_workspace_bytes(-1, 4) == 0
 

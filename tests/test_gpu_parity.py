@@ -384,9 +384,11 @@ def test_linear_fwd_ragged_multi_tile():
 # ------------------------------------------------------------------ backward
 
 
-@pytest.mark.parametrize("block", [32, 128])
-def test_bwd_prep_and_grad_x_parity(block):
-    M, K, N = 150, 256, 768
+@pytest.mark.parametrize("block,K,N", [(32, 256, 768), (128, 256, 768), (16, 48, 400), (8, 80, 272), (64, 192, 320),
+                                       (256, 512, 512)])
+def test_bwd_prep_and_grad_x_parity(block, K, N):
+    """Tiles of 128 (or b) weight rows and columns, ragged in both, every block size."""
+    M = 150
     W = synth.normal_bf16(9, synth.STREAM_W, N, K, 0.02)
     wq, sw = oracle.quantize_weight(W, block)
     wtq_ref, swt_ref = oracle.prepare_bwd_weight(wq, sw, block)
@@ -418,7 +420,7 @@ def _check_bf16_sums(got_bits, ref_bits, K):
     assert rel_fro(g, r) <= REL_FRO_ORACLE
 
 
-@pytest.mark.parametrize("N,K,block", [(80, 256, 32), (192, 1024, 128), (16, 512, 256), (64, 64, 8)])
+@pytest.mark.parametrize("N,K,block", [(80, 256, 32), (192, 1024, 128), (16, 512, 256), (64, 64, 8), (48, 48, 16)])
 def test_dequant_weight_t_parity(N, K, block):
     W = synth.normal_bf16(15, synth.STREAM_W, N, K, 0.02)
     wq, sw = oracle.quantize_weight(W, block)
