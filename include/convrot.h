@@ -143,8 +143,11 @@ CONVROT_API size_t convrot_act_workspace_bytes(int64_t M, int64_t K);
  * scales plus a transient fp16 copy of the weight codes, [N, K] (see below). */
 CONVROT_API size_t convrot_linear_workspace_bytes(int64_t M, int64_t K, int64_t N);
 
-/* Forward of the ConvRot INT8 linear layer: convrot_quantize_activation into
- * `workspace`, then the int8 GEMM with the dequantization epilogue.  x bf16
+/* Forward of the ConvRot INT8 linear layer (guide 7.1: online activation
+ * rotation and dynamic per-row int8 quantization fused with the int8 matmul
+ * and its dequantization; PR #2461 Summary on convrot_int8_kernels.py):
+ * convrot_quantize_activation into `workspace`, then the int8 GEMM with the
+ * dequantization epilogue.  x bf16
  * [M, K] contiguous; y bf16 [M, N]; workspace device memory of at least
  * convrot_act_workspace_bytes(M, K), 256-byte aligned.  With at least
  * convrot_linear_workspace_bytes(M, K, N) bytes the weight codes are first
@@ -237,7 +240,9 @@ CONVROT_API int convrot_prepare_bwd_weight(const int8_t *Wq, const float *scale_
                                int block, int8_t *WtQ, float *scale_wt, void *workspace,
                                size_t ws_bytes, convrot_stream_t stream);
 
-/* Input gradient of the frozen layer through the int8 GEMM:
+/* Input gradient of the frozen layer through the int8 GEMM (guide 4.1 and 7.1:
+ * the opt-in int8 backward reuses the fused int8 GEMM for grad_x; PR #2461
+ * Summary: frozen base, so only the input gradient):
  *   dX = bf16( acc * scale_dy[m] * scale_wt[k] ),  acc = quant(dY R_N) . WtQ^T
  *   dY bf16 [M, N]; WtQ int8 [K, N]; scale_wt fp32 [K]; dX out bf16 [M, K];
  *   workspace >= convrot_act_workspace_bytes(M, N). */
