@@ -60,7 +60,8 @@ typedef enum {
     CONVROT_ERR_UNSUPPORTED = 2,   /* no sm_100-family GPU, or size beyond a limit */
     CONVROT_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
     CONVROT_ERR_TIMEOUT = 4,       /* a device-side pipeline wait hit its limit */
-    CONVROT_ERR_INDEX = 5          /* an embedding id was outside [0, V) */
+    CONVROT_ERR_INDEX = 5,         /* an embedding id was outside [0, V) */
+    CONVROT_ERR_BOUNDS = 6         /* checked builds only: a kernel's access left its tensor (skipped) */
 } convrot_status;
 
 /* Longest row the rotate-and-quantize kernels accept (elements). */
@@ -76,7 +77,11 @@ CONVROT_API int convrot_version(void);
 
 /* Synchronises `stream`, then reports and clears the device error word:
  * CONVROT_ERR_INDEX / CONVROT_ERR_TIMEOUT if a kernel recorded one since the
- * last call, CONVROT_ERR_CUDA if the stream itself failed, else CONVROT_OK. */
+ * last call, CONVROT_ERR_CUDA if the stream itself failed, else CONVROT_OK.
+ * The checked variant of the library (libconvrot_checked, built with
+ * -DCONVROT_CHECKED) checks the index of the kernels' global-memory accesses
+ * against their tensors' extents, skips any that falls outside, and reports
+ * it here first as CONVROT_ERR_BOUNDS; the release library has no such checks. */
 CONVROT_API int convrot_get_error(convrot_stream_t stream);
 
 /* ---------------------------------------------------------------- weights -- */
@@ -328,6 +333,14 @@ CONVROT_API int convrot_gemm_s32(const int8_t *A, const int8_t *B, int64_t M, in
  * the next convrot_get_error() returns CONVROT_ERR_TIMEOUT and the context
  * remains usable.  (The GEMM's own waits use a 2 s limit.) */
 CONVROT_API int convrot_selftest_wait_timeout(uint64_t limit_ns, convrot_stream_t stream);
+
+/* Test entry for the checked variant's reporting path: launches one thread
+ * that evaluates a bounds check with an index one past its extent.  No memory
+ * is read or written by it.  In the checked library the next
+ * convrot_get_error() returns CONVROT_ERR_BOUNDS (and clears it); the release
+ * library compiles its checks away, so there the call returns
+ * CONVROT_ERR_UNSUPPORTED and launches nothing. */
+CONVROT_API int convrot_selftest_bounds_flag(convrot_stream_t stream);
 
 /* Measurement entry for a roofline denominator: launches a kernel of four
  * 256-thread CTAs per SM whose warps issue only dense int8 MMAs through the

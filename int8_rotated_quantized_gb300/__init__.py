@@ -18,9 +18,10 @@ import torch
 from . import _build
 
 _lock = threading.Lock()
-_lib = None
+_libs = {}               # variant -> loaded CDLL
+_variant = "release"     # "release" or "checked" (bounds-checked kernels)
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_INDEX = range(6)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_INDEX, ERR_BOUNDS = range(7)
 
 
 class ConvRotError(RuntimeError):
@@ -29,16 +30,28 @@ class ConvRotError(RuntimeError):
         super().__init__(f"{where}: {status_string(status)}")
 
 
-def library_path() -> str:
-    return _build.LIB_PATH
+def library_path(variant: str = "release") -> str:
+    return _build.CHECKED_LIB_PATH if variant == "checked" else _build.LIB_PATH
+
+
+def select_library(variant: str) -> str:
+    """Route every call of this module to the release library or to its checked
+    variant (every kernel access checked against its tensor, CONVROT_ERR_BOUNDS on
+    a violation).  Returns the previous choice."""
+    global _variant
+    if variant not in ("release", "checked"):
+        raise ValueError(variant)
+    with _lock:
+        prev, _variant = _variant, variant
+    return prev
 
 
 def lib():
     """The loaded shared library (ctypes), with argument types declared."""
-    global _lib
     with _lock:
+        _lib = _libs.get(_variant)
         if _lib is None:
-            path = library_path()
+            path = library_path(_variant)
             if not os.path.exists(path):
                 raise RuntimeError(f"libconvrot is not built ({path} missing); call "
                                    "int8_rotated_quantized_gb300._build.build() first")
@@ -72,6 +85,7 @@ def lib():
                 "convrot_linear_fwd_noalloc": ([P, I64, I64, P, P, I64, I, P, P, P], I),
                 "convrot_linear_fwd_noalloc_max_bytes": ([], S),
                 "convrot_selftest_wait_timeout": ([ctypes.c_uint64, P], I),
+                "convrot_selftest_bounds_flag": ([P], I),
                 "convrot_probe_mma_s8_rate": ([I, P, S, ctypes.POINTER(ctypes.c_double), P], I),
                 "convrot_selftest_gemm_fault": ([I, P, P, I64, I64, P, P, I64, P, ctypes.c_uint64, I64, I, P], I),
             }
@@ -81,7 +95,7 @@ def lib():
                 fn.restype = res
             L.convrot_status_string.argtypes = [I]
             L.convrot_status_string.restype = ctypes.c_char_p
-            _lib = L
+            _libs[_variant] = _lib = L
     return _lib
 
 

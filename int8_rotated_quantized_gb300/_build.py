@@ -14,6 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libconvrot.so")
+# The same sources with -DCONVROT_CHECKED: every instrumented kernel access is checked against its tensor.
+CHECKED_LIB_PATH = os.path.join(OUT_DIR, "libconvrot_checked.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 SOURCES = ["rotq.cu", "rotq_wide.cu", "lora_rotq.cu", "bwd_prep.cu", "bwd_r2.cu", "gemm_tc.cu", "convrot_api.cu",
            "noalloc.cu", "selftest.cu", "peak_probe.cu", "lora_down.cu",
@@ -33,23 +35,27 @@ def _nvcc() -> str:
     return cand if os.path.exists(cand) else "nvcc"
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(path: str) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(INCLUDE, "convrot.h"), __file__]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not _stale():
+    """Builds the release library and its checked variant (all objects compiled in parallel)."""
+    targets = [(LIB_PATH, [], ""), (CHECKED_LIB_PATH, ["-DCONVROT_CHECKED"], "_checked")]
+    todo = [t for t in targets if force or _stale(t[0])]
+    if not todo:
         return LIB_PATH
     os.makedirs(OUT_DIR, exist_ok=True)
     nvcc = _nvcc()
 
-    def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + ".o")
-        cmd = [nvcc, *NVCC_FLAGS, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(job):
+        src, flags, suffix = job
+        obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + suffix + ".o")
+        cmd = [nvcc, *NVCC_FLAGS, *flags, "-I", INCLUDE, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -57,14 +63,17 @@ def build(force: bool = False, verbose: bool = False) -> str:
             print(r.stderr)
         return obj
 
-    with concurrent.futures.ThreadPoolExecutor(len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", *objs, "-o", tmp, "-lcudart"]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
+    jobs = [(src, flags, suffix) for _, flags, suffix in todo for src in SOURCES]
+    with concurrent.futures.ThreadPoolExecutor(min(len(jobs), os.cpu_count() or 8)) as ex:
+        objs = list(ex.map(compile_one, jobs))
+    for i, (path, _, _) in enumerate(todo):
+        mine = objs[i * len(SOURCES):(i + 1) * len(SOURCES)]
+        tmp = path + f".tmp{os.getpid()}"
+        cmd = [nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", *mine, "-o", tmp, "-lcudart"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, path)
     return LIB_PATH
 
 

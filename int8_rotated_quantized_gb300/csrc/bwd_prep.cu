@@ -73,9 +73,11 @@ __global__ void __launch_bounds__(512) dequant_t_kernel(const int8_t *Wq, const 
     const bool ok = n < N && k0 + 32 * c < K;
     uint32_t w[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     float s = 0.f;
-    if (ok) {  // K is a multiple of 16: the second 16 codes may lie past the row
+    if (ok && CR_SPAN(n * K + k0 + 32 * c, 16, N * K)) {  // K is a multiple of 16: the second 16 codes may lie past the row
         const uint4 *src = reinterpret_cast<const uint4 *>(Wq + n * K + k0 + 32 * c);
-        const uint4 v0 = __ldg(src), v1 = k0 + 32 * c + 16 < K ? __ldg(src + 1) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 v0 = __ldg(src);
+        const uint4 v1 = k0 + 32 * c + 16 < K && CR_SPAN(n * K + k0 + 32 * c + 16, 16, N * K) ? __ldg(src + 1)
+                                                                                                : make_uint4(0u, 0u, 0u, 0u);
         w[0] = v0.x, w[1] = v0.y, w[2] = v0.z, w[3] = v0.w, w[4] = v1.x, w[5] = v1.y, w[6] = v1.z, w[7] = v1.w;
         s = __ldg(scale_w + n);
     }
@@ -132,10 +134,11 @@ __global__ void __launch_bounds__(512) dequant_t_kernel(const int8_t *Wq, const 
         const int64_t nn = n0 + 8 * g;
         uint16_t *dst = T + (k0 + kl) * N + nn;
         if (nn + 8 <= N) {
-            *reinterpret_cast<uint4 *>(dst) = v;
+            if (CR_SPAN((k0 + kl) * N + nn, 8, K * N)) *reinterpret_cast<uint4 *>(dst) = v;
         } else {
             const uint32_t q[4] = {v.x, v.y, v.z, v.w};
-            for (int j = 0; j < 8 && nn + j < N; ++j) dst[j] = (uint16_t)(q[j >> 1] >> (16 * (j & 1)));
+            for (int j = 0; j < 8 && nn + j < N; ++j)
+                if (CR_SPAN((k0 + kl) * N + nn + j, 1, K * N)) dst[j] = (uint16_t)(q[j >> 1] >> (16 * (j & 1)));
         }
     }
 }

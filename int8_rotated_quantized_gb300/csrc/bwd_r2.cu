@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) scaleq_kernel(const 
     for (int i = threadIdx.x; i < S * 8 * G; i += blockDim.x) {
         const int s = i / (8 * G), v = (i / G) & 7, tt = i % G;
         const int64_t c = (int64_t)s * G + tt;
-        cs_s[i] = c < chunks ? __ldg(reinterpret_cast<const float4 *>(colscale + 32 * c) + v)
+        cs_s[i] = c < chunks && CR_SPAN(32 * c + 4 * v, 4, L) ? __ldg(reinterpret_cast<const float4 *>(colscale + 32 * c) + v)
                              : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     __syncthreads();
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) scaleq_kernel(const 
 #pragma unroll
         for (int s = 0; s < S; ++s) {
             const int64_t c = (int64_t)s * G + t;
-            if (c < chunks && row < rows) {
+            if (c < chunks && row < rows && CR_SPAN(row * L + 32 * c, 32, rows * L)) {
                 ld256(x + row * L + 32 * c, raw[s]);
                 ld256(x + row * L + 32 * c + 16, raw[s] + 8);
             } else {
@@ -99,11 +99,11 @@ __global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) scaleq_kernel(const 
         for (int w = 0; w < wpg; ++w) m = fmaxf(m, red[par][g * wpg + w]);
         if (row < rows) {
             const float inv = m > 0.f ? __fdiv_rn(127.f, m) : 0.f;
-            if (t == 0) scale[row] = __fdiv_rn(m, 127.f);
+            if (t == 0 && CR_SPAN(row, 1, rows)) scale[row] = __fdiv_rn(m, 127.f);
 #pragma unroll
             for (int s = 0; s < S; ++s) {
                 const int64_t c = (int64_t)s * G + t;
-                if (c < chunks) store_codes32(e[s], inv, q + row * L + 32 * c);
+                if (c < chunks && CR_SPAN(row * L + 32 * c, 32, rows * L)) store_codes32(e[s], inv, q + row * L + 32 * c);
             }
         }
     }
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(256) transpose_widen_kernel(const int8_t *W, i
         const int r = t >> 2, c = (t & 3) * 16;  // row n0 + r, columns k0 + c .. + 15
         const int64_t n = n0 + r;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (n < N && k0 + c < K) v = __ldg(reinterpret_cast<const uint4 *>(W + n * K + k0 + c));
+        if (n < N && k0 + c < K && CR_SPAN(n * K + k0 + c, 16, N * K)) v = __ldg(reinterpret_cast<const uint4 *>(W + n * K + k0 + c));
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 16; ++i) tile[r][c + i] = (int)(int8_t)((w[i >> 2] >> (8 * (i & 3))) & 0xff);
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(256) transpose_widen_kernel(const int8_t *W, i
     __syncthreads();
     const int r = t >> 2, c = (t & 3) * 16;  // output row k0 + r, columns n0 + c .. + 15
     const int64_t k = k0 + r;
-    if (k < K && n0 + c < N) {
+    if (k < K && n0 + c < N && CR_SPAN(k * N + n0 + c, 16, K * N)) {
         uint32_t o[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kThreads) rot_rows_f32_kernel(const float *P, 
         for (int s = 0; s < S; ++s) {
             const int64_t c = (int64_t)s * G + t;
             float e[32];
-            if (c < chunks && row < rows) {
+            if (c < chunks && row < rows && CR_SPAN(row * L + 32 * c, 32, rows * L)) {
                 uint32_t raw[32];
 #pragma unroll
                 for (int v = 0; v < 4; ++v) ld256(P + row * L + 32 * c + 8 * v, raw + 8 * v);
@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kThreads) rot_rows_f32_kernel(const float *P, 
                 for (int i = 0; i < 32; ++i) e[i] = 0.f;
             }
             fwht32<LOGB>(e, lane);
-            if (c < chunks && row < rows) {
+            if (c < chunks && row < rows && CR_SPAN(row * L + 32 * c, 32, rows * L)) {
                 uint32_t w[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {

@@ -241,9 +241,10 @@ __global__ void __launch_bounds__(kWtThreads, WtShape<LOGB>::T == 128 ? 2 : 1) w
             const uint4 *src = reinterpret_cast<const uint4 *>(qs + (buf * T + r) * QROW + 32 * c);
             const uint4 v0 = src[0], v1 = src[1];
             w[0] = v0.x, w[1] = v0.y, w[2] = v0.z, w[3] = v0.w, w[4] = v1.x, w[5] = v1.y, w[6] = v1.z, w[7] = v1.w;
-        } else if (n < N && k < K) {  // K is a multiple of 16: the second 16 codes may lie past the row
+        } else if (n < N && k < K && CR_SPAN(n * K + k, 16, N * K)) {  // K is a multiple of 16: the second 16 codes may lie past the row
             const uint4 *src = reinterpret_cast<const uint4 *>(Wq + n * K + k);
-            const uint4 v0 = __ldg(src), v1 = k + 16 < K ? __ldg(src + 1) : make_uint4(0u, 0u, 0u, 0u);
+            const uint4 v0 = __ldg(src);
+            const uint4 v1 = k + 16 < K && CR_SPAN(n * K + k + 16, 16, N * K) ? __ldg(src + 1) : make_uint4(0u, 0u, 0u, 0u);
             w[0] = v0.x, w[1] = v0.y, w[2] = v0.z, w[3] = v0.w, w[4] = v1.x, w[5] = v1.y, w[6] = v1.z, w[7] = v1.w;
         }
         float e[32];
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(kWtThreads, WtShape<LOGB>::T == 128 ? 2 : 1) w
             *reinterpret_cast<uint16_t *>(et + kk * (2 * T) + (((r >> 3) ^ et_swz<LPR>(kk)) << 4) + ((r & 7) << 1)) =
                 (uint16_t)(__float_as_uint(e[i]) & 0xffffu);
         }
-        if (!PF && c == 0) ss[r] = n < N ? __ldg(scale_w + n) : 0.f;
+        if (!PF && c == 0) ss[r] = n < N && CR_SPAN(n, 1, N) ? __ldg(scale_w + n) : 0.f;
     }
     __syncthreads();
 
@@ -303,7 +304,7 @@ __global__ void __launch_bounds__(kWtThreads, WtShape<LOGB>::T == 128 ? 2 : 1) w
             for (int s2 = 1; s2 < LPR; s2 <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s2));
             // raise the column's lower bound; does this tile's upper bound still reach it?
             bool need = false;
-            if (c == 0 && k < K) {
+            if (c == 0 && k < K && CR_SPAN(k, 1, K)) {
                 const float mine = fmaxf(mx - delta, 0.f);
                 const float cur = fmaxf(__uint_as_float(atomicMax(lb + k, __float_as_uint(mine))), mine);
                 need = mx + delta >= cur && mx + delta > 0.f;
@@ -331,11 +332,11 @@ __global__ void __launch_bounds__(kWtThreads, WtShape<LOGB>::T == 128 ? 2 : 1) w
             }
 #pragma unroll
             for (int s2 = 1; s2 < LPR; s2 <<= 1) ex = fmaxf(ex, __shfl_xor_sync(0xffffffffu, ex, s2));
-            if (need && c == 0) atomicMax(m + k, __float_as_uint(ex));
+            if (need && c == 0 && CR_SPAN(k, 1, K)) atomicMax(m + k, __float_as_uint(ex));
         } else {
-            const float mk = k < K ? __uint_as_float(__ldcg(m + k)) : 0.f;
+            const float mk = k < K && CR_SPAN(k, 1, K) ? __uint_as_float(__ldcg(m + k)) : 0.f;
             const float iv = mk > 0.f ? __fdiv_rn(127.f, mk) : 0.f;
-            if (tn == 0 && c == 0 && k < K) scale_wt[k] = __fdiv_rn(mk, scale_denom);
+            if (tn == 0 && c == 0 && k < K && CR_SPAN(k, 1, K)) scale_wt[k] = __fdiv_rn(mk, scale_denom);
             // |t - t_exact| <= delta * iv + 2^-22 (|u| iv <= 127 + delta iv) + 2^-16 (the fp32 roundings of t)
             const float margin = __fmaf_rn(delta, iv * 1.0000002f, 3.0517578125e-05f + 1.52587890625e-05f);
             const float thr = 0.5f - margin;  // a residual |t - rne(t)| >= thr is near a rounding boundary
@@ -384,7 +385,7 @@ __global__ void __launch_bounds__(kWtThreads, WtShape<LOGB>::T == 128 ? 2 : 1) w
         for (int idx = threadIdx.x; idx < T * (T / 16); idx += kWtThreads) {
             const int kk = idx / (T / 16), g = idx - kk * (T / 16);
             const int64_t k = k0 + kk, n = n0 + 16 * g;
-            if (k < K && n < N)
+            if (k < K && n < N && CR_SPAN(k * N + n, 16, K * N))
                 *reinterpret_cast<uint4 *>(WtQ + k * N + n) = *reinterpret_cast<const uint4 *>(ct + kk * T + 16 * g);
         }
     }

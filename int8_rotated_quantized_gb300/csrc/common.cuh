@@ -40,4 +40,37 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+// Checked builds (-DCONVROT_CHECKED, the library variant libconvrot_checked):
+// CR_IN_BOUNDS(cond) guards a global-memory access with the condition that its
+// index lies inside the logical tensor; a false condition records a failure
+// in this translation unit's device flag (reported by convrot_get_error as
+// CONVROT_ERR_BOUNDS) and the access is skipped.  Release builds compile the
+// condition away.
+#ifdef CONVROT_CHECKED
+void register_bounds_flag(unsigned (*read_and_clear)());
+static __device__ unsigned g_bounds_fail;
+#define CR_IN_BOUNDS(cond) ((cond) ? true : (atomicOr(&::convrot::g_bounds_fail, 1u), false))
+namespace {
+struct BoundsFlagRegistration {
+    BoundsFlagRegistration() { register_bounds_flag(&read_and_clear); }
+    static unsigned read_and_clear() {
+        unsigned v = 0;
+        if (cudaMemcpyFromSymbol(&v, g_bounds_fail, sizeof v) != cudaSuccess) return 0u;
+        if (v != 0u) {
+            const unsigned zero = 0u;
+            (void)cudaMemcpyToSymbol(g_bounds_fail, &zero, sizeof zero);
+        }
+        return v;
+    }
+};
+static BoundsFlagRegistration g_bounds_registration;
+}  // namespace
+#else
+#define CR_IN_BOUNDS(cond) true
+#endif
+// An access of `len` elements at element offset `off` of a buffer holding
+// `extent` elements.
+#define CR_SPAN(off, len, extent) \
+    CR_IN_BOUNDS((int64_t)(off) >= 0 && (int64_t)(off) + (int64_t)(len) <= (int64_t)(extent))
+
 }  // namespace convrot

@@ -51,6 +51,16 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? CONVROT_OK : CONVROT_ERR_CUDA; }
 
+#ifdef CONVROT_CHECKED
+// The bounds flags of the checked build, one per translation unit.
+std::mutex &bounds_mu() {
+    static std::mutex mu;
+    return mu;
+}
+unsigned (*g_bounds_readers[32])() = {nullptr};
+int g_bounds_count = 0;
+#endif
+
 #define CHECK(cond)                                   \
     do {                                              \
         if (!(cond)) return CONVROT_ERR_INVALID_ARG; \
@@ -69,6 +79,12 @@ int gemm_impl(const uint16_t *xq, const float *sx, int64_t M, int64_t K, const i
 }  // namespace
 
 namespace convrot {
+#ifdef CONVROT_CHECKED
+void register_bounds_flag(unsigned (*read_and_clear)()) {
+    std::lock_guard<std::mutex> lock(bounds_mu());
+    if (g_bounds_count < 32) g_bounds_readers[g_bounds_count++] = read_and_clear;
+}
+#endif
 unsigned *current_error_word() {
     unsigned *err = nullptr;
     return device_setup(&err) == CONVROT_OK ? err : nullptr;
@@ -85,6 +101,7 @@ const char *convrot_status_string(int status) {
         case CONVROT_ERR_CUDA: return "CONVROT_ERR_CUDA";
         case CONVROT_ERR_TIMEOUT: return "CONVROT_ERR_TIMEOUT";
         case CONVROT_ERR_INDEX: return "CONVROT_ERR_INDEX";
+        case CONVROT_ERR_BOUNDS: return "CONVROT_ERR_BOUNDS";
         default: return "CONVROT_ERR_UNKNOWN";
     }
 }
@@ -102,6 +119,14 @@ int convrot_get_error(convrot_stream_t stream) {
         const unsigned zero = 0;
         if (cudaMemcpy(err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return CONVROT_ERR_CUDA;
     }
+#ifdef CONVROT_CHECKED
+    unsigned bounds = 0u;
+    {
+        std::lock_guard<std::mutex> lock(bounds_mu());
+        for (int i = 0; i < g_bounds_count; ++i) bounds |= g_bounds_readers[i]();
+    }
+    if (bounds != 0u) return CONVROT_ERR_BOUNDS;
+#endif
     if (v & convrot::DEVERR_TIMEOUT) return CONVROT_ERR_TIMEOUT;
     if (v & convrot::DEVERR_INDEX) return CONVROT_ERR_INDEX;
     return CONVROT_OK;
@@ -430,6 +455,15 @@ int convrot_selftest_wait_timeout(uint64_t limit_ns, convrot_stream_t stream) {
     int rc = device_setup(&err);
     if (rc != CONVROT_OK) return rc;
     return cuda_status(convrot::launch_wait_timeout(limit_ns, err, (cudaStream_t)stream));
+}
+
+int convrot_selftest_bounds_flag(convrot_stream_t stream) {
+    unsigned *err = nullptr;
+    int rc = device_setup(&err);
+    if (rc != CONVROT_OK) return rc;
+    cudaError_t e;
+    if (!convrot::launch_bounds_flag_selftest((cudaStream_t)stream, &e)) return CONVROT_ERR_UNSUPPORTED;
+    return cuda_status(e);
 }
 
 }  // extern "C"

@@ -462,14 +462,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if constexpr (MODE == kModeDequantW16Lora) {
                 // y = acc * (sx * sw) + bias in place (the registers now hold fp32), then
                 // + the bypass chunk from TMEM (every thread of the half takes part)
-                const float swn = n < p.N ? __ldg(p.sb + n) : 0.f;
+                const float swn = n < p.N && CR_SPAN(n, 1, p.N) ? __ldg(p.sb + n) : 0.f;
                 const bool has_bias = p.bias != nullptr && n < p.N;
                 const float bn = has_bias ? bf16_bits_to_float(__ldg(p.bias + n)) : 0.f;
 #pragma unroll
                 for (int i4 = 0; i4 < 128; i4 += 4) {
                     float sx[4];
                     if (full) {
-                        const float4 v = __ldg(reinterpret_cast<const float4 *>(p.sa + m0 + i4));
+                        const float4 v = CR_SPAN(m0 + i4, 4, p.M) ? __ldg(reinterpret_cast<const float4 *>(p.sa + m0 + i4))
+                                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
                         sx[0] = v.x, sx[1] = v.y, sx[2] = v.z, sx[3] = v.w;
                     } else {
 #pragma unroll
@@ -503,7 +504,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (lane == 0) mbar_arrive(bar(L::BAR_ACC_EMPTY + buf));
                 ++g;
             }
-            if (n < p.N) {
+            // (checked builds: the column's rows m0 .. m0 + min(128, mlim) - 1 lie inside out [M, N])
+            if (n < p.N && (mlim <= 0 || CR_SPAN((int64_t)m0 * p.N + n, (int64_t)((full ? 128 : mlim) - 1) * p.N + 1,
+                                                 (int64_t)p.M * p.N))) {
                 if constexpr (MODE == kModeS32) {
                     int32_t *out = static_cast<int32_t *>(p.out) + (int64_t)m0 * p.N + n;
 #pragma unroll
@@ -517,7 +520,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     for (int i4 = 0; i4 < 128; i4 += 4) {
                         float sx[4];
                         if (full) {
-                            const float4 v = __ldg(reinterpret_cast<const float4 *>(p.sa + m0 + i4));
+                            const float4 v = CR_SPAN(m0 + i4, 4, p.M) ? __ldg(reinterpret_cast<const float4 *>(p.sa + m0 + i4))
+                                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
                             sx[0] = v.x, sx[1] = v.y, sx[2] = v.z, sx[3] = v.w;
                         } else {
 #pragma unroll
@@ -545,14 +549,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 } else {  // kModeDequant, kModeDequantW16
                     uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)m0 * p.N + n;
-                    const float swn = __ldg(p.sb + n);
+                    const float swn = CR_SPAN(n, 1, p.N) ? __ldg(p.sb + n) : 0.f;
                     const bool has_bias = p.bias != nullptr;
                     const float bn = has_bias ? bf16_bits_to_float(__ldg(p.bias + n)) : 0.f;
 #pragma unroll
                     for (int i4 = 0; i4 < 128; i4 += 4) {
                         float sx[4];
                         if (full) {
-                            const float4 v = __ldg(reinterpret_cast<const float4 *>(p.sa + m0 + i4));
+                            const float4 v = CR_SPAN(m0 + i4, 4, p.M) ? __ldg(reinterpret_cast<const float4 *>(p.sa + m0 + i4))
+                                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
                             sx[0] = v.x, sx[1] = v.y, sx[2] = v.z, sx[3] = v.w;
                         } else {
 #pragma unroll

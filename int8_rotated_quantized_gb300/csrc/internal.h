@@ -96,6 +96,9 @@ cudaError_t launch_gemm_fault_selftest(bool widened, const uint16_t *A, const fl
                                       const float *sb, int64_t M, int64_t N, int64_t K, uint16_t *out, unsigned *err,
                                       uint64_t limit_ns, int skip_it, int role, cudaStream_t st);
 
+// Self-test of the checked build's bounds flag (selftest.cu): false (nothing
+// launched) in release builds.
+bool launch_bounds_flag_selftest(cudaStream_t st, cudaError_t *e);
 // Self-test of the bounded-wait failure path (selftest.cu).
 cudaError_t launch_wait_timeout(uint64_t limit_ns, unsigned *err, cudaStream_t st);
 

@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(128) lora_down_tc_kernel(const __grid_constant
 #pragma unroll
         for (int i = 0; i < kDnN; ++i) v[i] = 0.f;
     }
-    if (m < M) {
+    if (m < M && CR_SPAN(((int64_t)blockIdx.y * M + m) * kDnN, kDnN, (int64_t)gridDim.y * M * kDnN)) {
         float4 *dst = reinterpret_cast<float4 *>(part + ((int64_t)blockIdx.y * M + m) * kDnN);
 #pragma unroll
         for (int i = 0; i < kDnN / 4; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
@@ -162,9 +162,10 @@ __global__ void lora_down_combine_kernel(const float *part, int spans, int64_t M
         float v = 0.f;
         for (int s = 0; s < spans; ++s) {
             const float *d = part + ((int64_t)s * M + m) * kDnN;
+            if (!CR_SPAN(((int64_t)s * M + m) * kDnN + j, 33, (int64_t)spans * M * kDnN)) continue;
             v = __fadd_rn(v, __fadd_rn(__fadd_rn(d[j], d[16 + j]), d[32 + j]));
         }
-        store_parts(xa_parts + m * kLoraPartsRow, j, __fmul_rn(coef, v));
+        if (CR_SPAN(m * kLoraPartsRow + j, 49, M * kLoraPartsRow)) store_parts(xa_parts + m * kLoraPartsRow, j, __fmul_rn(coef, v));
     }
 }
 
@@ -177,7 +178,8 @@ __global__ void lora_parts_kernel(const float *A, int64_t K, const float *B, int
         if (i < na) {
             const int j = (int)(i / K);
             const int64_t k = i - (int64_t)j * K;
-            const float v = j < rank ? A[(int64_t)j * K + k] : 0.f;
+            const float v = j < rank && CR_SPAN((int64_t)j * K + k, 1, (int64_t)rank * K) ? A[(int64_t)j * K + k] : 0.f;
+            if (!CR_SPAN((int64_t)(32 + j) * K + k, 1, 48 * K)) continue;
             const __nv_bfloat16 hi = __float2bfloat16_rn(v);
             const float r1 = __fsub_rn(v, __bfloat162float(hi));
             const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
@@ -188,7 +190,8 @@ __global__ void lora_parts_kernel(const float *A, int64_t K, const float *B, int
         } else {
             const int64_t t = i - na, n = t >> 4;
             const int j = (int)(t & 15);
-            store_parts(b_parts + n * kLoraPartsRow, j, j < rank ? B[n * rank + j] : 0.f);
+            if (!CR_SPAN(n * kLoraPartsRow + j, 49, N * kLoraPartsRow)) continue;
+            store_parts(b_parts + n * kLoraPartsRow, j, j < rank && CR_SPAN(n * rank + j, 1, N * rank) ? B[n * rank + j] : 0.f);
         }
     }
 }

@@ -158,8 +158,9 @@ __global__ void __launch_bounds__(512, 1) lora_rotq_kernel(const LoraArgs a) {
         const int nr = left < kRowsPerTile ? (int)left : kRowsPerTile;
         const uint32_t bar = smem_u32(&sh.bar[buf]);
         mbar_expect_tx(bar, slice_bytes * nr);
-        for (int r = 0; r < nr; ++r)
-            bulk_load(smem_u32(win + (buf * kRowsPerTile + r) * KS), a.W + (r0 + r) * a.ldw + k0, slice_bytes, bar);
+        for (int r = 0; r < nr; ++r)  // (checked builds: a skipped copy leaves the barrier to its bounded wait)
+            if (CR_SPAN((r0 + r) * a.ldw + k0, KS, (a.rows - 1) * a.ldw + a.K))
+                bulk_load(smem_u32(win + (buf * kRowsPerTile + r) * KS), a.W + (r0 + r) * a.ldw + k0, slice_bytes, bar);
     };
     const int64_t stride = gridDim.y;
     int64_t tile = blockIdx.y;
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(512, 1) lora_rotq_kernel(const LoraArgs a) {
 #pragma unroll
     for (int j = 0; j < RB; ++j) {
         ulonglong2 v = make_ulonglong2(0ull, 0ull);
-        if (j < a.rank) v = __ldg(reinterpret_cast<const ulonglong2 *>(a.A + (int64_t)j * a.K + k0 + 4 * t));
+        if (j < a.rank && CR_SPAN((int64_t)j * a.K + k0 + 4 * t, 4, (int64_t)a.rank * a.K)) v = __ldg(reinterpret_cast<const ulonglong2 *>(a.A + (int64_t)j * a.K + k0 + 4 * t));
         av[j][0] = v.x, av[j][1] = v.y;
     }
     const uint64_t cc = pack2(a.coef, a.coef);
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(512, 1) lora_rotq_kernel(const LoraArgs a) {
         for (int i = t; i < kRowsPerTile * RB; i += blockDim.x) {
             const int r = i / RB, j = i - r * RB;
             const int64_t br = r0 + r < a.rows ? r0 + r : a.rows - 1;
-            const float bv = j < a.rank ? __ldg(a.B + br * a.rank + j) : 0.f;
+            const float bv = j < a.rank && CR_SPAN(br * a.rank + j, 1, a.rows * a.rank) ? __ldg(a.B + br * a.rank + j) : 0.f;
             sh.bp[pb][r][j] = pack2(bv, bv);
         }
     };
@@ -278,8 +279,8 @@ __global__ void __launch_bounds__(512, 1) lora_rotq_kernel(const LoraArgs a) {
         const int64_t row = r0 + prow;
         if (row < a.rows) {
             const float inv = mx > 0.f ? __fdiv_rn(127.f, mx) : 0.f;
-            store_codes32(e, inv, a.q + row * a.K + k0 + 32 * pc);
-            if (crank == 0 && pc == 0) a.scale[row] = __fdiv_rn(mx, a.scale_denom);
+            if (CR_SPAN(row * a.K + k0 + 32 * pc, 32, a.rows * a.K)) store_codes32(e, inv, a.q + row * a.K + k0 + 32 * pc);
+            if (crank == 0 && pc == 0 && CR_SPAN(row, 1, a.rows)) a.scale[row] = __fdiv_rn(mx, a.scale_denom);
         }
     }
     if (!ok) {  // a wait gave up: let the copies already issued land before the CTA exits

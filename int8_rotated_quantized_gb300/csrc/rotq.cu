@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kMaxThreads) rotq_rows_kernel(const RotqArgs a
             for (int s = 0; s < S; ++s) {
                 const int64_t c = (int64_t)s * G + t;
                 const int64_t row = row0 + r;
-                if (c < chunks && row < a.rows)
+                if (c < chunks && row < a.rows && CR_SPAN(row * a.ldx + 8 * c, 8, (a.rows - 1) * a.ldx + a.K))
                     raw[r][s].load(x + row * a.ldx + 8 * c);
                 else
                     raw[r][s].zero();
@@ -281,12 +281,14 @@ __global__ void __launch_bounds__(kMaxThreads) rotq_rows_kernel(const RotqArgs a
 #pragma unroll 4
                 for (int j = 0; j < a.rank; ++j) {
                     const float4 *ap = reinterpret_cast<const float4 *>(a.lora_A + (int64_t)j * a.K + 8 * c);
-                    float4 a0 = __ldg(ap), a1 = __ldg(ap + 1);
+                    const bool a_ok = CR_SPAN((int64_t)j * a.K + 8 * c, 8, (int64_t)a.rank * a.K);
+                    float4 a0 = a_ok ? __ldg(ap) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    float4 a1 = a_ok ? __ldg(ap + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
                     float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
                     for (int r = 0; r < RPT; ++r) {
                         const int64_t row = min(row0 + r, a.rows - 1);
-                        const float bj = __ldg(a.lora_B + row * a.rank + j);
+                        const float bj = CR_SPAN(row * a.rank + j, 1, a.rows * a.rank) ? __ldg(a.lora_B + row * a.rank + j) : 0.f;
 #pragma unroll
                         for (int i = 0; i < 8; ++i) d[r][i] = __fmaf_rn(bj, av[i], d[r][i]);
                     }
@@ -332,7 +334,7 @@ __global__ void __launch_bounds__(kMaxThreads) rotq_rows_kernel(const RotqArgs a
             const float inv = amax_f > 0.f ? __fdiv_rn(127.f, amax_f) : 0.f;
             // scale = amax_u / (127 sqrt(b)); fp32 on the hot path (fp64 issue
             // is scarce on this GPU), fp64 in the fp64 variant.
-            if (t == 0) {
+            if (t == 0 && CR_SPAN(row, 1, a.rows)) {
                 if constexpr (sizeof(CT) == 4)
                     a.scale[row] = __fdiv_rn(amax_f, a.scale_denom);
                 else
@@ -342,7 +344,7 @@ __global__ void __launch_bounds__(kMaxThreads) rotq_rows_kernel(const RotqArgs a
 #pragma unroll
             for (int s = 0; s < S; ++s) {
                 const int64_t c = (int64_t)s * G + t;
-                if (c >= chunks) continue;
+                if (c >= chunks || !CR_SPAN(row * a.K + 8 * c, 8, a.rows * a.K)) continue;
                 if constexpr (sizeof(CT) == 4) {
                     quant_store(e[r][s], inv, qrow + 8 * c);
                 } else {
@@ -424,11 +426,11 @@ __global__ void __launch_bounds__(kMaxThreads) emb_lookup_kernel(const int64_t *
             const bool ok = tok < n && id >= 0 && id < V;
             if (tok < n && !ok && t == 0) atomicOr(err, DEVERR_INDEX);
             idv[r] = ok ? id : -1;
-            sc[r] = ok ? __ldg(scale_e + id) : 0.f;
+            sc[r] = ok && CR_SPAN(id, 1, V) ? __ldg(scale_e + id) : 0.f;
 #pragma unroll
             for (int sl = 0; sl < S; ++sl) {
                 const int64_t c = (int64_t)sl * G + t;
-                raw[r][sl] = (ok && c < chunks) ? __ldcs(reinterpret_cast<const uint2 *>(Eq + id * D + 8 * c))
+                raw[r][sl] = (ok && c < chunks && CR_SPAN(id * D + 8 * c, 8, V * D)) ? __ldcs(reinterpret_cast<const uint2 *>(Eq + id * D + 8 * c))
                                                 : make_uint2(0, 0);
             }
         }
@@ -471,7 +473,8 @@ __global__ void __launch_bounds__(kMaxThreads) emb_lookup_kernel(const int64_t *
                     __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
                     w[i] = *reinterpret_cast<uint32_t *>(&h);
                 }
-                __stcs(reinterpret_cast<uint4 *>(out + tok * D + 8 * c), make_uint4(w[0], w[1], w[2], w[3]));
+                if (CR_SPAN(tok * D + 8 * c, 8, n * D))
+                    __stcs(reinterpret_cast<uint4 *>(out + tok * D + 8 * c), make_uint4(w[0], w[1], w[2], w[3]));
             }
         }
     }
@@ -479,6 +482,7 @@ __global__ void __launch_bounds__(kMaxThreads) emb_lookup_kernel(const int64_t *
 
 __global__ void widen_i8_kernel(const int8_t *A, int64_t count8, __half *out) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < count8; i += (int64_t)gridDim.x * blockDim.x) {
+        if (!CR_SPAN(8 * i, 8, 8 * count8)) continue;
         uint2 v = __ldg(reinterpret_cast<const uint2 *>(A) + i);
         uint32_t w[2] = {v.x, v.y};
         int q[8];

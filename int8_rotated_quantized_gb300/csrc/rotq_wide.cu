@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) rotq_wide_kernel(con
 #pragma unroll
         for (int s = 0; s < S; ++s) {
             const int64_t c = (int64_t)s * G + t;
-            if (c < chunks && row < a.rows) {
+            if (c < chunks && row < a.rows && CR_SPAN(row * a.ldx + 32 * c, 32, (a.rows - 1) * a.ldx + a.K)) {
                 const uint16_t *p = a.x + row * a.ldx + 32 * c;
                 ld256(p, raw[s]);
                 ld256(p + 16, raw[s] + 8);
@@ -99,12 +99,12 @@ __global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) rotq_wide_kernel(con
         if (row < a.rows) {
             // fp32 decision on the fp32 transform; scale = amax_u / (127 sqrt(b)).
             const float inv = m > 0.f ? __fdiv_rn(127.f, m) : 0.f;
-            if (t == 0) a.scale[row] = __fdiv_rn(m, a.scale_denom);
+            if (t == 0 && CR_SPAN(row, 1, a.rows)) a.scale[row] = __fdiv_rn(m, a.scale_denom);
             OutT *qrow = static_cast<OutT *>(a.q) + row * a.K;
 #pragma unroll
             for (int s = 0; s < S; ++s) {
                 const int64_t c = (int64_t)s * G + t;
-                if (c < chunks) store_codes32(e[s], inv, qrow + 32 * c);
+                if (c < chunks && CR_SPAN(row * a.K + 32 * c, 32, a.rows * a.K)) store_codes32(e[s], inv, qrow + 32 * c);
             }
         }
     }
@@ -207,8 +207,9 @@ __global__ void __launch_bounds__(kThreads, 2) rotq_tma_kernel(const __grid_cons
         for (int w = 0; w < wpg; ++w) m = fmaxf(m, red[par][g * wpg + w]);
         if (row < a.rows) {
             const float inv = m > 0.f ? __fdiv_rn(127.f, m) : 0.f;
-            if (t == 0) a.scale[row] = __fdiv_rn(m, a.scale_denom);
-            if (t < chunks) store_codes32(e, inv, static_cast<OutT *>(a.q) + row * a.K + 32 * t);
+            if (t == 0 && CR_SPAN(row, 1, a.rows)) a.scale[row] = __fdiv_rn(m, a.scale_denom);
+            if (t < chunks && CR_SPAN(row * a.K + 32 * t, 32, a.rows * a.K))
+                store_codes32(e, inv, static_cast<OutT *>(a.q) + row * a.K + 32 * t);
         }
     }
     if (abort_flag && threadIdx.x == 0) {  // a wait gave up: give copies still in flight time to land
@@ -243,11 +244,11 @@ __global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) lookup_wide_kernel(c
         const int64_t tok = blk * groups + g;
         const bool ok = tok < n && id >= 0 && id < V;
         if (tok < n && !ok && t == 0) atomicOr(err, DEVERR_INDEX);
-        sc = ok ? __ldg(scale_e + id) : 0.f;
+        sc = ok && CR_SPAN(id, 1, V) ? __ldg(scale_e + id) : 0.f;
 #pragma unroll
         for (int s = 0; s < S; ++s) {
             const int64_t c = (int64_t)s * G + t;
-            if (ok && c < chunks) {
+            if (ok && c < chunks && CR_SPAN(id * D + 32 * c, 32, V * D)) {
                 ld256(Eq + id * D + 32 * c, raw[s]);
             } else {
 #pragma unroll
@@ -288,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) lookup_wide_kernel(c
                 __nv_bfloat162 h = __floats2bfloat162_rn(y0, y1);
                 w[i] = *reinterpret_cast<uint32_t *>(&h);
             }
+            if (!CR_SPAN(tok * D + 32 * c, 32, n * D)) continue;
             uint16_t *dst = out + tok * D + 32 * c;
             st256(dst, w);
             st256(dst + 16, w + 8);
@@ -299,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, S == 1 ? 2 : 1) lookup_wide_kernel(c
 // step (one 256-bit load, two 256-bit stores), grid-stride.
 __global__ void __launch_bounds__(kThreads) widen_codes_kernel(const int8_t *A, int64_t n32, uint16_t *out) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n32; i += (int64_t)gridDim.x * blockDim.x) {
+        if (!CR_SPAN(32 * i, 32, 32 * n32)) continue;
         uint32_t r[8];
         ld256(A + 32 * i, r);
         uint32_t w[16];

@@ -33,7 +33,7 @@ def test_header_declares_the_boundary():
                  "convrot_linear_workspace_bytes", "convrot_widen_codes", "convrot_gemm_dequant_w16",
                  "convrot_linear_fwd_lora", "convrot_linear_lora_workspace_bytes", "convrot_linear_bwd_x_r2",
                  "convrot_bwd_x_r2_workspace_bytes", "convrot_selftest_gemm_fault",
-                 "convrot_probe_mma_s8_rate"]:
+                 "convrot_probe_mma_s8_rate", "convrot_selftest_bounds_flag"]:
         assert must in names
 
 
@@ -42,11 +42,22 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, name), name
 
 
+def test_checked_variant_exports_every_declared_symbol(L):
+    """The bounds-checked build (-DCONVROT_CHECKED) is a drop-in replacement."""
+    assert os.path.exists(cr.library_path("checked"))
+    C = ctypes.CDLL(cr.library_path("checked"))
+    for name in declared_symbols():
+        assert hasattr(C, name), name
+    C.convrot_status_string.restype = ctypes.c_char_p
+    assert C.convrot_status_string(6) == b"CONVROT_ERR_BOUNDS"
+
+
 def test_status_strings_and_version(L):
     assert cr.status_string(0) == "CONVROT_OK"
     assert cr.status_string(1) == "CONVROT_ERR_INVALID_ARG"
     assert cr.status_string(4) == "CONVROT_ERR_TIMEOUT"
     assert cr.status_string(5) == "CONVROT_ERR_INDEX"
+    assert cr.status_string(6) == "CONVROT_ERR_BOUNDS"
     assert cr.status_string(99) == "CONVROT_ERR_UNKNOWN"
     assert L.convrot_version() >= 100
 
@@ -123,7 +134,7 @@ def test_null_and_misaligned_pointers_are_rejected(L):
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
-    monkeypatch.setattr(cr, "_lib", None)
-    monkeypatch.setattr(cr, "library_path", lambda: str(tmp_path / "missing.so"))
+    monkeypatch.setattr(cr, "_libs", {})
+    monkeypatch.setattr(cr, "library_path", lambda variant="release": str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         cr.lib()
