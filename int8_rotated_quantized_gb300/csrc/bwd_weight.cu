@@ -81,13 +81,7 @@ __device__ __forceinline__ int et_swz(int k) {
     return LPR == 4 ? (((k >> 5) & 3) | ((k & 1) << 2)) : ((k >> 5) & 7);
 }
 
-// (a0, a1) <- (a0 * b0, a1 * b1) and (q0, q1) <- (a0 * a0 + q0, a1 * a1 + q1), one rounding per lane.
-__device__ __forceinline__ void mul2v(float &a0, float &a1, float b0, float b1) {
-    asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%0, %1};\n mov.b64 rb, {%2, %3};\n"
-        " mul.rn.f32x2 ra, ra, rb;\n mov.b64 {%0, %1}, ra;\n}"
-        : "+f"(a0), "+f"(a1)
-        : "f"(b0), "f"(b1));
-}
+// (q0, q1) <- (a0 * a0 + q0, a1 * a1 + q1), one rounding per lane.
 __device__ __forceinline__ void sq2acc(float &q0, float &q1, float a0, float a1) {
     asm("{\n .reg .b64 rq, ra;\n mov.b64 rq, {%0, %1};\n mov.b64 ra, {%2, %3};\n"
         " fma.rn.f32x2 rq, ra, ra, rq;\n mov.b64 {%0, %1}, rq;\n}"

@@ -356,7 +356,7 @@ int convrot_dequant_weight_t(const int8_t *Wq, const float *scale_w, int64_t N, 
     int rc = device_setup(&err);
     if (rc != CONVROT_OK) return rc;
     if (N == 0) return CONVROT_OK;
-    return cuda_status(convrot::launch_dequant_t(Wq, scale_w, N, K, block, WeffT, (cudaStream_t)stream));
+    return cuda_status(convrot::launch_dequant_t(Wq, scale_w, N, K, block, WeffT, err, (cudaStream_t)stream));
 }
 
 int convrot_gemm_bf16(const uint16_t *A, int64_t M, int64_t K, const uint16_t *B, int64_t N, uint16_t *C,
@@ -390,7 +390,7 @@ int convrot_linear_bwd_x_bf16(const uint16_t *dY, int64_t M, int64_t N, const in
     if (M == 0 || N == 0) return CONVROT_OK;
     cudaStream_t st = (cudaStream_t)stream;
     uint16_t *weff_t = static_cast<uint16_t *>(workspace);
-    rc = cuda_status(convrot::launch_dequant_t(Wq, scale_w, N, K, block, weff_t, st));
+    rc = cuda_status(convrot::launch_dequant_t(Wq, scale_w, N, K, block, weff_t, err, st));
     if (rc != CONVROT_OK) return rc;
     // dX [M, K] = dY [M, N] . (WeffT [K, N])^T
     return cuda_status(convrot::launch_gemm_bf16(dY, weff_t, M, K, N, dX, err, st));

@@ -39,6 +39,14 @@ __device__ __forceinline__ void mul2c(float &e0, float &e1, float k) {
         : "f"(k));
 }
 
+// (a0, a1) <- (a0 * b0, a1 * b1), one rounding per lane.
+__device__ __forceinline__ void mul2v(float &a0, float &a1, float b0, float b1) {
+    asm("{\n .reg .b64 ra, rb;\n mov.b64 ra, {%0, %1};\n mov.b64 rb, {%2, %3};\n"
+        " mul.rn.f32x2 ra, ra, rb;\n mov.b64 {%0, %1}, ra;\n}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ void add2c(float &e0, float &e1, float c) {
     asm("{\n .reg .b64 rc, re;\n mov.b64 rc, {%2, %2};\n mov.b64 re, {%0, %1};\n"
         " add.rn.f32x2 re, re, rc;\n mov.b64 {%0, %1}, re;\n}"

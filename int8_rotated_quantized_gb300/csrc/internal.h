@@ -38,8 +38,9 @@ cudaError_t launch_bwd_prep_df(const int8_t *Wq, const float *scale_w, int64_t N
                                int8_t *WtQ, float *scale_wt, cudaStream_t st);
 
 // bf16-mode backward weight (bwd_prep.cu): T [K, N] bf16 = bf16((s_w (.) Wq) R)^T.
+// b <= 128 on the tensor cores (bounded waits; a timeout sets DEVERR_TIMEOUT in err).
 cudaError_t launch_dequant_t(const int8_t *Wq, const float *scale_w, int64_t N, int64_t K, int block, uint16_t *T,
-                             cudaStream_t st);
+                             unsigned *err, cudaStream_t st);
 
 cudaError_t launch_widen_i8(const int8_t *A, int64_t count, uint16_t *out, cudaStream_t st);
 
