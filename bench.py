@@ -44,8 +44,8 @@ L2_FLUSH_BYTES = 256 << 20
 #   python -m int8_rotated_quantized_gb300.profile_case gemm_bf16 --M 20480 --N 4096 --K 16384 --reps 3  (bf16 grad_x)
 # keyed by the hash of the kernel source they were taken on; reported as null
 # once the kernel source differs (or where no capture was taken on it).
-GEMM_TRAFFIC = {"source_sha256_16": "7527c16dc26a2d82", "fwd": 857039189 + 649365675, "bwd": 3195929429 + 160749312,
-                "bf16_bwd": None}
+GEMM_TRAFFIC = {"source_sha256_16": "c3d5002d190611ad", "fwd": 870010368 + 651447040, "bwd": 3196726272 + 162807040,
+                "bf16_bwd": 3195051520 + 162809088}
 
 
 def _gemm_source_current():
