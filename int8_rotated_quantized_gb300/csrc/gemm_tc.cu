@@ -103,9 +103,13 @@ struct Layout {
     static constexpr int OFF_W8 = OFF_X + XS * X_STAGE;
     static constexpr int OFF_WH = OFF_W8 + WS * W8_STAGE;
     static constexpr int OFF_BAR = OFF_WH + CS * WH_STAGE;
-    static constexpr int BAR_X_FULL = 0, BAR_X_EMPTY = XS, BAR_W_FULL = 2 * XS, BAR_W_EMPTY = BAR_W_FULL + WS,
-                         BAR_CONV_FULL = BAR_W_EMPTY + WS, BAR_CONV_EMPTY = BAR_CONV_FULL + CS,
-                         BAR_ACC_FULL = BAR_CONV_EMPTY + CS, BAR_ACC_EMPTY = BAR_ACC_FULL + 2,
+    // One full and one empty barrier per stage of the MMA's two operands (the
+    // activation ring and the fp16 weight ring advance together): the MMA
+    // thread waits once and frees a stage with one commit.  The int8 weight
+    // ring of the fused-widening modes has its own pair for the converters.
+    static_assert(XS == CS, "the two operand rings advance together");
+    static constexpr int BAR_FULL = 0, BAR_EMPTY = XS, BAR_W_FULL = 2 * XS, BAR_W_EMPTY = BAR_W_FULL + WS,
+                         BAR_ACC_FULL = BAR_W_EMPTY + WS, BAR_ACC_EMPTY = BAR_ACC_FULL + 2,
                          BAR_DRAIN = BAR_ACC_EMPTY + 2, NUM_BARS = BAR_DRAIN + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
@@ -207,17 +211,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < L::XS; ++i) {
-            mbar_init(bar(L::BAR_X_FULL + i), 1);
-            mbar_init(bar(L::BAR_X_EMPTY + i), 1);  // MMA commit
+            // the producer's expect_tx (both operands' bytes when the weight tiles
+            // come ready), plus the 4 converter warps in the fused-widening modes
+            mbar_init(bar(L::BAR_FULL + i), L::kDirect ? 1 : 5);
+            mbar_init(bar(L::BAR_EMPTY + i), 1);  // MMA commit
         }
         for (int i = 0; i < L::WS; ++i) {
             mbar_init(bar(L::BAR_W_FULL + i), 1);
             mbar_init(bar(L::BAR_W_EMPTY + i), 4);  // 4 converter warps
-        }
-        for (int i = 0; i < L::CS; ++i) {
-            // converted by the 4 converter warps, or (bf16 mode) loaded by TMA
-            mbar_init(bar(L::BAR_CONV_FULL + i), weight_direct(MODE) ? 1 : 4);
-            mbar_init(bar(L::BAR_CONV_EMPTY + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(L::BAR_ACC_FULL + i), 1);
@@ -250,19 +251,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (warp < 4) {
         regs_dec<REGS_WG0>();
-        if ((warp == 0 || warp == 2) && lane == 0) {
+        if ((warp == 0 || (warp == 2 && !L::kDirect)) && lane == 0) {
             // ---------------------------------------------------- producers
-            // warp 0 streams activation tiles (freed by the MMA), warp 2 the
-            // int8 weight tiles (freed by the converters), each in its own ring.
-            // In bf16 mode warp 2 loads the bf16 weight tiles straight into the
-            // ring the MMA reads (freed by the MMA).
+            // warp 0 streams the activation tiles and, in the modes whose weight
+            // tiles arrive ready (widened codes, bf16), the weight tile of the
+            // same stage onto the same barrier.  In the fused-widening modes warp
+            // 2 streams the int8 weight tiles into their own ring, freed by the
+            // converter warps.
             const bool is_x = warp == 0;
-            const bool w_direct = !is_x && weight_direct(MODE);
-            const int nst = is_x ? L::XS : w_direct ? L::CS : L::WS;
-            const int full0 = is_x ? L::BAR_X_FULL : w_direct ? L::BAR_CONV_FULL : L::BAR_W_FULL;
-            const int empty0 = is_x ? L::BAR_X_EMPTY : w_direct ? L::BAR_CONV_EMPTY : L::BAR_W_EMPTY;
-            const CUtensorMap *map = is_x ? &tmX : &tmW;
-            asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+            const int nst = is_x ? L::XS : L::WS;
+            const int full0 = is_x ? L::BAR_FULL : L::BAR_W_FULL;
+            const int empty0 = is_x ? L::BAR_EMPTY : L::BAR_W_EMPTY;
+            asm volatile("prefetch.tensormap [%0];" ::"l"(is_x ? &tmX : &tmW) : "memory");
+            if (is_x && L::kDirect) asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
             int it = 0, skipped = -1;
             bool ok = true;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
@@ -274,22 +275,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ok = false;
                         break;
                     }
-                    if (it == p.fault_skip_it && p.fault_role == (is_x ? 0 : 1)) {
-                        skipped = it;  // self-test: this stage is never filled
-                        continue;
-                    }
+                    // self-test: the named operand's copy of this stage is never issued
+                    const bool skip_x = it == p.fault_skip_it && p.fault_role == 0;
+                    const bool skip_w = it == p.fault_skip_it && p.fault_role == 1;
                     const bool extra = kExtra && kb == num_kb;  // bypass parts: 128 bytes per row
                     if (is_x) {
-                        mbar_expect_tx(bar(full0 + s), X_STAGE);
-                        tma_load_2d(sX + s * X_STAGE, extra ? &tmXA : map, bar(full0 + s), extra ? 0 : kb * BK,
-                                    tb * TT);
-                    } else if (w_direct) {
-                        mbar_expect_tx(bar(full0 + s), WH_STAGE);
-                        tma_load_2d(sWh + s * WH_STAGE, extra ? &tmLB : map, bar(full0 + s), extra ? 0 : kb * BK,
-                                    wb * TW);
+                        mbar_expect_tx(bar(full0 + s), X_STAGE + (L::kDirect ? WH_STAGE : 0));
+                        if (!skip_x)
+                            tma_load_2d(sX + s * X_STAGE, extra ? &tmXA : &tmX, bar(full0 + s), extra ? 0 : kb * BK,
+                                        tb * TT);
+                        if (L::kDirect && !skip_w)
+                            tma_load_2d(sWh + s * WH_STAGE, extra ? &tmLB : &tmW, bar(full0 + s),
+                                        extra ? 0 : kb * BK, wb * TW);
+                        if (skip_x || (L::kDirect && skip_w)) skipped = it;  // this stage never completes
                     } else {
+                        if (skip_w) {
+                            skipped = it;
+                            continue;
+                        }
                         mbar_expect_tx(bar(full0 + s), W8_STAGE);
-                        tma_load_2d(sW8 + s * W8_STAGE, map, bar(full0 + s), kb * BK, wb * TW);
+                        tma_load_2d(sW8 + s * W8_STAGE, &tmW, bar(full0 + s), kb * BK, wb * TW);
                     }
                 }
             }
@@ -316,10 +321,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tc_fence_after();
                         dcol = (uint32_t)(buf * TT);
                     }
-                    const int s = it % L::XS;
-                    const int c = it % L::CS;
-                    if (!mbar_wait(bar(L::BAR_X_FULL + s), (it / L::XS) & 1, abort_flag, p.err, p.wait_limit_ns) ||
-                        !mbar_wait(bar(L::BAR_CONV_FULL + c), (it / L::CS) & 1, abort_flag, p.err, p.wait_limit_ns)) {
+                    const int s = it % L::XS;  // stage of both operands
+                    if (!mbar_wait(bar(L::BAR_FULL + s), (it / L::XS) & 1, abort_flag, p.err, p.wait_limit_ns)) {
                         ok = false;
                         break;
                     }
@@ -331,21 +334,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         for (int q = 0; q < 6; ++q) {
                             const int pa = q == 0 ? 0 : q == 1 ? 0 : q == 2 ? 1 : q == 3 ? 0 : q == 4 ? 1 : 2;
                             const int pb = q == 0 ? 0 : q == 1 ? 1 : q == 2 ? 0 : q == 3 ? 2 : q == 4 ? 1 : 0;
-                            const uint64_t ad = sw128_desc(sWh + c * WH_STAGE + pa * 32);
+                            const uint64_t ad = sw128_desc(sWh + s * WH_STAGE + pa * 32);
                             const uint64_t bd = sw128_desc(sX + s * X_STAGE + pb * 32);
                             umma_f16(tmem + dcol, ad, bd, kIdescBF16, q > 0 ? 1u : 0u);
                         }
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < BK / 16; ++kk) {
-                            const uint64_t ad = sw128_desc(sWh + c * WH_STAGE + kk * 32);
+                            const uint64_t ad = sw128_desc(sWh + s * WH_STAGE + kk * 32);
                             const uint64_t bd = sw128_desc(sX + s * X_STAGE + kk * 32);
                             umma_f16(tmem + dcol, ad, bd, MODE == kModeBf16 ? kIdescBF16 : kIdescF16,
                                      (kc > 0 || kk > 0) ? 1u : 0u);
                         }
                     }
-                    umma_commit(bar(L::BAR_X_EMPTY + s));
-                    umma_commit(bar(L::BAR_CONV_EMPTY + c));
+                    umma_commit(bar(L::BAR_EMPTY + s));
                     if (extra || kc == chunk_kb - 1 || kb == num_kb - 1) {
                         umma_commit(bar(L::BAR_ACC_FULL + (g & 1)));
                         ++g;
@@ -374,7 +376,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int s = it % L::WS;
                 const int c = it % L::CS;
                 if (!warp_wait(bar(L::BAR_W_FULL + s), (it / L::WS) & 1, abort_flag, p.err, p.wait_limit_ns) ||
-                    !warp_wait(bar(L::BAR_CONV_EMPTY + c), ((it / L::CS) & 1) ^ 1, abort_flag, p.err, p.wait_limit_ns)) {
+                    !warp_wait(bar(L::BAR_EMPTY + c), ((it / L::CS) & 1) ^ 1, abort_flag, p.err, p.wait_limit_ns)) {
                     ok = false;
                     break;
                 }
@@ -407,7 +409,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(bar(L::BAR_W_EMPTY + s));
-                    mbar_arrive(bar(L::BAR_CONV_FULL + c));
+                    mbar_arrive(bar(L::BAR_FULL + c));  // the stage's weight operand is ready
                 }
             }
         }
