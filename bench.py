@@ -44,8 +44,8 @@ L2_FLUSH_BYTES = 256 << 20
 #   python -m int8_rotated_quantized_gb300.profile_case gemm_bf16 --M 20480 --N 4096 --K 16384 --reps 3  (bf16 grad_x)
 # keyed by the hash of the kernel source they were taken on; reported as null
 # once the kernel source differs (or where no capture was taken on it).
-GEMM_TRAFFIC = {"source_sha256_16": "c3d5002d190611ad", "fwd": 870010368 + 651447040, "bwd": 3196726272 + 162807040,
-                "bf16_bwd": 3195051520 + 162809088}
+GEMM_TRAFFIC = {"source_sha256_16": "15c2af51b3fd39d5", "fwd": 800396800 + 650350592, "bwd": 3196012032 + 162386432,
+                "bf16_bwd": 3195729408 + 162459904}
 
 
 def _gemm_source_current():
