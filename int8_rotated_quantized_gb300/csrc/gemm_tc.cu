@@ -191,6 +191,83 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
     return __all_sync(0xffffffffu, got);
 }
 
+// The epilogue's stores of one thread: weight row n, the 128 tokens m0 ..
+// m0 + 127 of its column half in acc (mlim of them exist; full: all 128).
+// Each store instruction of a warp writes 32 consecutive n of one row m.
+template <int MODE>
+__device__ __forceinline__ void epi_store(const int (&acc)[128], int n, int m0, int mlim, bool full,
+                                          const GemmArgs &p) {
+    // (checked builds: the column's rows m0 .. m0 + min(128, mlim) - 1 lie inside out [M, N])
+    if (n < p.N && (mlim <= 0 || CR_SPAN((int64_t)m0 * p.N + n, (int64_t)((full ? 128 : mlim) - 1) * p.N + 1,
+                                         (int64_t)p.M * p.N))) {
+        if constexpr (MODE == kModeS32) {
+            int32_t *out = static_cast<int32_t *>(p.out) + (int64_t)m0 * p.N + n;
+#pragma unroll
+            for (int i = 0; i < 128; ++i) {
+                if (full || i < mlim) *out = acc[i];
+                out += p.N;
+            }
+        } else if constexpr (MODE == kModeScaleF32) {
+            float *out = static_cast<float *>(p.out) + (int64_t)m0 * p.N + n;
+#pragma unroll
+            for (int i4 = 0; i4 < 128; i4 += 4) {
+                float sx[4];
+                if (full) {
+                    const float4 v = CR_SPAN(m0 + i4, 4, p.M) ? __ldg(reinterpret_cast<const float4 *>(p.sa + m0 + i4))
+                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                    sx[0] = v.x, sx[1] = v.y, sx[2] = v.z, sx[3] = v.w;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) sx[j] = i4 + j < mlim ? __ldg(p.sa + m0 + i4 + j) : 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    if (full || i4 + j < mlim) *out = __fmul_rn(__int2float_rn(acc[i4 + j]), sx[j]);
+                    out += p.N;
+                }
+            }
+        } else if constexpr (MODE == kModeBf16) {
+            uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)m0 * p.N + n;
+#pragma unroll
+            for (int i = 0; i < 128; ++i) {
+                if (full || i < mlim) *out = (uint16_t)float_to_bf16_bits(__int_as_float(acc[i]));
+                out += p.N;
+            }
+        } else if constexpr (MODE == kModeDequantW16Lora) {  // y (with the bypass) is in the registers
+            uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)m0 * p.N + n;
+#pragma unroll
+            for (int i = 0; i < 128; ++i) {
+                if (full || i < mlim) *out = (uint16_t)float_to_bf16_bits(__int_as_float(acc[i]));
+                out += p.N;
+            }
+        } else {  // kModeDequant, kModeDequantW16
+            uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)m0 * p.N + n;
+            const float swn = CR_SPAN(n, 1, p.N) ? __ldg(p.sb + n) : 0.f;
+            const bool has_bias = p.bias != nullptr;
+            const float bn = has_bias ? bf16_bits_to_float(__ldg(p.bias + n)) : 0.f;
+#pragma unroll
+            for (int i4 = 0; i4 < 128; i4 += 4) {
+                float sx[4];
+                if (full) {
+                    const float4 v = CR_SPAN(m0 + i4, 4, p.M) ? __ldg(reinterpret_cast<const float4 *>(p.sa + m0 + i4))
+                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+                    sx[0] = v.x, sx[1] = v.y, sx[2] = v.z, sx[3] = v.w;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) sx[j] = i4 + j < mlim ? __ldg(p.sa + m0 + i4 + j) : 0.f;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    float y = __fmul_rn(__int2float_rn(acc[i4 + j]), __fmul_rn(sx[j], swn));
+                    if (has_bias) y = __fadd_rn(y, bn);
+                    if (full || i4 + j < mlim) *out = (uint16_t)float_to_bf16_bits(y);
+                    out += p.N;
+                }
+            }
+        }
+    }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_s8_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
@@ -506,77 +583,269 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (lane == 0) mbar_arrive(bar(L::BAR_ACC_EMPTY + buf));
                 ++g;
             }
-            // (checked builds: the column's rows m0 .. m0 + min(128, mlim) - 1 lie inside out [M, N])
-            if (n < p.N && (mlim <= 0 || CR_SPAN((int64_t)m0 * p.N + n, (int64_t)((full ? 128 : mlim) - 1) * p.N + 1,
-                                                 (int64_t)p.M * p.N))) {
-                if constexpr (MODE == kModeS32) {
-                    int32_t *out = static_cast<int32_t *>(p.out) + (int64_t)m0 * p.N + n;
-#pragma unroll
-                    for (int i = 0; i < 128; ++i) {
-                        if (full || i < mlim) *out = acc[i];
-                        out += p.N;
+            epi_store<MODE>(acc, n, m0, mlim, full, p);
+        }
+        end_barrier();
+    }
+}
+
+
+// ----------------------------------------------------------- CTA-pair GEMM --
+// The modes whose weight tiles arrive ready (widened codes, bf16, the fp32-
+// scaled mode) on pairs of CTAs with the 2-SM MMA.  A pair (a cluster of two
+// CTAs on neighbouring SMs) computes 256 weight rows x 256 tokens: CTA r of
+// the pair holds, in every stage, weight rows 128 r .. 128 r + 127 (its half
+// of the MMA's A) and token rows 128 r .. 128 r + 127 (its half of B), so a
+// stage is 32 KB per SM instead of 48 and six stages are in flight.  The
+// leader (r = 0) sets the stage's byte count, both CTAs' copies complete on
+// the leader's barrier, the leader issues tcgen05.mma.cta_group::2 (M = 256,
+// N = 256) and multicasts every commit to both CTAs; each CTA's accumulator
+// holds its 128 weight rows x 256 tokens and its epilogue (the same as the
+// single-CTA kernel's) stores them; the epilogue warps of both CTAs free an
+// accumulator buffer on the leader's barrier.  Both CTAs take part in the
+// pair's TMEM allocation and release.
+namespace pair {
+constexpr int STAGES = 6;                    // 7 measured slower
+constexpr int XH_STAGE = (TT / 2) * BK * 2;  // 16 KB: this CTA's 128 token rows
+constexpr int W_STAGE = TW * BK * 2;         // 16 KB: this CTA's 128 weight rows
+constexpr int OFF_X = 0, OFF_W = STAGES * XH_STAGE, OFF_BAR = OFF_W + STAGES * W_STAGE;
+constexpr int BAR_FULL = 0, BAR_EMPTY = STAGES, BAR_ACC_FULL = 2 * STAGES, BAR_ACC_EMPTY = BAR_ACC_FULL + 2,
+              BAR_DRAIN = BAR_ACC_EMPTY + 2, NUM_BARS = BAR_DRAIN + 1;
+constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+constexpr int SMEM = OFF_MISC + 16 + 1024;
+static_assert(SMEM <= 227 * 1024, "shared memory budget");
+// kind::f16 with M = 256 (the pair; bits 24-28: M >> 4) and N = 256 tokens
+constexpr uint32_t kIdescPairF16 = (1u << 4) | ((uint32_t)(TT >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+constexpr uint32_t kIdescPairBF16 = kIdescPairF16 | (1u << 7) | (1u << 10);
+}  // namespace pair
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// The address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// A tile into this CTA's shared memory, completing on a barrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%3, %4}], [%2];" ::"r"(
+            dst),
+        "l"(map), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+__device__ __forceinline__ void umma_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrives on the barrier at this offset in both CTAs of the pair once the MMAs issued so far complete.
+__device__ __forceinline__ void umma_commit_both(uint32_t bar) {
+    const uint16_t mask = 3;
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+                 "h"(mask)
+                 : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant__ CUtensorMap tmW,
+                     const GemmArgs p) {
+    static_assert(MODE == kModeDequantW16 || MODE == kModeBf16 || MODE == kModeScaleF32, "pair modes");
+    using namespace pair;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    const uint32_t sX = base + OFF_X, sW = base + OFF_W;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_MISC + 4);
+    auto bar = [&](int i) -> uint32_t { return base + OFF_BAR + 8u * (uint32_t)i; };
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int pair_id = blockIdx.x >> 1, num_pairs = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(bar(BAR_FULL + i), 1);   // the leader's expect_tx (both CTAs' bytes)
+            mbar_init(bar(BAR_EMPTY + i), 1);  // the leader's multicast commit
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(BAR_ACC_FULL + i), 1);    // the leader's multicast commit
+            mbar_init(bar(BAR_ACC_EMPTY + i), 16);  // the 8 epilogue warps of each CTA (the leader's copy is used)
+        }
+        mbar_init(bar(BAR_DRAIN), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {  // one warp of each CTA takes part in the pair's allocation
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync_all();  // the barriers of both CTAs are initialised and the TMEM allocated
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int num_t = (p.M + TT - 1) / TT;
+    const int num_w2 = (p.N + 2 * TW - 1) / (2 * TW);
+    const int num_tiles = num_t * num_w2;
+    const int num_kb = (p.K + BK - 1) / BK;
+    const int chunk_kb = MODE == kModeBf16 ? num_kb : CHUNK_KB;
+
+    if (warp < 4) {
+        regs_dec<REGS_WG0>();
+        if (warp == 0 && lane == 0) {
+            // ------------------------------------------------------ producer
+            // this CTA's token and weight halves of each stage, onto the leader's barrier
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmXh) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
+            int it = 0, skipped = -1;
+            bool ok = true;
+            for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
+                int tb, wb2;
+                tile_coords(tile, num_t, num_w2, p.group, p.group_weight != 0, tb, wb2);
+                for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    if (!mbar_wait(bar(BAR_EMPTY + s), ((it / STAGES) & 1) ^ 1, abort_flag, p.err, p.wait_limit_ns)) {
+                        ok = false;
+                        break;
                     }
-                } else if constexpr (MODE == kModeScaleF32) {
-                    float *out = static_cast<float *>(p.out) + (int64_t)m0 * p.N + n;
-#pragma unroll
-                    for (int i4 = 0; i4 < 128; i4 += 4) {
-                        float sx[4];
-                        if (full) {
-                            const float4 v = CR_SPAN(m0 + i4, 4, p.M) ? __ldg(reinterpret_cast<const float4 *>(p.sa + m0 + i4))
-                                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-                            sx[0] = v.x, sx[1] = v.y, sx[2] = v.z, sx[3] = v.w;
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) sx[j] = i4 + j < mlim ? __ldg(p.sa + m0 + i4 + j) : 0.f;
+                    if (rank == 0) mbar_expect_tx(bar(BAR_FULL + s), 2 * (XH_STAGE + W_STAGE));
+                    const uint32_t full = mapa_shared(bar(BAR_FULL + s), 0);
+                    // self-test: the named operand's copies of this stage are never issued
+                    const bool skip_x = it == p.fault_skip_it && p.fault_role == 0;
+                    const bool skip_w = it == p.fault_skip_it && p.fault_role == 1;
+                    if (!skip_x) tma_load_2d_pair(sX + s * XH_STAGE, &tmXh, full, kb * BK, tb * TT + (int)rank * (TT / 2));
+                    if (!skip_w) tma_load_2d_pair(sW + s * W_STAGE, &tmW, full, kb * BK, (wb2 * 2 + (int)rank) * TW);
+                    if (skip_x || skip_w) skipped = it;
+                }
+            }
+            // Let the copies already issued land before the CTA exits: the leader waits on its
+            // barriers (which both CTAs' copies complete on); the partner's producer left its loop
+            // only after a wait that ran out, far longer than a copy in flight takes.
+            if ((!ok || skipped >= 0) && rank == 0) {
+                for (int j = it - 1; j >= 0 && j >= it - STAGES; --j)
+                    if (j != skipped) mbar_wait_drain(bar(BAR_FULL + j % STAGES), (j / STAGES) & 1, p.wait_limit_ns);
+            }
+        } else if (warp == 1 && lane == 0 && rank == 0) {
+            // ----------------------------------------------------- MMA (leader)
+            int it = 0, g = 0;
+            bool ok = true;
+            uint32_t dcol = 0;
+            constexpr uint32_t kIdesc = MODE == kModeBf16 ? kIdescPairBF16 : kIdescPairF16;
+            for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
+                for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                    const int kc = kb % chunk_kb;
+                    if (kc == 0) {
+                        const int buf = g & 1;
+                        if (!mbar_wait(bar(BAR_ACC_EMPTY + buf), ((g >> 1) & 1) ^ 1, abort_flag, p.err,
+                                       p.wait_limit_ns)) {
+                            ok = false;
+                            break;
                         }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            if (full || i4 + j < mlim) *out = __fmul_rn(__int2float_rn(acc[i4 + j]), sx[j]);
-                            out += p.N;
-                        }
+                        tc_fence_after();
+                        dcol = (uint32_t)(buf * TT);
                     }
-                } else if constexpr (MODE == kModeBf16) {
-                    uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)m0 * p.N + n;
-#pragma unroll
-                    for (int i = 0; i < 128; ++i) {
-                        if (full || i < mlim) *out = (uint16_t)float_to_bf16_bits(__int_as_float(acc[i]));
-                        out += p.N;
+                    const int s = it % STAGES;
+                    if (!mbar_wait(bar(BAR_FULL + s), (it / STAGES) & 1, abort_flag, p.err, p.wait_limit_ns)) {
+                        ok = false;
+                        break;
                     }
-                } else if constexpr (MODE == kModeDequantW16Lora) {  // y (with the bypass) is in the registers
-                    uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)m0 * p.N + n;
+                    tc_fence_after();
 #pragma unroll
-                    for (int i = 0; i < 128; ++i) {
-                        if (full || i < mlim) *out = (uint16_t)float_to_bf16_bits(__int_as_float(acc[i]));
-                        out += p.N;
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = sw128_desc(sW + s * W_STAGE + kk * 32);
+                        const uint64_t bd = sw128_desc(sX + s * XH_STAGE + kk * 32);
+                        umma_f16_pair(tmem + dcol, ad, bd, kIdesc, (kc > 0 || kk > 0) ? 1u : 0u);
                     }
-                } else {  // kModeDequant, kModeDequantW16
-                    uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)m0 * p.N + n;
-                    const float swn = CR_SPAN(n, 1, p.N) ? __ldg(p.sb + n) : 0.f;
-                    const bool has_bias = p.bias != nullptr;
-                    const float bn = has_bias ? bf16_bits_to_float(__ldg(p.bias + n)) : 0.f;
-#pragma unroll
-                    for (int i4 = 0; i4 < 128; i4 += 4) {
-                        float sx[4];
-                        if (full) {
-                            const float4 v = CR_SPAN(m0 + i4, 4, p.M) ? __ldg(reinterpret_cast<const float4 *>(p.sa + m0 + i4))
-                                                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-                            sx[0] = v.x, sx[1] = v.y, sx[2] = v.z, sx[3] = v.w;
-                        } else {
-#pragma unroll
-                            for (int j = 0; j < 4; ++j) sx[j] = i4 + j < mlim ? __ldg(p.sa + m0 + i4 + j) : 0.f;
-                        }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            float y = __fmul_rn(__int2float_rn(acc[i4 + j]), __fmul_rn(sx[j], swn));
-                            if (has_bias) y = __fadd_rn(y, bn);
-                            if (full || i4 + j < mlim) *out = (uint16_t)float_to_bf16_bits(y);
-                            out += p.N;
-                        }
+                    umma_commit_both(bar(BAR_EMPTY + s));
+                    if (kc == chunk_kb - 1 || kb == num_kb - 1) {
+                        umma_commit_both(bar(BAR_ACC_FULL + (g & 1)));
+                        ++g;
                     }
                 }
             }
+            umma_commit_pair(bar(BAR_DRAIN));  // fires once every MMA issued above has completed
+            mbar_wait_drain(bar(BAR_DRAIN), 0, p.wait_limit_ns);
+        }
+        __syncwarp();
+        end_barrier();
+    } else if (warp < 8) {
+        regs_dec<REGS_CONV>();  // no widening in these modes
+        end_barrier();
+    } else {
+        // ---------------------------------------------------------- epilogue
+        regs_inc<REGS_EPI>();
+        const int q = warp & 3;          // TMEM lane quarter = weight rows 32q .. 32q+31 of this CTA's half
+        const int h = (warp - 8) >> 2;   // token half of the 256-wide tile
+        const uint32_t acc_empty0 = mapa_shared(bar(BAR_ACC_EMPTY), 0);  // the leader's
+        int g = 0;
+        bool ok = true;
+        for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
+            int tb, wb2;
+            tile_coords(tile, num_t, num_w2, p.group, p.group_weight != 0, tb, wb2);
+            int acc[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i) acc[i] = 0;
+            const int nchunks = (num_kb + chunk_kb - 1) / chunk_kb;
+            for (int ch = 0; ch < nchunks; ++ch, ++g) {
+                const int buf = g & 1;
+                if (!warp_wait(bar(BAR_ACC_FULL + buf), (g >> 1) & 1, abort_flag, p.err, p.wait_limit_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * TT + h * 128);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    uint32_t r[16];
+                    tmem_ld16(taddr + 16 * j, r);
+                    tmem_wait_ld();
+                    if constexpr (MODE == kModeBf16) {  // one chunk: keep the fp32 bits
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[16 * j + i] = (int)r[i];
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[16 * j + i] += __float2int_rn(__uint_as_float(r[i]));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8u * (uint32_t)buf);
+            }
+            if (!ok) break;
+            const int n = (wb2 * 2 + (int)rank) * TW + 32 * q + lane;
+            const int m0 = tb * TT + h * 128;
+            const int mlim = p.M - m0;
+            epi_store<MODE>(acc, n, m0, mlim, mlim >= 128, p);
         }
         end_barrier();
+    }
+    // both CTAs: the partner's epilogue has read its accumulator and the leader's MMAs are
+    // complete before the pair releases the TMEM
+    tc_fence_before();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
     }
 }
 
@@ -611,6 +880,41 @@ cudaError_t launch_mode(const CUtensorMap &tmX, const CUtensorMap &tmW, const Ge
     if (e != cudaSuccess) return e;
     gemm_s8_tc_kernel<MODE><<<grid, NUM_THREADS, kSmem, st>>>(tmX, tmW, tmXA ? *tmXA : tmX, tmLB ? *tmLB : tmW, p);
     return cudaGetLastError();
+}
+
+
+// The CTA-pair kernel: clusters of two CTAs, one pair per two SMs.  A is the
+// token matrix (encoded here with a box of 128 rows: each CTA loads half a tile).
+template <int MODE>
+cudaError_t launch_pair(CUtensorMapDataType dt, const void *A, const CUtensorMap &tmW, GemmArgs p, cudaStream_t st) {
+    CUtensorMap tmXh;
+    if (!encode_2d(&tmXh, dt, 2, A, (uint64_t)p.K, (uint64_t)p.M, BK, TT / 2, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    const int64_t num_t = (p.M + TT - 1) / TT, num_w2 = (p.N + 2 * TW - 1) / (2 * TW);
+    int group, group_weight;
+    choose_raster(num_t, num_w2, p.K, 4, group, group_weight);  // a pair's weight tile: 256 rows x 2 bytes
+    p.group = group;
+    p.group_weight = group_weight;
+    const int64_t tiles = num_t * num_w2;
+    const int max_pairs = sm_count() / 2;
+    if (max_pairs <= 0) return cudaErrorNotSupported;
+    const int pairs = (int)(tiles < max_pairs ? tiles : max_pairs);
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_pair_kernel<MODE>), pair::SMEM);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * pairs), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = pair::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<MODE>, tmXh, tmW, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -650,7 +954,8 @@ cudaError_t launch_gemm_w16(const uint16_t *A, const float *sa, const uint16_t *
     int group, group_weight;
     choose_raster(num_t, num_w, K, 2, group, group_weight);
     GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, sa, sb, bias, out, err};
-    return launch_mode<kModeDequantW16>(tmX, tmW, p, num_t * num_w, st);
+    (void)tmX;
+    return launch_pair<kModeDequantW16>(CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, tmW, p, st);
 }
 
 cudaError_t launch_gemm_w16_lora(const uint16_t *A, const float *sa, const uint16_t *B16, const float *sb,
@@ -691,7 +996,8 @@ cudaError_t launch_gemm_w16_scale_f32(const uint16_t *A, const float *sa, const 
     int group, group_weight;
     choose_raster(num_t, num_w, K, 2, group, group_weight);
     GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, sa, nullptr, nullptr, out, err};
-    return launch_mode<kModeScaleF32>(tmX, tmW, p, num_t * num_w, st);
+    (void)tmX;
+    return launch_pair<kModeScaleF32>(CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, tmW, p, st);
 }
 
 cudaError_t launch_gemm_fault_selftest(bool widened, const uint16_t *A, const float *sa, const void *B,
@@ -715,7 +1021,7 @@ cudaError_t launch_gemm_fault_selftest(bool widened, const uint16_t *A, const fl
     p.wait_limit_ns = limit_ns;
     p.fault_skip_it = skip_it;
     p.fault_role = role;
-    return widened ? launch_mode<kModeDequantW16>(tmX, tmW, p, num_t * num_w, st)
+    return widened ? launch_pair<kModeDequantW16>(CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, tmW, p, st)
                    : launch_mode<kModeDequant>(tmX, tmW, p, num_t * num_w, st);
 }
 
@@ -734,7 +1040,8 @@ cudaError_t launch_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t M, in
     int group, group_weight;
     choose_raster(num_t, num_w, K, 2, group, group_weight);
     GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, nullptr, nullptr, nullptr, out, err};
-    return launch_mode<kModeBf16>(tmX, tmW, p, num_t * num_w, st);
+    (void)tmX;
+    return launch_pair<kModeBf16>(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, tmW, p, st);
 }
 
 }  // namespace convrot
