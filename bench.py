@@ -37,15 +37,15 @@ WORKLOAD = ("train20k: packed 20k-token training step of one ConvRot INT8 linear
             "+ dequant -> y, rotate+quantize dY, widen the int8 backward weight, int8 grad_x GEMM -> dX")
 L2_FLUSH_BYTES = 256 << 20
 
-# DRAM bytes (read + write) per launch of gemm_s8_tc_kernel, from one-pass ncu
+# DRAM bytes (read + write) per launch of the GEMM (gemm_pair_kernel), from one-pass ncu
 # captures (dram__bytes_read.sum + dram__bytes_write.sum) of
 #   python -m int8_rotated_quantized_gb300.profile_case gemm_w16 --M 20480 --N 16384 --K 4096 --reps 3   (forward)
 #   python -m int8_rotated_quantized_gb300.profile_case gemm_w16 --M 20480 --N 4096 --K 16384 --reps 3   (grad_x)
 #   python -m int8_rotated_quantized_gb300.profile_case gemm_bf16 --M 20480 --N 4096 --K 16384 --reps 3  (bf16 grad_x)
 # keyed by the hash of the kernel source they were taken on; reported as null
 # once the kernel source differs (or where no capture was taken on it).
-GEMM_TRAFFIC = {"source_sha256_16": "15c2af51b3fd39d5", "fwd": 800396800 + 650350592, "bwd": 3196012032 + 162386432,
-                "bf16_bwd": 3195729408 + 162459904}
+GEMM_TRAFFIC = {"source_sha256_16": "3010cc6baa5dcba2", "fwd": 962232576 + 652294400, "bwd": 3196455168 + 162352640,
+                "bf16_bwd": 3261911808 + 162498816}
 
 
 def _gemm_source_current():
@@ -359,7 +359,7 @@ def run_gpu(args):
                        "tokens_per_gpu": M, "l2": "flushed between steps (256 MiB write, outside the events)",
                        "parallelism": f"replicas x{world} (rows sharded, no collective)"},
             "roofline": {
-                "kernel": "gemm_s8_tc_kernel, widened-weight mode (fwd and grad_x launches)",
+                "kernel": "gemm_pair_kernel (CTA pairs, 2-SM MMA), widened-weight mode (fwd and grad_x launches)",
                 "bound": "tensor",
                 "achieved": round(gemm_tflops, 1),
                 "peak": pk["bf16"],
@@ -499,10 +499,10 @@ def measure_rows(cr, synth, sg, torch, dev, flush, pk, int8_peak=None):
     w16 = cr.convrot_widen_codes(Wq2)
     y2 = torch.empty((M2, N2), dtype=torch.bfloat16, device=dev)
     ms = _time(torch, lambda i: cr.convrot_gemm_dequant_w16(xq2, sx2, w16, sw2, None, y2), flush, reps)
-    tiles = -(-M2 // 256) * -(-N2 // 128)
+    tiles = -(-M2 // 256) * -(-N2 // 256)
     rows["c2_a4a5_gemm"] = _tc_row(2.0 * M2 * N2 * K2, ms, pk,
                                    f"img1024 4096x4096x4096 GEMM + dequant (widened-weight mode; {tiles} tiles of "
-                                   "256 tokens x 128 weight rows on the SMs)", int8_peak)
+                                   "256 tokens x 256 weight rows on CTA pairs, one per two SMs)", int8_peak)
     ws2 = torch.empty(cr.convrot_linear_workspace_bytes(M2, K2, N2), dtype=torch.uint8, device=dev)
     ms = _time(torch, lambda i: cr.convrot_linear_fwd(x2, Wq2, sw2, b2, y=y2, workspace=ws2), flush, reps)
     rows["c2_fwd_call"] = _tc_row(2.0 * M2 * N2 * K2, ms, pk,
