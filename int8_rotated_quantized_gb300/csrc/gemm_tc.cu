@@ -608,7 +608,9 @@ namespace pair {
 constexpr int STAGES = 6;                    // 7 measured slower
 constexpr int XH_STAGE = (TT / 2) * BK * 2;  // 16 KB: this CTA's 128 token rows
 constexpr int W_STAGE = TW * BK * 2;         // 16 KB: this CTA's 128 weight rows
-constexpr int OFF_X = 0, OFF_W = STAGES * XH_STAGE, OFF_BAR = OFF_W + STAGES * W_STAGE;
+constexpr int STG_BYTES = 32 * 32 * 2;  // a warp's 32 tokens x 32 features of bf16 output
+constexpr int OFF_X = 0, OFF_W = STAGES * XH_STAGE, OFF_STG = OFF_W + STAGES * W_STAGE,
+              OFF_BAR = OFF_STG + 8 * STG_BYTES;
 constexpr int BAR_FULL = 0, BAR_EMPTY = STAGES, BAR_ACC_FULL = 2 * STAGES, BAR_ACC_EMPTY = BAR_ACC_FULL + 2,
               BAR_DRAIN = BAR_ACC_EMPTY + 2, NUM_BARS = BAR_DRAIN + 1;
 constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
@@ -660,6 +662,60 @@ __device__ __forceinline__ void umma_commit_both(uint32_t bar) {
 }
 __device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// The bf16-output epilogue stores of the pair kernel for a warp whose 32
+// features and 128 tokens all exist: each 32-token block goes through the
+// warp's 2 KB of shared memory ([token][feature], written one feature per
+// lane) and leaves as 16-byte stores of 8 features of one token (a quarter of
+// the store instructions of writing each value on its own; measured 1.4-2%
+// faster on the forward shapes).  y = bf16(acc * (sa[m] * sb[n]) + bias[n])
+// (dequantization mode) or bf16 of the fp32 bits in acc (bf16 mode).
+template <int MODE>
+__device__ __forceinline__ void epi_store_staged(const int (&acc)[128], int n, int m0, const GemmArgs &p, uint16_t *stg,
+                                                 int lane) {
+    float swn = 0.f, bn = 0.f;
+    bool has_bias = false;
+    if constexpr (MODE == kModeDequantW16) {
+        swn = __ldg(p.sb + n);
+        has_bias = p.bias != nullptr;
+        bn = has_bias ? bf16_bits_to_float(__ldg(p.bias + n)) : 0.f;
+    }
+    const int nb = n - lane;  // the warp's first feature
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+#pragma unroll
+        for (int i4 = 0; i4 < 32; i4 += 4) {
+            float sx[4] = {0.f, 0.f, 0.f, 0.f};
+            if constexpr (MODE == kModeDequantW16) {
+                const float4 v = CR_SPAN(m0 + 32 * r + i4, 4, p.M)
+                                     ? __ldg(reinterpret_cast<const float4 *>(p.sa + m0 + 32 * r + i4))
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                sx[0] = v.x, sx[1] = v.y, sx[2] = v.z, sx[3] = v.w;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float y;
+                if constexpr (MODE == kModeDequantW16) {
+                    y = __fmul_rn(__int2float_rn(acc[32 * r + i4 + j]), __fmul_rn(sx[j], swn));
+                    if (has_bias) y = __fadd_rn(y, bn);
+                } else {
+                    y = __int_as_float(acc[32 * r + i4 + j]);
+                }
+                stg[(i4 + j) * 32 + lane] = (uint16_t)float_to_bf16_bits(y);
+            }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int row = 8 * t + (lane >> 2), c = lane & 3;  // 16 bytes: features nb + 8c .. + 7 of token row
+            const int64_t off = (int64_t)(m0 + 32 * r + row) * p.N + nb + 8 * c;
+            if (CR_SPAN(off, 8, (int64_t)p.M * p.N))
+                *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(p.out) + off) =
+                    *reinterpret_cast<const uint4 *>(stg + row * 32 + 8 * c);
+        }
+        __syncwarp();
+    }
 }
 
 template <int MODE>
@@ -835,7 +891,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int n = (wb2 * 2 + (int)rank) * TW + 32 * q + lane;
             const int m0 = tb * TT + h * 128;
             const int mlim = p.M - m0;
-            epi_store<MODE>(acc, n, m0, mlim, mlim >= 128, p);
+            if ((MODE == kModeDequantW16 || MODE == kModeBf16) && mlim >= 128 && n - lane + 32 <= p.N)
+                epi_store_staged<MODE>(acc, n, m0, p, reinterpret_cast<uint16_t *>(smem + OFF_STG + (warp - 8) * STG_BYTES),
+                                       lane);
+            else
+                epi_store<MODE>(acc, n, m0, mlim, mlim >= 128, p);
         }
         end_barrier();
     }
