@@ -165,10 +165,8 @@ CONVROT_API int convrot_linear_fwd(const uint16_t *x, int64_t M, int64_t K, cons
                        uint16_t *y, void *workspace, size_t ws_bytes, convrot_stream_t stream);
 
 /* Bytes of workspace convrot_linear_fwd_lora needs: those of the widened-weight
- * path, the scaled down-projection and the adapter's B as three bf16 parts per
- * value (128 bytes per row of M and of N), and, when the down-projection
- * splits K into column spans (few rows), fp32 partial sums (16 x M rounded up
- * to 256 per span, at most 8 spans). */
+ * path plus the scaled down-projection and the adapter's B as three bf16 parts
+ * per value (128 bytes per row of M and of N, each rounded up to 256). */
 CONVROT_API size_t convrot_linear_lora_workspace_bytes(int64_t M, int64_t K, int64_t N);
 
 /* Forward with an unmerged LoRA adapter as a bypass (the LoRA branch of a
@@ -177,12 +175,18 @@ CONVROT_API size_t convrot_linear_lora_workspace_bytes(int64_t M, int64_t K, int
  *   y = bf16( acc * scale_x[m] * scale_w[n] + bias[n]
  *             + sum_j (coef * sum_k x[m,k] lora_A[j,k]) * lora_B[n,j] ),
  *   coef = fp32(scale * alpha / rank).  The down-projection is summed in fp32;
- *   the branch runs on the tensor cores with each fp32 factor split into three
- *   bf16 parts (about 24 bits) and fp32 accumulation, and is added to the
- *   dequantized product before the rounding.
+ *   the branch runs on the tensor cores in the GEMM's accumulator units (its
+ *   factors divided by scale_x[m] and scale_w[n], 1 taking the place of a zero
+ *   scale), each fp32 factor split into three bf16 parts (about 24 bits), and
+ *   is accumulated in fp32 onto the last integer chunk of the product before
+ *   the dequantization and the rounding.  coef = 0 runs convrot_linear_fwd
+ *   (bit for bit its result).
  * x bf16 [M, K] (K multiple of 32); lora_A fp32 [rank, K] (16-byte aligned); lora_B fp32 [N, rank];
  * 1 <= rank <= 16; workspace >= convrot_linear_lora_workspace_bytes(M, K, N),
- * 256-byte aligned.  Weight codes as in convrot_linear_fwd. */
+ * 256-byte aligned.  Weight codes as in convrot_linear_fwd; a weight row whose
+ * scale is 0 must hold zero codes (convrot_quantize_weight writes it so), or
+ * that row of y is undefined.  Branch values beyond fp32's range once divided
+ * by scale_x[m] * scale_w[n] (scales near 1e-30) overflow to inf. */
 CONVROT_API int convrot_linear_fwd_lora(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq,
                             const float *scale_w, int64_t N, int block, const uint16_t *bias,
                             const float *lora_A, const float *lora_B, int rank, float alpha, float scale,

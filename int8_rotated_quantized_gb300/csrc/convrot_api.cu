@@ -244,9 +244,7 @@ int convrot_linear_fwd(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq
 size_t convrot_linear_lora_workspace_bytes(int64_t M, int64_t K, int64_t N) {
     if (M < 0 || K < 0 || N < 0) return 0;
     const size_t parts_row = (size_t)convrot::kLoraPartsRow * 2;
-    return convrot_linear_workspace_bytes(M, K, N) + align256((size_t)M * parts_row) +
-           align256((size_t)N * parts_row) + align256((size_t)48 * (size_t)K * 2) +
-           align256((size_t)convrot::lora_down_spans(M, K) * (size_t)M * 48 * sizeof(float));
+    return convrot_linear_workspace_bytes(M, K, N) + align256((size_t)M * parts_row) + align256((size_t)N * parts_row);
 }
 
 int convrot_linear_fwd_lora(const uint16_t *x, int64_t M, int64_t K, const int8_t *Wq, const float *scale_w,
@@ -260,6 +258,9 @@ int convrot_linear_fwd_lora(const uint16_t *x, int64_t M, int64_t K, const int8_
            aligned16(y) && aligned16(scale_w) && aligned16(lora_A) && ((uintptr_t)lora_B & 3u) == 0 &&
            ((uintptr_t)workspace & 255u) == 0 && (bias == nullptr || aligned16(bias))));
     CHECK(M == 0 || N == 0 || ws_bytes >= convrot_linear_lora_workspace_bytes(M, K, N));
+    const float coef = (float)((double)scale * (double)alpha / (double)rank);
+    if (coef == 0.f)  // the branch is zero: the plain forward (its widened-weight path, bit-identical)
+        return convrot_linear_fwd(x, M, K, Wq, scale_w, N, block, bias, y, workspace, ws_bytes, stream);
     unsigned *err = nullptr;
     int rc = device_setup(&err);
     if (rc != CONVROT_OK) return rc;
@@ -272,17 +273,11 @@ int convrot_linear_fwd_lora(const uint16_t *x, int64_t M, int64_t K, const int8_
     const size_t parts_row = (size_t)convrot::kLoraPartsRow * 2;
     char *lw = ws + convrot_linear_workspace_bytes(M, K, N);
     uint16_t *xa_parts = reinterpret_cast<uint16_t *>(lw);
-    lw += align256((size_t)M * parts_row);
-    uint16_t *b_parts = reinterpret_cast<uint16_t *>(lw);
-    lw += align256((size_t)N * parts_row);
-    uint16_t *ap = reinterpret_cast<uint16_t *>(lw);
-    lw += align256((size_t)48 * (size_t)K * 2);
-    float *part = reinterpret_cast<float *>(lw);
-    const float coef = (float)((double)scale * (double)alpha / (double)rank);
+    uint16_t *b_parts = reinterpret_cast<uint16_t *>(lw + align256((size_t)M * parts_row));
     rc = quantize_act_impl(x, M, K, K, block, xq, sx, st);
     if (rc != CONVROT_OK) return rc;
     rc = cuda_status(
-        convrot::launch_lora_operands(x, M, K, lora_A, lora_B, N, rank, coef, ap, xa_parts, b_parts, part, err, st));
+        convrot::launch_lora_operands(x, sx, M, K, lora_A, lora_B, scale_w, N, rank, coef, xa_parts, b_parts, err, st));
     if (rc != CONVROT_OK) return rc;
     rc = cuda_status(convrot::launch_widen_codes(Wq, N * K, w16, st));
     if (rc != CONVROT_OK) return rc;

@@ -70,12 +70,15 @@ constexpr int WH_STAGE = TW * BK * 2;  // 16 KB widened weight tile
 // dequantization epilogue on weight codes that a separate pass already
 // widened to fp16 (no converter in the loop, the same exact integer chunks).
 constexpr int kModeS32 = 0, kModeDequant = 1, kModeBf16 = 2, kModeDequantW16 = 3;
-// The widened-weight dequantization mode plus a LoRA bypass term:
-// y += sum_j xa[m, j] * B[n, j] (xa already scaled).  The term is one more
-// K block per tile on the tensor cores: xa and B enter as three bf16 parts
-// each (hi + mid + lo = the fp32 value to about 24 bits), the six products of
-// parts whose orders add up to at most 2 accumulate in fp32 into the next
-// TMEM chunk buffer, and the epilogue adds that chunk to the dequantized y.
+// The widened-weight dequantization mode plus a LoRA bypass term (CTA pairs
+// only): y = bf16(acc * (sx * sw) + bias + sum_j xa[m, j] B[n, j]).  The term
+// joins each tile's last exact-integer chunk as one more K block on the tensor
+// cores: the operands arrive divided by the output's scales (xa[m] / dx[m] and
+// B[n] / dw[n], d = s, or 1 where s = 0, whose codes are all zero) as three
+// bf16 parts each (hi + mid + lo = the fp32 value to about 24 bits), and the
+// six products of parts whose orders add up to at most 2 accumulate in fp32
+// onto the chunk's integer sum; the epilogue adds that chunk to the earlier
+// chunks' sum in fp32 and scales by dx * dw.
 constexpr int kModeDequantW16Lora = 4;
 // Widened weight codes, exact integer chunks, and an fp32 result scaled by the
 // token's scale only: P[m, n] = float(acc) * sa[m] (the second reading of the
@@ -226,14 +229,7 @@ __device__ __forceinline__ void epi_store(const int (&acc)[128], int n, int m0, 
                     out += p.N;
                 }
             }
-        } else if constexpr (MODE == kModeBf16) {
-            uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)m0 * p.N + n;
-#pragma unroll
-            for (int i = 0; i < 128; ++i) {
-                if (full || i < mlim) *out = (uint16_t)float_to_bf16_bits(__int_as_float(acc[i]));
-                out += p.N;
-            }
-        } else if constexpr (MODE == kModeDequantW16Lora) {  // y (with the bypass) is in the registers
+        } else if constexpr (MODE == kModeBf16) {  // (also the bypass mode: y's fp32 bits)
             uint16_t *out = static_cast<uint16_t *>(p.out) + (int64_t)m0 * p.N + n;
 #pragma unroll
             for (int i = 0; i < 128; ++i) {
@@ -271,7 +267,6 @@ __device__ __forceinline__ void epi_store(const int (&acc)[128], int n, int m0, 
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_s8_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                      const __grid_constant__ CUtensorMap tmXA, const __grid_constant__ CUtensorMap tmLB,
                       const GemmArgs p) {
     using L = Layout<MODE>;
     extern __shared__ uint8_t smem_raw[];
@@ -323,8 +318,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int num_kb = (p.K + BK - 1) / BK;
     // K blocks per TMEM accumulation: exact-integer chunks, or all of K for bf16
     const int chunk_kb = MODE == kModeBf16 ? num_kb : CHUNK_KB;
-    // the bypass mode's extra K block per tile (the LoRA parts), its own chunk
-    constexpr int kExtra = MODE == kModeDequantW16Lora ? 1 : 0;
 
     if (warp < 4) {
         regs_dec<REGS_WG0>();
@@ -346,7 +339,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
                 int tb, wb;
                 tile_coords(tile, num_t, num_w, p.group, p.group_weight != 0, tb, wb);
-                for (int kb = 0; kb < num_kb + kExtra; ++kb, ++it) {
+                for (int kb = 0; kb < num_kb; ++kb, ++it) {
                     const int s = it % nst;
                     if (!mbar_wait(bar(empty0 + s), ((it / nst) & 1) ^ 1, abort_flag, p.err, p.wait_limit_ns)) {
                         ok = false;
@@ -355,15 +348,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // self-test: the named operand's copy of this stage is never issued
                     const bool skip_x = it == p.fault_skip_it && p.fault_role == 0;
                     const bool skip_w = it == p.fault_skip_it && p.fault_role == 1;
-                    const bool extra = kExtra && kb == num_kb;  // bypass parts: 128 bytes per row
                     if (is_x) {
                         mbar_expect_tx(bar(full0 + s), X_STAGE + (L::kDirect ? WH_STAGE : 0));
-                        if (!skip_x)
-                            tma_load_2d(sX + s * X_STAGE, extra ? &tmXA : &tmX, bar(full0 + s), extra ? 0 : kb * BK,
-                                        tb * TT);
-                        if (L::kDirect && !skip_w)
-                            tma_load_2d(sWh + s * WH_STAGE, extra ? &tmLB : &tmW, bar(full0 + s),
-                                        extra ? 0 : kb * BK, wb * TW);
+                        if (!skip_x) tma_load_2d(sX + s * X_STAGE, &tmX, bar(full0 + s), kb * BK, tb * TT);
+                        if (L::kDirect && !skip_w) tma_load_2d(sWh + s * WH_STAGE, &tmW, bar(full0 + s), kb * BK, wb * TW);
                         if (skip_x || (L::kDirect && skip_w)) skipped = it;  // this stage never completes
                     } else {
                         if (skip_w) {
@@ -385,9 +373,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             uint32_t dcol = 0;
             for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                for (int kb = 0; kb < num_kb + kExtra; ++kb, ++it) {
-                    const bool extra = kExtra && kb == num_kb;
-                    const int kc = extra ? 0 : kb % chunk_kb;
+                for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                    const int kc = kb % chunk_kb;
                     if (kc == 0) {
                         const int buf = g & 1;
                         if (!mbar_wait(bar(L::BAR_ACC_EMPTY + buf), ((g >> 1) & 1) ^ 1, abort_flag, p.err,
@@ -404,28 +391,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
-                    if (extra) {
-                        // parts at byte offsets 0 (hi), 32 (mid), 64 (lo) of each 128-byte row:
-                        // hi*hi, hi*mid, mid*hi, hi*lo, mid*mid, lo*hi
 #pragma unroll
-                        for (int q = 0; q < 6; ++q) {
-                            const int pa = q == 0 ? 0 : q == 1 ? 0 : q == 2 ? 1 : q == 3 ? 0 : q == 4 ? 1 : 2;
-                            const int pb = q == 0 ? 0 : q == 1 ? 1 : q == 2 ? 0 : q == 3 ? 2 : q == 4 ? 1 : 0;
-                            const uint64_t ad = sw128_desc(sWh + s * WH_STAGE + pa * 32);
-                            const uint64_t bd = sw128_desc(sX + s * X_STAGE + pb * 32);
-                            umma_f16(tmem + dcol, ad, bd, kIdescBF16, q > 0 ? 1u : 0u);
-                        }
-                    } else {
-#pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk) {
-                            const uint64_t ad = sw128_desc(sWh + s * WH_STAGE + kk * 32);
-                            const uint64_t bd = sw128_desc(sX + s * X_STAGE + kk * 32);
-                            umma_f16(tmem + dcol, ad, bd, MODE == kModeBf16 ? kIdescBF16 : kIdescF16,
-                                     (kc > 0 || kk > 0) ? 1u : 0u);
-                        }
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = sw128_desc(sWh + s * WH_STAGE + kk * 32);
+                        const uint64_t bd = sw128_desc(sX + s * X_STAGE + kk * 32);
+                        umma_f16(tmem + dcol, ad, bd, MODE == kModeBf16 ? kIdescBF16 : kIdescF16,
+                                 (kc > 0 || kk > 0) ? 1u : 0u);
                     }
                     umma_commit(bar(L::BAR_EMPTY + s));
-                    if (extra || kc == chunk_kb - 1 || kb == num_kb - 1) {
+                    if (kc == chunk_kb - 1 || kb == num_kb - 1) {
                         umma_commit(bar(L::BAR_ACC_FULL + (g & 1)));
                         ++g;
                     }
@@ -538,51 +512,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int m0 = tb * TT + h * 128;
             const int mlim = p.M - m0;  // tokens of this column half that exist
             const bool full = mlim >= 128;
-            if constexpr (MODE == kModeDequantW16Lora) {
-                // y = acc * (sx * sw) + bias in place (the registers now hold fp32), then
-                // + the bypass chunk from TMEM (every thread of the half takes part)
-                const float swn = n < p.N && CR_SPAN(n, 1, p.N) ? __ldg(p.sb + n) : 0.f;
-                const bool has_bias = p.bias != nullptr && n < p.N;
-                const float bn = has_bias ? bf16_bits_to_float(__ldg(p.bias + n)) : 0.f;
-#pragma unroll
-                for (int i4 = 0; i4 < 128; i4 += 4) {
-                    float sx[4];
-                    if (full) {
-                        const float4 v = CR_SPAN(m0 + i4, 4, p.M) ? __ldg(reinterpret_cast<const float4 *>(p.sa + m0 + i4))
-                                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
-                        sx[0] = v.x, sx[1] = v.y, sx[2] = v.z, sx[3] = v.w;
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) sx[j] = i4 + j < mlim ? __ldg(p.sa + m0 + i4 + j) : 0.f;
-                    }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        float y = __fmul_rn(__int2float_rn(acc[i4 + j]), __fmul_rn(sx[j], swn));
-                        if (has_bias) y = __fadd_rn(y, bn);
-                        acc[i4 + j] = __float_as_int(y);
-                    }
-                }
-                const int buf = g & 1;
-                if (!warp_wait(bar(L::BAR_ACC_FULL + buf), (g >> 1) & 1, abort_flag, p.err, p.wait_limit_ns)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * TT + h * 128);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t r[16];
-                    tmem_ld16(taddr + 16 * j, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        acc[16 * j + i] = __float_as_int(__fadd_rn(__int_as_float(acc[16 * j + i]), __uint_as_float(r[i])));
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::BAR_ACC_EMPTY + buf));
-                ++g;
-            }
             epi_store<MODE>(acc, n, m0, mlim, full, p);
         }
         end_barrier();
@@ -718,11 +647,55 @@ __device__ __forceinline__ void epi_store_staged(const int (&acc)[128], int n, i
     }
 }
 
+// The bypass mode's last chunk of a tile (thread = weight row n, tokens m0 ..
+// m0 + 127): TMEM holds c = that chunk's integer sum + the bypass term in
+// accumulator units, L / (dx * dw); v = fl(float(acc) + c) and y = v * (dx *
+// dw) + bias, left as fp32 bits in acc.  With a zero term and |acc| < 2^24
+// (float(acc) exact) v = float(acc + c), so y is the plain mode's float(acc) *
+// (sx * sw) + bias bit for bit (where sx or sw is 0 the codes, and so acc, are
+// zero).  Writing c exactly as rint(c) + (c - rint(c)) would keep that for
+// any |acc|, but its two more conversions per value cost 2% of the GEMM in
+// this drain, which holds the TMEM buffer; the host runs the plain forward
+// for a zero coefficient instead.  The 128 token scales come in with four
+// coalesced loads and reach every lane by shuffles (a load per value measured
+// 2x slower).
+__device__ __forceinline__ void lora_fold_chunk(int (&acc)[128], uint32_t taddr, int n, int m0, int lane,
+                                                const GemmArgs &p) {
+    const float swn = n < p.N && CR_SPAN(n, 1, p.N) ? __ldg(p.sb + n) : 0.f;
+    const float dw = swn != 0.f ? swn : 1.f;
+    const bool has_bias = p.bias != nullptr && n < p.N;
+    const float bn = has_bias ? bf16_bits_to_float(__ldg(p.bias + n)) : 0.f;
+    float sxr[4];  // lane l: the scales of tokens m0 + 32 u + l
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int m = m0 + 32 * u + lane;
+        sxr[u] = m < p.M && CR_SPAN(m, 1, p.M) ? __ldg(p.sa + m) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t r[16];
+        tmem_ld16(taddr + 16 * j, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            const int i = 16 * j + t;
+            const float sxm = __shfl_sync(0xffffffffu, sxr[i >> 5], i & 31);
+            const float v = __fadd_rn(__int2float_rn(acc[i]), __uint_as_float(r[t]));
+            const float dx = sxm != 0.f ? sxm : 1.f;
+            float y = __fmul_rn(v, __fmul_rn(dx, dw));
+            if (has_bias) y = __fadd_rn(y, bn);
+            acc[i] = __float_as_int(y);
+        }
+    }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmXh, const __grid_constant__ CUtensorMap tmW,
+                     const __grid_constant__ CUtensorMap tmXA, const __grid_constant__ CUtensorMap tmLB,
                      const GemmArgs p) {
-    static_assert(MODE == kModeDequantW16 || MODE == kModeBf16 || MODE == kModeScaleF32, "pair modes");
+    static_assert(MODE == kModeDequantW16 || MODE == kModeBf16 || MODE == kModeScaleF32 || MODE == kModeDequantW16Lora,
+                  "pair modes");
     using namespace pair;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -765,6 +738,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int num_tiles = num_t * num_w2;
     const int num_kb = (p.K + BK - 1) / BK;
     const int chunk_kb = MODE == kModeBf16 ? num_kb : CHUNK_KB;
+    // the bypass mode's extra K block per tile (tmXA / tmLB: the parts of xa / dx and
+    // B / dw, 128 bytes per row); it joins the tile's last chunk
+    constexpr int kExtra = MODE == kModeDequantW16Lora ? 1 : 0;
 
     if (warp < 4) {
         regs_dec<REGS_WG0>();
@@ -773,12 +749,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // this CTA's token and weight halves of each stage, onto the leader's barrier
             asm volatile("prefetch.tensormap [%0];" ::"l"(&tmXh) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(&tmW) : "memory");
+            if (kExtra) {
+                asm volatile("prefetch.tensormap [%0];" ::"l"(&tmXA) : "memory");
+                asm volatile("prefetch.tensormap [%0];" ::"l"(&tmLB) : "memory");
+            }
             int it = 0, skipped = -1;
             bool ok = true;
             for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
                 int tb, wb2;
                 tile_coords(tile, num_t, num_w2, p.group, p.group_weight != 0, tb, wb2);
-                for (int kb = 0; kb < num_kb; ++kb, ++it) {
+                for (int kb = 0; kb < num_kb + kExtra; ++kb, ++it) {
                     const int s = it % STAGES;
                     if (!mbar_wait(bar(BAR_EMPTY + s), ((it / STAGES) & 1) ^ 1, abort_flag, p.err, p.wait_limit_ns)) {
                         ok = false;
@@ -789,8 +769,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     // self-test: the named operand's copies of this stage are never issued
                     const bool skip_x = it == p.fault_skip_it && p.fault_role == 0;
                     const bool skip_w = it == p.fault_skip_it && p.fault_role == 1;
-                    if (!skip_x) tma_load_2d_pair(sX + s * XH_STAGE, &tmXh, full, kb * BK, tb * TT + (int)rank * (TT / 2));
-                    if (!skip_w) tma_load_2d_pair(sW + s * W_STAGE, &tmW, full, kb * BK, (wb2 * 2 + (int)rank) * TW);
+                    const bool extra = kExtra && kb == num_kb;  // same box sizes: 128 rows x 128 bytes
+                    if (!skip_x)
+                        tma_load_2d_pair(sX + s * XH_STAGE, extra ? &tmXA : &tmXh, full, extra ? 0 : kb * BK,
+                                         tb * TT + (int)rank * (TT / 2));
+                    if (!skip_w)
+                        tma_load_2d_pair(sW + s * W_STAGE, extra ? &tmLB : &tmW, full, extra ? 0 : kb * BK,
+                                         (wb2 * 2 + (int)rank) * TW);
                     if (skip_x || skip_w) skipped = it;
                 }
             }
@@ -808,8 +793,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t dcol = 0;
             constexpr uint32_t kIdesc = MODE == kModeBf16 ? kIdescPairBF16 : kIdescPairF16;
             for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
-                for (int kb = 0; kb < num_kb; ++kb, ++it) {
-                    const int kc = kb % chunk_kb;
+                for (int kb = 0; kb < num_kb + kExtra; ++kb, ++it) {
+                    const bool extra = kExtra && kb == num_kb;
+                    const int kc = extra ? 1 : kb % chunk_kb;  // the bypass block opens no chunk
                     if (kc == 0) {
                         const int buf = g & 1;
                         if (!mbar_wait(bar(BAR_ACC_EMPTY + buf), ((g >> 1) & 1) ^ 1, abort_flag, p.err,
@@ -826,14 +812,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         break;
                     }
                     tc_fence_after();
+                    if (extra) {
+                        // parts at byte offsets 0 (hi), 32 (mid), 64 (lo) of each 128-byte row, onto
+                        // the chunk's integer sum: hi*hi, hi*mid, mid*hi, hi*lo, mid*mid, lo*hi
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = sw128_desc(sW + s * W_STAGE + kk * 32);
-                        const uint64_t bd = sw128_desc(sX + s * XH_STAGE + kk * 32);
-                        umma_f16_pair(tmem + dcol, ad, bd, kIdesc, (kc > 0 || kk > 0) ? 1u : 0u);
+                        for (int q = 0; q < 6; ++q) {
+                            const int pa = q == 2 || q == 4 ? 1 : q == 5 ? 2 : 0;  // weight side
+                            const int pb = q == 1 || q == 4 ? 1 : q == 3 ? 2 : 0;  // token side
+                            const uint64_t ad = sw128_desc(sW + s * W_STAGE + pa * 32);
+                            const uint64_t bd = sw128_desc(sX + s * XH_STAGE + pb * 32);
+                            umma_f16_pair(tmem + dcol, ad, bd, kIdescPairBF16, 1u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            const uint64_t ad = sw128_desc(sW + s * W_STAGE + kk * 32);
+                            const uint64_t bd = sw128_desc(sX + s * XH_STAGE + kk * 32);
+                            umma_f16_pair(tmem + dcol, ad, bd, kIdesc, (kc > 0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     umma_commit_both(bar(BAR_EMPTY + s));
-                    if (kc == chunk_kb - 1 || kb == num_kb - 1) {
+                    // a chunk closes after its 16th K block or the tile's last block (the
+                    // bypass block, when there is one)
+                    const bool close = extra || (kb == num_kb - 1 ? !kExtra : kc == chunk_kb - 1);
+                    if (close) {
                         umma_commit_both(bar(BAR_ACC_FULL + (g & 1)));
                         ++g;
                     }
@@ -858,6 +860,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int tile = pair_id; tile < num_tiles && ok; tile += num_pairs) {
             int tb, wb2;
             tile_coords(tile, num_t, num_w2, p.group, p.group_weight != 0, tb, wb2);
+            const int n = (wb2 * 2 + (int)rank) * TW + 32 * q + lane;  // weight row (TMEM lane)
+            const int mt = tb * TT + h * 128;                            // first token of the half
             int acc[128];
 #pragma unroll
             for (int i = 0; i < 128; ++i) acc[i] = 0;
@@ -870,17 +874,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 tc_fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * TT + h * 128);
+                if (kExtra && ch == nchunks - 1) {
+                    lora_fold_chunk(acc, taddr, n, mt, lane, p);
+                } else {
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    uint32_t r[16];
-                    tmem_ld16(taddr + 16 * j, r);
-                    tmem_wait_ld();
-                    if constexpr (MODE == kModeBf16) {  // one chunk: keep the fp32 bits
+                    for (int j = 0; j < 8; ++j) {
+                        uint32_t r[16];
+                        tmem_ld16(taddr + 16 * j, r);
+                        tmem_wait_ld();
+                        if constexpr (MODE == kModeBf16) {  // one chunk: keep the fp32 bits
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[16 * j + i] = (int)r[i];
-                    } else {
+                            for (int i = 0; i < 16; ++i) acc[16 * j + i] = (int)r[i];
+                        } else {
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[16 * j + i] += __float2int_rn(__uint_as_float(r[i]));
+                            for (int i = 0; i < 16; ++i) acc[16 * j + i] += __float2int_rn(__uint_as_float(r[i]));
+                        }
                     }
                 }
                 tc_fence_before();
@@ -888,14 +896,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8u * (uint32_t)buf);
             }
             if (!ok) break;
-            const int n = (wb2 * 2 + (int)rank) * TW + 32 * q + lane;
-            const int m0 = tb * TT + h * 128;
+            const int m0 = mt;
             const int mlim = p.M - m0;
-            if ((MODE == kModeDequantW16 || MODE == kModeBf16) && mlim >= 128 && n - lane + 32 <= p.N)
-                epi_store_staged<MODE>(acc, n, m0, p, reinterpret_cast<uint16_t *>(smem + OFF_STG + (warp - 8) * STG_BYTES),
-                                       lane);
+            // the bypass mode's registers hold y's fp32 bits, stored as the bf16 mode stores them
+            constexpr int SMODE = MODE == kModeDequantW16Lora ? kModeBf16 : MODE;
+            if ((SMODE == kModeDequantW16 || SMODE == kModeBf16) && mlim >= 128 && n - lane + 32 <= p.N)
+                epi_store_staged<SMODE>(acc, n, m0, p,
+                                        reinterpret_cast<uint16_t *>(smem + OFF_STG + (warp - 8) * STG_BYTES), lane);
             else
-                epi_store<MODE>(acc, n, m0, mlim, mlim >= 128, p);
+                epi_store<SMODE>(acc, n, m0, mlim, mlim >= 128, p);
         }
         end_barrier();
     }
@@ -929,24 +938,25 @@ void choose_raster(int64_t num_t, int64_t num_w, int64_t K, int64_t w_elem, int 
     group = (int)(group_weight ? gw : gt);
 }
 
-// tmXA / tmLB: the bypass parts (bypass mode only; other modes pass any map, unused).
 template <int MODE>
 cudaError_t launch_mode(const CUtensorMap &tmX, const CUtensorMap &tmW, const GemmArgs &p, int64_t tiles,
-                        cudaStream_t st, const CUtensorMap *tmXA = nullptr, const CUtensorMap *tmLB = nullptr) {
+                        cudaStream_t st) {
     const int sms = sm_count();
     const int grid = (int)(tiles < sms ? tiles : sms);
     constexpr int kSmem = Layout<MODE>::SMEM_BYTES;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gemm_s8_tc_kernel<MODE>), kSmem);
     if (e != cudaSuccess) return e;
-    gemm_s8_tc_kernel<MODE><<<grid, NUM_THREADS, kSmem, st>>>(tmX, tmW, tmXA ? *tmXA : tmX, tmLB ? *tmLB : tmW, p);
+    gemm_s8_tc_kernel<MODE><<<grid, NUM_THREADS, kSmem, st>>>(tmX, tmW, p);
     return cudaGetLastError();
 }
 
 
 // The CTA-pair kernel: clusters of two CTAs, one pair per two SMs.  A is the
 // token matrix (encoded here with a box of 128 rows: each CTA loads half a tile).
+// tmXA / tmLB: the bypass parts (bypass mode only; other modes pass none).
 template <int MODE>
-cudaError_t launch_pair(CUtensorMapDataType dt, const void *A, const CUtensorMap &tmW, GemmArgs p, cudaStream_t st) {
+cudaError_t launch_pair(CUtensorMapDataType dt, const void *A, const CUtensorMap &tmW, GemmArgs p, cudaStream_t st,
+                        const CUtensorMap *tmXA = nullptr, const CUtensorMap *tmLB = nullptr) {
     CUtensorMap tmXh;
     if (!encode_2d(&tmXh, dt, 2, A, (uint64_t)p.K, (uint64_t)p.M, BK, TT / 2, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
@@ -973,7 +983,7 @@ cudaError_t launch_pair(CUtensorMapDataType dt, const void *A, const CUtensorMap
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<MODE>, tmXh, tmW, p);
+    e = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<MODE>, tmXh, tmW, tmXA ? *tmXA : tmXh, tmLB ? *tmLB : tmW, p);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -1004,17 +1014,11 @@ cudaError_t launch_gemm_w16(const uint16_t *A, const float *sa, const uint16_t *
     if (M == 0 || N == 0) return cudaSuccess;
     cudaError_t e = get_encoder();
     if (e != cudaSuccess) return e;
-    CUtensorMap tmX, tmW;
-    if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, (uint64_t)K, (uint64_t)M, BK, TT,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B16, (uint64_t)K, (uint64_t)N, BK, TW,
+    CUtensorMap tmW;
+    if (!encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B16, (uint64_t)K, (uint64_t)N, BK, TW,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    const int64_t num_t = (M + TT - 1) / TT, num_w = (N + TW - 1) / TW;
-    int group, group_weight;
-    choose_raster(num_t, num_w, K, 2, group, group_weight);
-    GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, sa, sb, bias, out, err};
-    (void)tmX;
+    GemmArgs p{(int)M, (int)N, (int)K, 0, 0, sa, sb, bias, out, err};  // the raster is the launcher's
     return launch_pair<kModeDequantW16>(CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, tmW, p, st);
 }
 
@@ -1024,21 +1028,16 @@ cudaError_t launch_gemm_w16_lora(const uint16_t *A, const float *sa, const uint1
     if (M == 0 || N == 0) return cudaSuccess;
     cudaError_t e = get_encoder();
     if (e != cudaSuccess) return e;
-    CUtensorMap tmX, tmW, tmXA, tmLB;
-    if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, (uint64_t)K, (uint64_t)M, BK, TT,
+    CUtensorMap tmW, tmXA, tmLB;  // parts: 128-row boxes, one CTA's half of the pair's tile
+    if (!encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B16, (uint64_t)K, (uint64_t)N, BK, TW,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B16, (uint64_t)K, (uint64_t)N, BK, TW,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmXA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xa_parts, kLoraPartsRow, (uint64_t)M, BK, TT,
+        !encode_2d(&tmXA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, xa_parts, kLoraPartsRow, (uint64_t)M, BK, TT / 2,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmLB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, b_parts, kLoraPartsRow, (uint64_t)N, BK, TW,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    const int64_t num_t = (M + TT - 1) / TT, num_w = (N + TW - 1) / TW;
-    int group, group_weight;
-    choose_raster(num_t, num_w, K, 2, group, group_weight);
-    GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, sa, sb, bias, out, err};
-    return launch_mode<kModeDequantW16Lora>(tmX, tmW, p, num_t * num_w, st, &tmXA, &tmLB);
+    GemmArgs p{(int)M, (int)N, (int)K, 0, 0, sa, sb, bias, out, err};  // the raster is the launcher's
+    return launch_pair<kModeDequantW16Lora>(CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, tmW, p, st, &tmXA, &tmLB);
 }
 
 cudaError_t launch_gemm_w16_scale_f32(const uint16_t *A, const float *sa, const uint16_t *B16, int64_t M, int64_t N,
@@ -1046,17 +1045,11 @@ cudaError_t launch_gemm_w16_scale_f32(const uint16_t *A, const float *sa, const 
     if (M == 0 || N == 0) return cudaSuccess;
     cudaError_t e = get_encoder();
     if (e != cudaSuccess) return e;
-    CUtensorMap tmX, tmW;
-    if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, A, (uint64_t)K, (uint64_t)M, BK, TT,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B16, (uint64_t)K, (uint64_t)N, BK, TW,
+    CUtensorMap tmW;
+    if (!encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, B16, (uint64_t)K, (uint64_t)N, BK, TW,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    const int64_t num_t = (M + TT - 1) / TT, num_w = (N + TW - 1) / TW;
-    int group, group_weight;
-    choose_raster(num_t, num_w, K, 2, group, group_weight);
-    GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, sa, nullptr, nullptr, out, err};
-    (void)tmX;
+    GemmArgs p{(int)M, (int)N, (int)K, 0, 0, sa, nullptr, nullptr, out, err};  // the raster is the launcher's
     return launch_pair<kModeScaleF32>(CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, tmW, p, st);
 }
 
@@ -1090,17 +1083,11 @@ cudaError_t launch_gemm_bf16(const uint16_t *A, const uint16_t *B, int64_t M, in
     if (M == 0 || N == 0) return cudaSuccess;
     cudaError_t e = get_encoder();
     if (e != cudaSuccess) return e;
-    CUtensorMap tmX, tmW;
-    if (!encode_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, A, (uint64_t)K, (uint64_t)M, BK, TT,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, (uint64_t)K, (uint64_t)N, BK, TW,
+    CUtensorMap tmW;
+    if (!encode_2d(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, B, (uint64_t)K, (uint64_t)N, BK, TW,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    const int64_t num_t = (M + TT - 1) / TT, num_w = (N + TW - 1) / TW;
-    int group, group_weight;
-    choose_raster(num_t, num_w, K, 2, group, group_weight);
-    GemmArgs p{(int)M, (int)N, (int)K, group, group_weight, nullptr, nullptr, nullptr, out, err};
-    (void)tmX;
+    GemmArgs p{(int)M, (int)N, (int)K, 0, 0, nullptr, nullptr, nullptr, out, err};  // the raster is the launcher's
     return launch_pair<kModeBf16>(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, tmW, p, st);
 }
 

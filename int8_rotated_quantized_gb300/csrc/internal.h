@@ -55,23 +55,25 @@ cudaError_t launch_gemm(const uint16_t *A, const float *sa, const int8_t *B, con
 cudaError_t launch_gemm_w16(const uint16_t *A, const float *sa, const uint16_t *B16, const float *sb,
                             const uint16_t *bias, int64_t M, int64_t N, int64_t K, uint16_t *out, unsigned *err,
                             cudaStream_t st);
-// The same with the LoRA bypass term y += sum_j xa[m, j] lora_b[n, j]: both
-// operands as three bf16 parts per value (kLoraPartsRow = 64 bf16 per row: hi
-// at columns 0-15, mid at 16-31, lo at 32-47, zeros at 48-63; j >= rank zero),
-// xa_parts [M][64] and b_parts [N][64] from launch_lora_operands.  The GEMM
-// adds the term as one more K block per tile on the tensor cores.
+// The same with the LoRA bypass term y += sum_j xa[m, j] lora_b[n, j]: the
+// operands divided by the output's scales (xa[m] / dx[m], lora_b[n] / dw[n], d
+// = the scale or 1 where it is 0) as three bf16 parts per value
+// (kLoraPartsRow = 64 bf16 per row: hi at columns 0-15, mid at 16-31, lo at
+// 32-47, zeros at 48-63; j >= rank zero), xa_parts [M][64] and b_parts [N][64]
+// from launch_lora_operands.  The GEMM adds the term to each tile's last
+// integer chunk as one more K block on the tensor cores.
 constexpr int kLoraPartsRow = 64;
 cudaError_t launch_gemm_w16_lora(const uint16_t *A, const float *sa, const uint16_t *B16, const float *sb,
                                  const uint16_t *bias, const uint16_t *xa_parts, const uint16_t *b_parts, int64_t M,
                                  int64_t N, int64_t K, uint16_t *out, unsigned *err, cudaStream_t st);
 // K spans of the tensor-core down-projection for M rows of length K (lora_down.cu).
 int lora_down_spans(int64_t M, int64_t K);
-// The bypass operands (lora_down.cu): ap [48, K] bf16 (the parts of A's rows),
-// b_parts [N][64], part [spans][M][48] fp32 (scratch), and xa_parts [M][64] =
-// the parts of coef * x A^T computed on the tensor cores.  K % 32 == 0.
-cudaError_t launch_lora_operands(const uint16_t *x, int64_t M, int64_t K, const float *A, const float *B, int64_t N,
-                                 int rank, float coef, uint16_t *ap, uint16_t *xa_parts, uint16_t *b_parts,
-                                 float *part, unsigned *err, cudaStream_t st);
+// The bypass operands (lora_down.cu), one cluster kernel: b_parts [N][64] (the
+// parts of B[n] / dw[n]) and xa_parts [M][64] = the parts of (coef * x A^T)[m]
+// / dx[m], the product computed on the tensor cores.  K % 32 == 0.
+cudaError_t launch_lora_operands(const uint16_t *x, const float *scale_x, int64_t M, int64_t K, const float *A,
+                                 const float *B, const float *scale_w, int64_t N, int rank, float coef,
+                                 uint16_t *xa_parts, uint16_t *b_parts, unsigned *err, cudaStream_t st);
 // int8 codes -> fp16 values holding the same integers, 32 per thread (rotq_wide.cu).
 cudaError_t launch_widen_codes(const int8_t *A, int64_t count, uint16_t *out, cudaStream_t st);
 

@@ -143,7 +143,7 @@ def test_checked_linear_fwd(M, K, N, block, bias):
     _both(lambda: cr.convrot_linear_fwd_noalloc(x, Wq, s, block, bias=b))
 
 
-@pytest.mark.parametrize("M,K,N,rank", [(300, 1024, 272, 16), (65, 512, 128, 5)])
+@pytest.mark.parametrize("M,K,N,rank", [(300, 1024, 272, 16), (65, 512, 128, 5), (5, 256, 4096, 16)])
 def test_checked_linear_fwd_lora(M, K, N, rank):
     block = 128
     W = synth.normal_bf16(12, synth.STREAM_W, N, K, 0.02)

@@ -276,10 +276,13 @@ def test_widened_weight_path_is_bit_identical(M, K, N):
 
 @pytest.mark.parametrize("M,K,N,rank,with_bias", [(300, 1024, 272, 16, False), (65, 512, 128, 5, True),
                                                    (513, 4096, 400, 16, True), (65, 256, 128, 8, False),
-                                                   (40, 1056, 96, 16, True)])
+                                                   (40, 1056, 96, 16, True), (5, 256, 4096, 16, True),
+                                                   (1, 512, 2064, 3, False)])
 def test_linear_fwd_lora_bypass_parity(M, K, N, rank, with_bias):
-    """Shapes cover one column span (K = 256), 2, 4 and 8 spans, and spans that do not
-    divide K (K = 1056: the last span is empty)."""
+    """Shapes cover one column span (K = 256), 2, 4 and 8 spans (the clusters of the
+    down-projection), spans that do not divide K (K = 1056: the last span is empty),
+    and few rows with many weight rows (the row tiles past M that only write B's
+    parts)."""
     b = 128 if K % 128 == 0 else 32
     x = synth.activations_bf16(21, M, K, 8, 30.0)
     W = synth.normal_bf16(21, synth.STREAM_W, N, K, 0.02)
@@ -306,6 +309,54 @@ def test_linear_fwd_lora_bypass_parity(M, K, N, rank, with_bias):
     if bias is not None:
         full = full + f64(bias)
     assert rel_fro(f64(yb), full) <= REL_FRO_BF16
+
+
+def test_linear_fwd_lora_zero_adapter_is_the_plain_forward():
+    """A zero B with a nonzero coefficient runs the bypass kernels with a zero
+    branch: the result equals the plain forward bit for bit (the integer sums
+    here stay below 2^24, where the fp32 addition of the last chunk is exact)."""
+    M, K, N, rank, b = 300, 1024, 400, 16, 128
+    x = synth.activations_bf16(25, M, K, 8, 30.0)
+    W = synth.normal_bf16(25, synth.STREAM_W, N, K, 0.02)
+    A, _ = synth.lora_pair(25, N, K, rank, 0.05)
+    B = np.zeros((N, rank), dtype=np.float32)
+    bias = torch_bf16(synth.normal_bf16(25, 9, 1, N, 0.5)[0])
+    wq, sw = oracle.quantize_weight(W, b)
+    y = cr.convrot_linear_fwd_lora(torch_bf16(x), _i8(wq), _f32(sw), b, _f32(A), _f32(B), 16.0, 1.0, bias=bias)
+    assert cr.convrot_get_error() == cr.OK
+    assert torch.equal(y, cr.convrot_linear_fwd(torch_bf16(x), _i8(wq), _f32(sw), b, bias=bias))
+
+
+@pytest.mark.parametrize("lora_sigma", [0.05, 2.0])
+def test_linear_fwd_lora_bypass_zero_rows_and_large_branch(lora_sigma):
+    """All-zero rows of x and of W (scale 0, codes 0): those outputs are bias +
+    the branch alone.  lora_sigma = 2 makes the branch larger than the base
+    product, so the branch carries most of each output.  scale = 0 still gives
+    the plain forward bit for bit, zero rows included."""
+    M, K, N, rank, b = 300, 1024, 400, 16, 128
+    x = synth.activations_bf16(23, M, K, 8, 30.0)
+    x[[3, 100, 299]] = 0
+    W = synth.normal_bf16(23, synth.STREAM_W, N, K, 0.02)
+    W[[5, 130, 399]] = 0
+    A, B = synth.lora_pair(23, N, K, rank, lora_sigma)
+    bias = synth.normal_bf16(23, 9, 1, N, 0.5)[0]
+    wq, sw = oracle.quantize_weight(W, b)
+    assert sw[5] == 0 and not wq[5].any()
+    args = (torch_bf16(x), _i8(wq), _f32(sw), b, _f32(A), _f32(B), 16.0)
+    y = cr.convrot_linear_fwd_lora(*args, 1.0, bias=torch_bf16(bias))
+    assert cr.convrot_get_error() == cr.OK
+    ref = oracle.linear_fwd_lora(x, wq, sw, b, A, B, 16.0, 1.0, bias)
+    yb = bits_of(y)
+    ulps = np.abs(yb.astype(np.int32) - ref.astype(np.int32))
+    same_sign = (yb >> 15) == (ref >> 15)
+    assert np.mean(ulps[same_sign] <= 1) > 0.999 and np.mean(yb == ref) > 0.9
+    zr = np.ix_([3, 100, 299], np.arange(N))
+    zc = np.ix_(np.arange(M), [5, 130, 399])
+    for sel in (zr, zc):
+        d = np.abs(yb[sel].astype(np.int32) - ref[sel].astype(np.int32))
+        assert np.all(d[(yb[sel] >> 15) == (ref[sel] >> 15)] <= 1)
+    y0 = cr.convrot_linear_fwd_lora(*args, 0.0, bias=torch_bf16(bias))
+    assert torch.equal(y0, cr.convrot_linear_fwd(torch_bf16(x), _i8(wq), _f32(sw), b, bias=torch_bf16(bias)))
 
 
 @pytest.mark.parametrize("case", range(8))
