@@ -314,6 +314,14 @@ __global__ void __launch_bounds__(tcdq::kThreads, 1)
                 const int L = j * 32 + lane;  // row 32 cw + L / 8, columns 16 (L % 8) .. + 15
                 v[j] = *reinterpret_cast<const uint4 *>(src + (32 * cw + (L >> 3)) * 128 + (L & 7) * 16);
             }
+            // The stage goes back to the TMA (an async-proxy write) only after these loads are performed:
+            // the fence depends on every loaded word and orders the generic accesses before the async ones.
+            // (Without it, with the codes resident in L2, the next copy could land in the stage before
+            // some lanes' loads were performed, and those lanes widened a row of a later tile.)
+            uint32_t dep = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) dep ^= v[j].x ^ v[j].y ^ v[j].z ^ v[j].w;
+            asm volatile("fence.proxy.async.shared::cta;" ::"r"(dep) : "memory");
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_Q8E + s));
             if (!warp_wait_b(bar(B_Q16E + c), ((it / kQ16Stages) & 1) ^ 1, abort_flag, err)) break;

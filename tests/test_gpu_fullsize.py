@@ -196,6 +196,29 @@ def test_train20k_forward_and_backward_full_size():
     assert rel_fro(f64(dx_s), f64(dy_rows) @ f64(w_rows_k)) <= REL_FRO_BF16
 
 
+def test_dequant_weight_t_on_l2_resident_codes_full_size():
+    """The transient transpose of the bf16 backward, made from codes the quantizer
+    has just written (resident in L2, so the copies into the kernel's int8 ring
+    land fast), and twice more after touching the codes again: every element of
+    every call equals the oracle.  (A stage handed back to the copy engine
+    before its loads were performed showed up only in this regime.)"""
+    wl = synth.WORKLOADS["train20k"]
+    K, N, b = wl["K"], wl["N"], wl["block"]
+    W = sg.normal_bf16(0, synth.STREAM_W, N, K, wl["w_sigma"], "cuda")
+    Wq, sw = cr.convrot_quantize_weight(W, b)
+    Ts = [cr.convrot_dequant_weight_t(Wq, sw, b)]
+    for _ in range(2):
+        Wq.add_(0)  # the codes back into L2
+        Ts.append(cr.convrot_dequant_weight_t(Wq, sw, b))
+    assert cr.convrot_get_error() == cr.OK
+    wq_np, sw_np = Wq.cpu().numpy(), sw.cpu().numpy()
+    Tb = [T.view(torch.int16).cpu().numpy().view(np.uint16) for T in Ts]
+    for kb in range(K // b):
+        ref = oracle.dequant_weight_t(np.ascontiguousarray(wq_np[:, kb * b:(kb + 1) * b]), sw_np, b)
+        for T in Tb:
+            np.testing.assert_array_equal(T[kb * b:(kb + 1) * b], ref)
+
+
 def test_train20k_bf16_backward_full_size():
     wl = synth.WORKLOADS["train20k"]
     M, K, N, b = wl["M"], wl["K"], wl["N"], wl["block"]
