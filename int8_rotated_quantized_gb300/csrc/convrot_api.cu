@@ -44,35 +44,6 @@ int device_setup(unsigned **err) {
     return CONVROT_OK;
 }
 
-// A second stream per device for work that may run beside the caller's stream
-// within one call, with the two events of a fork and a join (created on first
-// use, kept for the life of the process).  The high priority lets its blocks
-// in ahead of a bandwidth-bound kernel queued beside it.  Callers hold
-// g_side_mu while they enqueue a fork ... join sequence, so two host threads
-// never interleave their records of the same events.
-struct SideStream {
-    cudaStream_t st = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
-};
-SideStream g_side[kMaxDevices];
-std::mutex g_side_mu;
-
-SideStream *side_stream() {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    SideStream &s = g_side[dev];
-    if (s.st == nullptr) {
-        int lo = 0, hi = 0;
-        if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess ||
-            cudaStreamCreateWithPriority(&s.st, cudaStreamNonBlocking, hi) != cudaSuccess)
-            return nullptr;
-        if (cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming) != cudaSuccess)
-            return nullptr;
-    }
-    return &s;
-}
-
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 bool block_ok(int b) { return b == 8 || b == 16 || b == 32 || b == 64 || b == 128 || b == 256; }
 bool row_ok(int64_t K, int b) { return K > 0 && K % b == 0 && K % 16 == 0 && K <= CONVROT_MAX_ROW; }
@@ -305,21 +276,11 @@ int convrot_linear_fwd_lora(const uint16_t *x, int64_t M, int64_t K, const int8_
     uint16_t *b_parts = reinterpret_cast<uint16_t *>(lw + align256((size_t)M * parts_row));
     rc = quantize_act_impl(x, M, K, K, block, xq, sx, st);
     if (rc != CONVROT_OK) return rc;
-    {
-        // The bypass operands (a latency-bound pass) run on the side stream beside the weight-code widening
-        // (a bandwidth-bound pass); the GEMM waits for both.
-        std::lock_guard<std::mutex> lock(g_side_mu);
-        SideStream *side = side_stream();
-        if (side == nullptr) return CONVROT_ERR_CUDA;
-        if (cudaEventRecord(side->fork, st) != cudaSuccess || cudaStreamWaitEvent(side->st, side->fork, 0) != cudaSuccess)
-            return CONVROT_ERR_CUDA;
-        rc = cuda_status(convrot::launch_lora_operands(x, sx, M, K, lora_A, lora_B, scale_w, N, rank, coef, xa_parts,
-                                                       b_parts, err, side->st));
-        if (cudaEventRecord(side->join, side->st) != cudaSuccess) return CONVROT_ERR_CUDA;
-        if (rc == CONVROT_OK) rc = cuda_status(convrot::launch_widen_codes(Wq, N * K, w16, st));
-        if (cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess) return CONVROT_ERR_CUDA;  // joined on every path
-        if (rc != CONVROT_OK) return rc;
-    }
+    rc = cuda_status(
+        convrot::launch_lora_operands(x, sx, M, K, lora_A, lora_B, scale_w, N, rank, coef, xa_parts, b_parts, err, st));
+    if (rc != CONVROT_OK) return rc;
+    rc = cuda_status(convrot::launch_widen_codes(Wq, N * K, w16, st));
+    if (rc != CONVROT_OK) return rc;
     return cuda_status(
         convrot::launch_gemm_w16_lora(xq, sx, w16, scale_w, bias, xa_parts, b_parts, M, N, K, y, err, st));
 }
