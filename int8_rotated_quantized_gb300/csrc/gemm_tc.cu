@@ -25,11 +25,18 @@
 // per MMA compared with the opposite assignment.  The accumulator is therefore
 // the transposed tile (TMEM lane = weight row n, column = token m).
 //
-// CTA roles (512 threads, one persistent CTA per SM, 128 weight rows x 256
-// tokens per tile):
+// Two kernels.  gemm_s8_tc_kernel (one persistent CTA per SM) runs the modes
+// that widen the int8 weight codes inside the loop (int32 output, fused
+// dequantization) and is described here; gemm_pair_kernel (clusters of two
+// CTAs and the 2-SM MMA, further down) runs the modes whose weight tiles
+// arrive ready: codes widened beforehand, bf16 weights, the fp32-scaled
+// product, and the LoRA bypass.
+//
+// CTA roles of gemm_s8_tc_kernel (512 threads, 128 weight rows x 256 tokens
+// per tile):
 //   warp 0        TMA producer of the activation tiles (one lane)
 //   warp 1        TMEM allocator and MMA issuer (one lane)
-//   warp 2        TMA producer of the weight tiles (one lane)
+//   warp 2        TMA producer of the int8 weight tiles (one lane)
 //   warp 3        idle (completes warpgroup 0 for setmaxnreg)
 //   warps 4-7     int8 -> fp16 converters of the weight tiles
 //   warps 8-15    epilogue: TMEM -> registers, int32 accumulation, output
