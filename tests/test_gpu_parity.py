@@ -277,12 +277,14 @@ def test_widened_weight_path_is_bit_identical(M, K, N):
 @pytest.mark.parametrize("M,K,N,rank,with_bias", [(300, 1024, 272, 16, False), (65, 512, 128, 5, True),
                                                    (513, 4096, 400, 16, True), (65, 256, 128, 8, False),
                                                    (40, 1056, 96, 16, True), (5, 256, 4096, 16, True),
-                                                   (1, 512, 2064, 3, False)])
+                                                   (1, 512, 2064, 3, False), (33, 32, 48, 1, True),
+                                                   (70, 96, 272, 7, False)])
 def test_linear_fwd_lora_bypass_parity(M, K, N, rank, with_bias):
     """Shapes cover one column span (K = 256), 2, 4 and 8 spans (the clusters of the
     down-projection), spans that do not divide K (K = 1056: the last span is empty),
-    and few rows with many weight rows (the row tiles past M that only write B's
-    parts)."""
+    few rows with many weight rows (the row tiles past M that only write B's
+    parts), and K = 32 and 96 (a K block only half filled: zeros from the copies of x
+    and A), rank 1 and 7."""
     b = 128 if K % 128 == 0 else 32
     x = synth.activations_bf16(21, M, K, 8, 30.0)
     W = synth.normal_bf16(21, synth.STREAM_W, N, K, 0.02)
