@@ -31,61 +31,13 @@ namespace {
 
 constexpr int kMaxThreads = 512;
 
-// ------------------------------------------------------------------ loads --
-
-__device__ __forceinline__ void load8(const uint16_t *p, float (&e)[8]) {
-    uint4 v = __ldcs(reinterpret_cast<const uint4 *>(p));
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        e[2 * i] = __uint_as_float(w[i] << 16);
-        e[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
-}
-
 __device__ __forceinline__ float absv(float v) { return fabsf(v); }
 __device__ __forceinline__ float maxv(float a, float b) { return fmaxf(a, b); }
-
-template <typename CT>
-__device__ __forceinline__ void zero8(CT (&e)[8]) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) e[i] = CT(0);
-}
 
 // ------------------------------------------------------------------- FWHT --
 
 // In-register stages h = 1, 2, 4 on the 8 elements of one lane.
-template <typename CT>
-__device__ __forceinline__ void fwht8(CT (&e)[8]) {
-#pragma unroll
-    for (int h = 1; h < 8; h <<= 1) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            if ((i & h) == 0) {
-                CT a = e[i], c = e[i + h];
-                e[i] = a + c;
-                e[i + h] = a - c;
-            }
-        }
-    }
-}
-
-// Cross-lane stages h = 8, 16, ..., b/2 (lane xor masks 1 .. lanes/2).  Every
-// lane of the warp must call this with the same `lanes`.
-template <typename CT>
-__device__ __forceinline__ void fwht_lanes(CT (&e)[8], int lanes, int lane) {
-    for (int m = 1; m < lanes; m <<= 1) {
-        const bool upper = (lane & m) != 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            CT p = __shfl_xor_sync(0xffffffffu, e[i], m);
-            e[i] = upper ? (p - e[i]) : (e[i] + p);
-        }
-    }
-}
-
-template <>
-__device__ __forceinline__ void fwht8<float>(float (&e)[8]) {
+__device__ __forceinline__ void fwht8(float (&e)[8]) {
 #pragma unroll
     for (int i = 0; i < 8; i += 2) {  // h = 1 lies inside a pair: scalar
         const float a = e[i], c = e[i + 1];
@@ -98,8 +50,9 @@ __device__ __forceinline__ void fwht8<float>(float (&e)[8]) {
     addsub2(e[2], e[3], e[6], e[7]);
 }
 
-template <>
-__device__ __forceinline__ void fwht_lanes<float>(float (&e)[8], int lanes, int lane) {
+// Cross-lane stages h = 8, 16, ..., b/2 (lane xor masks 1 .. lanes/2).  Every
+// lane of the warp must call this with the same `lanes`.
+__device__ __forceinline__ void fwht_lanes(float (&e)[8], int lanes, int lane) {
     for (int m = 1; m < lanes; m <<= 1) {
         const float sg = (lane & m) ? -1.f : 1.f;
         float p[8];
@@ -146,23 +99,7 @@ __device__ __forceinline__ void quant_store(float (&e)[8], float inv, __half *ds
     *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// fp64 path (the one-off backward-weight preparation): round in fp32 after
-// converting the transform, with an explicit clamp.
-__device__ __forceinline__ int quant_code(float u, float inv) {
-    int q = __float2int_rn(__fmul_rn(u, inv));
-    return max(-127, min(127, q));
-}
-
-__device__ __forceinline__ void store_codes(int8_t *dst, const int (&q)[8]) {
-    uint32_t lo = 0, hi = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        lo |= (uint32_t)(q[i] & 0xff) << (8 * i);
-        hi |= (uint32_t)(q[i + 4] & 0xff) << (8 * i);
-    }
-    *reinterpret_cast<uint2 *>(dst) = make_uint2(lo, hi);
-}
-
+// fp16-held codes of 8 integers (the widening of int8 codes).
 __device__ __forceinline__ void store_codes(__half *dst, const int (&q)[8]) {
     uint32_t w[4];
 #pragma unroll
@@ -180,7 +117,6 @@ struct RotqArgs {
     int64_t rows, K, ldx;
     int lanes;          // b / 8
     int G;              // threads per row group (multiple of 32, <= 512)
-    double scale_coef;  // 1 / (127 sqrt(b))
     float scale_denom;  // fp32(127 sqrt(b))
     void *q;            // codes, row stride K
     float *scale;
@@ -190,13 +126,10 @@ struct RotqArgs {
     float coef;  // scale * alpha / rank
 };
 
-// Raw storage of one 8-element slot as loaded (bf16: one 16-byte vector;
-// fp64: four 16-byte vectors), so the next rows can be prefetched into
-// registers while the current ones are transformed.
-template <typename InT>
-struct Raw8;
-template <>
-struct Raw8<uint16_t> {
+// Raw storage of one 8-element slot of bf16 as loaded (one 16-byte vector), so
+// the next rows can be prefetched into registers while the current ones are
+// transformed.
+struct Raw8 {
     uint4 v;
     __device__ __forceinline__ void load(const uint16_t *p) { v = __ldcs(reinterpret_cast<const uint4 *>(p)); }
     __device__ __forceinline__ void zero() { v = make_uint4(0, 0, 0, 0); }
@@ -209,17 +142,17 @@ struct Raw8<uint16_t> {
         }
     }
 };
-// InT: element type of x (uint16_t = bf16 bits).  CT: arithmetic type of the
-// transform (float).  OutT: int8_t codes or __half-held codes.  S: 8-element
+// x is bf16 (uint16_t bits), the transform fp32.  OutT: int8_t codes or
+// __half-held codes.  S: 8-element
 // slots per thread.  RPT: rows held per thread group at once.  LORA: merge
 // W + coef * B@A (fp32, sequential fma over the rank, rounded to bf16) first.
 //
 // Persistent: each CTA walks row blocks (groups * RPT rows) with a grid
 // stride; the raw data of the next block is loaded before the current one is
 // transformed, so HBM reads overlap the arithmetic.
-template <typename InT, typename CT, typename OutT, int S, int RPT, bool LORA>
+template <typename OutT, int S, int RPT, bool LORA>
 __global__ void __launch_bounds__(kMaxThreads) rotq_rows_kernel(const RotqArgs a) {
-    __shared__ CT red[2][RPT][kMaxThreads / 32];
+    __shared__ float red[2][RPT][kMaxThreads / 32];
     const int G = a.G;
     const int g = threadIdx.x / G;
     const int t = threadIdx.x - g * G;
@@ -229,10 +162,10 @@ __global__ void __launch_bounds__(kMaxThreads) rotq_rows_kernel(const RotqArgs a
     const int64_t chunks = a.K >> 3;
     const int64_t rows_per_block = (int64_t)groups * RPT;
     const int64_t nblocks = (a.rows + rows_per_block - 1) / rows_per_block;
-    const InT *x = static_cast<const InT *>(a.x);
+    const uint16_t *x = static_cast<const uint16_t *>(a.x);
     const int wpg = G >> 5;
 
-    Raw8<InT> raw[RPT][S];
+    Raw8 raw[RPT][S];
     auto fetch = [&](int64_t blk) {
         const int64_t row0 = (blk * groups + g) * RPT;
 #pragma unroll
@@ -249,21 +182,17 @@ __global__ void __launch_bounds__(kMaxThreads) rotq_rows_kernel(const RotqArgs a
         }
     };
 
-    // The fp64 variant (one-off backward-weight preparation) has no register
-    // room for a second copy: it loads at the top of each block instead.
-    constexpr bool kPrefetch = sizeof(InT) == 2;
     int par = 0;
     int64_t blk = blockIdx.x;
-    if (kPrefetch && blk < nblocks) fetch(blk);
+    if (blk < nblocks) fetch(blk);
     for (; blk < nblocks; blk += gridDim.x, par ^= 1) {
         const int64_t row0 = (blk * groups + g) * RPT;
-        if (!kPrefetch) fetch(blk);
-        CT e[RPT][S][8];
+        float e[RPT][S][8];
 #pragma unroll
         for (int r = 0; r < RPT; ++r)
 #pragma unroll
             for (int s = 0; s < S; ++s) raw[r][s].unpack(e[r][s]);
-        if (kPrefetch && blk + gridDim.x < nblocks) fetch(blk + gridDim.x);
+        if (blk + gridDim.x < nblocks) fetch(blk + gridDim.x);
 
         if constexpr (LORA) {
             // W' = bf16(W + coef * sum_j B[n,j] A[j,k]) with d accumulated by
@@ -298,14 +227,14 @@ __global__ void __launch_bounds__(kMaxThreads) rotq_rows_kernel(const RotqArgs a
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         e[r][s][i] =
-                            __bfloat162float(__float2bfloat16_rn(__fmaf_rn(a.coef, d[r][i], (float)e[r][s][i])));
+                            __bfloat162float(__float2bfloat16_rn(__fmaf_rn(a.coef, d[r][i], e[r][s][i])));
             }
         }
 
-        CT amax[RPT];
+        float amax[RPT];
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
-            amax[r] = CT(0);
+            amax[r] = 0.f;
 #pragma unroll
             for (int s = 0; s < S; ++s) {
                 fwht8(e[r][s]);
@@ -320,7 +249,7 @@ __global__ void __launch_bounds__(kMaxThreads) rotq_rows_kernel(const RotqArgs a
         __syncthreads();
 #pragma unroll
         for (int r = 0; r < RPT; ++r) {
-            CT m = CT(0);
+            float m = 0.f;
             for (int w = 0; w < wpg; ++w) m = maxv(m, red[par][r][g * wpg + w]);
             amax[r] = m;
         }
@@ -330,35 +259,22 @@ __global__ void __launch_bounds__(kMaxThreads) rotq_rows_kernel(const RotqArgs a
             const int64_t row = row0 + r;
             if (row >= a.rows) continue;
             // The code decision is taken in fp32 on the fp32-rounded transform.
-            const float amax_f = (float)amax[r];
+            const float amax_f = amax[r];
             const float inv = amax_f > 0.f ? __fdiv_rn(127.f, amax_f) : 0.f;
-            // scale = amax_u / (127 sqrt(b)); fp32 on the hot path (fp64 issue
-            // is scarce on this GPU), fp64 in the fp64 variant.
-            if (t == 0 && CR_SPAN(row, 1, a.rows)) {
-                if constexpr (sizeof(CT) == 4)
-                    a.scale[row] = __fdiv_rn(amax_f, a.scale_denom);
-                else
-                    a.scale[row] = (float)((double)amax[r] * a.scale_coef);
-            }
+            // scale = amax_u / (127 sqrt(b)), in fp32
+            if (t == 0 && CR_SPAN(row, 1, a.rows)) a.scale[row] = __fdiv_rn(amax_f, a.scale_denom);
             OutT *qrow = static_cast<OutT *>(a.q) + row * a.K;
 #pragma unroll
             for (int s = 0; s < S; ++s) {
                 const int64_t c = (int64_t)s * G + t;
                 if (c >= chunks || !CR_SPAN(row * a.K + 8 * c, 8, a.rows * a.K)) continue;
-                if constexpr (sizeof(CT) == 4) {
-                    quant_store(e[r][s], inv, qrow + 8 * c);
-                } else {
-                    int q[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) q[i] = quant_code((float)e[r][s][i], inv);
-                    store_codes(qrow + 8 * c, q);
-                }
+                quant_store(e[r][s], inv, qrow + 8 * c);
             }
         }
     }
 }
 
-template <typename InT, typename CT, typename OutT, bool LORA>
+template <typename OutT, bool LORA>
 cudaError_t launch_rotq_t(const RotqArgs &base, int64_t rows, int64_t K, cudaStream_t st) {
     RotqArgs a = base;
     const int64_t chunks = K / 8;
@@ -384,14 +300,13 @@ cudaError_t launch_rotq_t(const RotqArgs &base, int64_t rows, int64_t K, cudaStr
     };
     // Rows held per thread group: enough independent 16-byte loads in flight
     // per SM for HBM, within the register budget of 512-thread CTAs.
-    constexpr bool dbl = sizeof(CT) == 8;
-    constexpr int R1 = LORA ? 4 : (dbl ? 1 : 2);
-    constexpr int R2 = LORA ? 2 : (dbl ? 1 : 2);
+    constexpr int R1 = LORA ? 4 : 2;
+    constexpr int R2 = 2;
     switch (S) {
-        case 1: return go(rotq_rows_kernel<InT, CT, OutT, 1, R1, LORA>, R1);
-        case 2: return go(rotq_rows_kernel<InT, CT, OutT, 2, R2, LORA>, R2);
-        case 4: return go(rotq_rows_kernel<InT, CT, OutT, 4, 1, LORA>, 1);
-        default: return go(rotq_rows_kernel<InT, CT, OutT, 8, 1, LORA>, 1);
+        case 1: return go(rotq_rows_kernel<OutT, 1, R1, LORA>, R1);
+        case 2: return go(rotq_rows_kernel<OutT, 2, R2, LORA>, R2);
+        case 4: return go(rotq_rows_kernel<OutT, 4, 1, LORA>, 1);
+        default: return go(rotq_rows_kernel<OutT, 8, 1, LORA>, 1);
     }
 }
 
@@ -508,7 +423,6 @@ cudaError_t launch_rotq_bf16(const uint16_t *x, int64_t rows, int64_t K, int64_t
     a.K = K;
     a.ldx = ldx;
     a.lanes = lanes_of(block);
-    a.scale_coef = 1.0 / (127.0 * sqrt((double)block));
     a.scale_denom = (float)(127.0 * sqrt((double)block));
     a.q = q;
     a.scale = scale;
@@ -516,9 +430,9 @@ cudaError_t launch_rotq_bf16(const uint16_t *x, int64_t rows, int64_t K, int64_t
     a.lora_B = lora_B;
     a.rank = rank;
     a.coef = coef;
-    if (lora_A != nullptr) return launch_rotq_t<uint16_t, float, int8_t, true>(a, rows, K, st);
-    if (out_f16) return launch_rotq_t<uint16_t, float, __half, false>(a, rows, K, st);
-    return launch_rotq_t<uint16_t, float, int8_t, false>(a, rows, K, st);
+    if (lora_A != nullptr) return launch_rotq_t<int8_t, true>(a, rows, K, st);
+    if (out_f16) return launch_rotq_t<__half, false>(a, rows, K, st);
+    return launch_rotq_t<int8_t, false>(a, rows, K, st);
 }
 
 cudaError_t launch_emb_lookup(const int64_t *ids, int64_t n, const int8_t *Eq, const float *scale_e, int64_t V,
