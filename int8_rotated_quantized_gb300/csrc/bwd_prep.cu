@@ -155,10 +155,12 @@ __global__ void __launch_bounds__(512) dequant_t_kernel(const int8_t *Wq, const 
 // fp32 accumulator, so U is the same exact integer transform as the butterflies
 // of dequant_t_kernel, and the rounding that follows is that kernel's.
 // Roles (512 threads, one CTA per SM, persistent over the tiles):
-//   warp 0 lane 0   the int8 tiles by TMA into a 3-stage ring (128 rows x 128 bytes);
+//   warp 0 lane 0   the int8 tiles by TMA into a 3-stage ring (128 rows x 128 bytes,
+//                   128B swizzle);
 //   warp 1          allocates TMEM; lane 0 issues the 8 MMAs of a tile (M = 128
 //                   columns k, N = 128 rows n, K = 128) into one of two 128-column
-//                   accumulators;
+//                   accumulators, with Hd read from TMEM (written once at the start by
+//                   warps 8-11), so that only the codes are read from shared memory;
 //   warps 4-7       widen the int8 tiles to fp16 in the MMA's 128B-swizzled layout
 //                   (2-stage ring), 32 rows per warp;
 //   warps 8-15      one TMEM lane (column k) per thread and 64 of the tile's rows n
@@ -176,8 +178,7 @@ constexpr int kQ8Stages = 3, kQ16Stages = 2;
 constexpr int kQ8Bytes = kT * kT;       // int8 tile, rows of 128 bytes
 constexpr int kQ16Bytes = kT * kT * 2;  // fp16 tile: 2 atoms of 128 rows x 128 bytes (64 columns each)
 constexpr int kOutBytes = kT * kT * 2;  // bf16 [k][n] tile: 2 boxes of 128 rows x 64 n
-constexpr int OFF_H = 0;                // Hd, same layout as a fp16 tile
-constexpr int OFF_Q8 = OFF_H + kQ16Bytes;
+constexpr int OFF_Q8 = 0;
 constexpr int OFF_Q16 = OFF_Q8 + kQ8Stages * kQ8Bytes;
 constexpr int OFF_OUT = OFF_Q16 + kQ16Stages * kQ16Bytes;
 constexpr int OFF_SC = OFF_OUT + 2 * kOutBytes;  // per epilogue warp: [2 buffers][sh, sl][64] floats
@@ -187,12 +188,36 @@ constexpr int B_Q8F = 0, B_Q8E = kQ8Stages, B_Q16F = 2 * kQ8Stages, B_Q16E = B_Q
 constexpr int OFF_MISC = OFF_BAR + NBARS * 8;
 constexpr int SMEM = OFF_MISC + 16 + 1024;  // + slack for 1024-byte alignment
 static_assert(SMEM <= 227 * 1024, "shared memory budget");
+// TMEM columns: two 128-column accumulators, then Hd (128 lanes = rows, 64 columns of fp16 pairs)
+constexpr int kTmemCols = 512, kTmemH = 2 * kT;
 // kind::f16: D fp32, A and B fp16, both K-major, N = 128 (bits 17-22: N >> 3), M = 128 (bits 24-28: M >> 4)
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kT >> 3) << 17) | ((uint32_t)(kT >> 4) << 24);
 }  // namespace tcdq
 
 __device__ __forceinline__ bool warp_wait_b(uint32_t bar, uint32_t parity, volatile int *abort_flag, unsigned *err) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, err));
+}
+
+// D += A . B with A (M = 128 rows, 16 fp16 of K per row in 8 columns) in tensor memory
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
+            d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// 32 consecutive columns of this warp's 32 TMEM lanes from 32 registers per thread
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+        "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
 }
 
 template <int B>
@@ -213,25 +238,6 @@ __global__ void __launch_bounds__(tcdq::kThreads, 1)
     const int ntn = (N + kT - 1) / kT, ntk = (K + kT - 1) / kT;
     const int tiles = ntn * ntk;
 
-    // Hd[r][c] = H_b[r mod b][c mod b] within a diagonal block, else 0; in the
-    // K-major operand layout (chunk j of row r at j ^ (r & 7) in its atom)
-    for (int idx = threadIdx.x; idx < kT * 16; idx += blockDim.x) {
-        const int r = idx >> 4, j = idx & 15;  // row r, columns 8j .. 8j + 7
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            uint32_t h2 = 0;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int c = 8 * j + 2 * e + h;
-                const uint32_t v = (r / B) != (c / B) ? 0u : (__popc(r & c & (B - 1)) & 1) ? 0xBC00u : 0x3C00u;
-                h2 |= v << (16 * h);
-            }
-            w[e] = h2;
-        }
-        *reinterpret_cast<uint4 *>(smem + OFF_H + (j >> 3) * (kT * 128) + r * 128 + (((j & 7) ^ (r & 7)) << 4)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < kQ8Stages; ++i) {
             mbar_init(bar(B_Q8F + i), 1);
@@ -251,15 +257,39 @@ __global__ void __launch_bounds__(tcdq::kThreads, 1)
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(2 * kT)
+                     "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Hd, written above, is read by the MMAs
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (warp >= 8 && warp < 12) {
+        // Hd[r][c] = H_b[r mod b][c mod b] within a diagonal block, else 0: row r = TMEM lane r, the
+        // pair c = 2i, 2i + 1 in column i (low half first); warp 8 + q writes lanes 32q .. 32q + 31
+        const int r = 32 * (warp & 3) + lane;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t w[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                uint32_t pair = 0;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int c = 64 * h + 2 * i + e;
+                    const uint32_t v = (r / B) != (c / B) ? 0u : (__popc(r & c & (B - 1)) & 1) ? 0xBC00u : 0x3C00u;
+                    pair |= v << (16 * e);
+                }
+                w[i] = pair;
+            }
+            tmem_st32(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kTmemH + 32 * h), w);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();  // Hd is in TMEM before the first MMA
+    tc_fence_after();
 
     if (warp == 0) {
         if (lane == 0) {  // ------------------------------------------ producer
@@ -291,8 +321,8 @@ __global__ void __launch_bounds__(tcdq::kThreads, 1)
 #pragma unroll
                 for (int ks = 0; ks < kT / 16; ++ks) {
                     const uint32_t off = (uint32_t)((ks >> 2) * (kT * 128) + (ks & 3) * 32);
-                    umma_f16(tmem + (uint32_t)(buf * kT), sw128_desc(base + OFF_H + off),
-                             sw128_desc(base + OFF_Q16 + c * kQ16Bytes + off), kIdesc, ks > 0 ? 1u : 0u);
+                    umma_f16_tmem_a(tmem + (uint32_t)(buf * kT), tmem + (uint32_t)(kTmemH + 8 * ks),
+                                    sw128_desc(base + OFF_Q16 + c * kQ16Bytes + off), kIdesc, ks > 0 ? 1u : 0u);
                 }
                 umma_commit(bar(B_Q16E + c));
                 umma_commit(bar(B_ACCF + buf));
@@ -302,6 +332,10 @@ __global__ void __launch_bounds__(tcdq::kThreads, 1)
         }
     } else if (warp >= 4 && warp < 8) {  // ------------------------------- widening
         const int cw = warp - 4;           // rows 32 cw .. 32 cw + 31 of each tile
+        // Load j of a lane: row 32 cw + 8 (j / 2) + rsub, codes 16 c16 .. 16 c16 + 15.  Each group of 8
+        // lanes takes 4 chunks of two rows whose positions mod 8 differ by xor 5, so its 16-byte reads of
+        // the swizzled int8 stage and its 16-byte fp16 writes each fall on 8 distinct bank groups.
+        const int rsub = (lane >> 3) ^ (((lane >> 2) & 1) * 5), csub = lane & 3;
         int it = 0;
         for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
             const int s = it % kQ8Stages, c = it % kQ16Stages;
@@ -311,8 +345,8 @@ __global__ void __launch_bounds__(tcdq::kThreads, 1)
             uint4 v[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const int L = j * 32 + lane;  // row 32 cw + L / 8, columns 16 (L % 8) .. + 15
-                v[j] = *reinterpret_cast<const uint4 *>(src + (32 * cw + (L >> 3)) * 128 + (L & 7) * 16);
+                const int r = 32 * cw + 8 * (j >> 1) + rsub, c16 = 4 * (j & 1) + csub;
+                v[j] = *reinterpret_cast<const uint4 *>(src + r * 128 + ((c16 ^ (r & 7)) << 4));
             }
             // The stage goes back to the TMA (an async-proxy write) only after these loads are performed:
             // the fence depends on every loaded word and orders the generic accesses before the async ones.
@@ -328,15 +362,14 @@ __global__ void __launch_bounds__(tcdq::kThreads, 1)
             uint8_t *dst = smem + OFF_Q16 + c * kQ16Bytes;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const int L = j * 32 + lane;
-                const int r = 32 * cw + (L >> 3), c16 = L & 7;
+                const int r = 32 * cw + 8 * (j >> 1) + rsub;
                 uint32_t w[8];
                 widen4(v[j].x, w[0], w[1]);
                 widen4(v[j].y, w[2], w[3]);
                 widen4(v[j].z, w[4], w[5]);
                 widen4(v[j].w, w[6], w[7]);
-                uint8_t *row = dst + (c16 >> 2) * (kT * 128) + r * 128;
-                const int jj = 2 * (c16 & 3);
+                uint8_t *row = dst + (j & 1) * (kT * 128) + r * 128;  // 64-column atom j & 1
+                const int jj = 2 * csub;
                 *reinterpret_cast<uint4 *>(row + ((jj ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
                 *reinterpret_cast<uint4 *>(row + (((jj + 1) ^ (r & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
             }
@@ -437,7 +470,7 @@ __global__ void __launch_bounds__(tcdq::kThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * kT) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
 }
 
@@ -450,7 +483,7 @@ cudaError_t launch_dequant_t_tc(const int8_t *Wq, const float *scale_w, int64_t 
     if (e != cudaSuccess) return e;
     CUtensorMap tmQ, tmT;
     if (!encode_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, Wq, (uint64_t)K, (uint64_t)N, tcdq::kT, tcdq::kT,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&tmT, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, T, (uint64_t)N, (uint64_t)K, 64, 32,
                    CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
