@@ -274,6 +274,26 @@ def test_widened_weight_path_is_bit_identical(M, K, N):
     np.testing.assert_array_equal(acc.cpu().numpy(), oracle.gemm_s32(A, wq_ref))
 
 
+def test_widened_gemm_row_slices_agree():
+    """Every output row of the widened-weight GEMM depends only on its own token row, so a large call (80
+    token tiles, a ragged last one, the raster of its shape) and calls on row slices of it (other tile
+    boundaries, other rasters, ragged first and last tiles) give the same rows bit for bit, and the fused
+    single-CTA kernel agrees."""
+    M, K, N, b = 20000, 256, 16384, 128
+    x = synth.activations_bf16(23, M, K, 8, 30.0)
+    W = synth.normal_bf16(23, synth.STREAM_W, N, K, 0.02)
+    Wq, sw = cr.convrot_quantize_weight(torch_bf16(W), b)
+    w16 = cr.convrot_widen_codes(Wq)
+    xq, sx = cr.convrot_quantize_activation(torch_bf16(x), b)
+    bias = torch_bf16(synth.normal_bf16(23, 9, 1, N, 0.5)[0])
+    y = cr.convrot_gemm_dequant_w16(xq, sx, w16, sw, bias=bias)
+    for r0, r1 in [(0, 4096), (M - 300, M), (7777, 7777 + 513)]:
+        ys = cr.convrot_gemm_dequant_w16(xq[r0:r1].clone(), sx[r0:r1].clone(), w16, sw, bias=bias)  # fresh, aligned
+        assert torch.equal(ys, y[r0:r1]), (r0, r1)
+    yf = cr.convrot_gemm_dequant(xq[:4096].clone(), sx[:4096].clone(), Wq, sw, bias=bias)
+    assert torch.equal(yf, y[:4096])
+
+
 @pytest.mark.parametrize("M,K,N,rank,with_bias", [(300, 1024, 272, 16, False), (65, 512, 128, 5, True),
                                                    (513, 4096, 400, 16, True), (65, 256, 128, 8, False),
                                                    (40, 1056, 96, 16, True), (5, 256, 4096, 16, True),
