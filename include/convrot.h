@@ -362,8 +362,10 @@ CONVROT_API int convrot_probe_mma_s8_rate(int iters, int32_t *sink, size_t sink_
  * every pipeline wait of the GEMM gives up after `limit_ns` (1 ns .. 10 s)
  * instead of 2 s, and the copy that `producer` (0: the activation tiles,
  * 1: the weight tiles) would issue at its iteration `skip_iteration` (counted
- * over the K blocks of the tiles a CTA processes, from 0) is never issued.  The
- * stage it would fill stays empty, so a consumer's bounded wait expires: every
+ * over the pipeline stages of the tiles a CTA or CTA pair processes, from 0: a
+ * stage holds one K block of 64 when widened = 0 and two when widened = 1) is
+ * never issued.  The stage it would fill stays empty, so a consumer's bounded
+ * wait expires: every
  * role of the CTA then stops, copies and MMAs in flight are drained, the
  * tensor memory is freed and the kernel returns.  The next convrot_get_error()
  * returns CONVROT_ERR_TIMEOUT; y is partly written; the context stays usable.

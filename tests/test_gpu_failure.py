@@ -56,10 +56,11 @@ def _gemm_fault(widened, xq, sx, W, sw, y, limit_ns, skip, producer):
                                                 cr._ptr(y), limit_ns, skip, producer, cr._stream(None))
 
 
-# (M, N, K, skip): one tile per CTA with the copy of K block 5 missing, and several tiles per
-# CTA (512 tiles on the SMs) with the copy missing in each CTA's third tile, after two tiles
-# have gone through the epilogue.
-@pytest.mark.parametrize("M,N,K,skip", [(1024, 512, 2048, 5), (4096, 4096, 1024, 2 * 16 + 3)])
+# (M, N, K, skip in tiles, stages): one tile per CTA with the copies of stage 5 missing, and
+# several tiles per CTA (or CTA pair) with the copies missing in its third tile, after two tiles
+# have gone through the epilogue. A stage holds one K block of 64 in the single-CTA kernel
+# (widened = 0) and two in the pair kernel (widened = 1).
+@pytest.mark.parametrize("M,N,K,skip", [(1024, 512, 2048, (0, 5)), (4096, 4096, 1024, (2, 3))])
 @pytest.mark.parametrize("widened", [0, 1])
 @pytest.mark.parametrize("producer", [0, 1])
 def test_gemm_abort_path_ends_at_the_limit_and_frees_the_sm(M, N, K, skip, widened, producer):
@@ -81,8 +82,9 @@ def test_gemm_abort_path_ends_at_the_limit_and_frees_the_sm(M, N, K, skip, widen
     assert _gemm_fault(widened, xq, sx, W, sw, y, 20_000_000, 1 << 30, producer) == cr.OK
     assert cr.convrot_get_error() == cr.OK
     assert torch.equal(y, before)
+    stages_per_tile = (K // 64) // (2 if widened else 1)
     t0 = time.perf_counter()
-    assert _gemm_fault(widened, xq, sx, W, sw, y, 20_000_000, skip, producer) == cr.OK
+    assert _gemm_fault(widened, xq, sx, W, sw, y, 20_000_000, skip[0] * stages_per_tile + skip[1], producer) == cr.OK
     assert cr.convrot_get_error() == cr.ERR_TIMEOUT
     assert time.perf_counter() - t0 < 1.5  # ended by the 20 ms limit, not the default 2 s
     assert cr.convrot_get_error() == cr.OK
