@@ -245,7 +245,7 @@ def test_gemm_dequant_on_oracle_codes(with_bias):
     assert np.mean(yb == y_ref) > 0.99
 
 
-@pytest.mark.parametrize("M,K,N", [(300, 1024, 400), (64, 256, 128), (513, 4096, 272)])
+@pytest.mark.parametrize("M,K,N", [(300, 1024, 400), (64, 256, 128), (513, 4096, 272), (129, 1088, 272)])
 def test_widened_weight_path_is_bit_identical(M, K, N):
     """The widened-weight path (fp16 copy of the codes in the workspace, GEMM without
     in-loop widening) and the fused path give the same bits; both match the oracle."""
@@ -538,7 +538,7 @@ def test_dequant_weight_t_rounding_midpoints():
     np.testing.assert_array_equal(got, ref)
 
 
-@pytest.mark.parametrize("M,N,K", [(300, 272, 1008), (64, 128, 64), (513, 400, 4096)])
+@pytest.mark.parametrize("M,N,K", [(300, 272, 1008), (64, 128, 64), (513, 400, 4096), (129, 272, 1040)])
 def test_gemm_bf16_parity(M, N, K):
     A = synth.normal_bf16(16, synth.STREAM_DY, M, K, 1.0)
     B = synth.normal_bf16(16, synth.STREAM_W, N, K, 0.05)
