@@ -121,7 +121,7 @@ CONVROT_API int convrot_quantize_activation(const uint16_t *x, int64_t M, int64_
  *   scale_x  fp32 [M], 16-byte aligned.
  *   Wq       int8 [N, K]; scale_w fp32 [N]; bias bf16 [N] or NULL.
  *   y        out bf16 [M, N] contiguous.
- * K multiple of 16 and <= 2^20; N multiple of 16. */
+ * K multiple of 16 and <= 2^17 (so |acc| < 2^31 for any codes); N multiple of 16. */
 CONVROT_API int convrot_gemm_dequant(const uint16_t *xq, const float *scale_x, int64_t M, int64_t K,
                          const int8_t *Wq, const float *scale_w, int64_t N, const uint16_t *bias,
                          uint16_t *y, convrot_stream_t stream);
@@ -134,7 +134,7 @@ CONVROT_API int convrot_widen_codes(const int8_t *q, int64_t count, uint16_t *ou
 
 /* convrot_gemm_dequant with the weight codes already widened to fp16 values
  * (Wq16 [N, K], from convrot_widen_codes): the same exact integer accumulation
- * and epilogue, without widening inside the GEMM. */
+ * and epilogue, without widening inside the GEMM.  Same limits. */
 CONVROT_API int convrot_gemm_dequant_w16(const uint16_t *xq, const float *scale_x, int64_t M, int64_t K,
                              const uint16_t *Wq16, const float *scale_w, int64_t N, const uint16_t *bias,
                              uint16_t *y, convrot_stream_t stream);

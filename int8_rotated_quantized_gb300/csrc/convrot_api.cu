@@ -46,6 +46,9 @@ int device_setup(unsigned **err) {
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 bool block_ok(int b) { return b == 8 || b == 16 || b == 32 || b == 64 || b == 128 || b == 256; }
+// Longest contraction of the integer GEMM entry points: 127 * 127 * 2^17 < 2^31, so the int32 accumulator
+// cannot overflow for any codes in [-127, 127].
+constexpr int64_t kMaxIntK = int64_t(1) << 17;
 bool row_ok(int64_t K, int b) { return K > 0 && K % b == 0 && K % 16 == 0 && K <= CONVROT_MAX_ROW; }
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
@@ -165,7 +168,7 @@ int convrot_quantize_activation(const uint16_t *x, int64_t M, int64_t K, int64_t
 int convrot_gemm_dequant(const uint16_t *xq, const float *scale_x, int64_t M, int64_t K, const int8_t *Wq,
                          const float *scale_w, int64_t N, const uint16_t *bias, uint16_t *y,
                          convrot_stream_t stream) {
-    CHECK(M >= 0 && N >= 0 && K > 0 && K % 16 == 0 && K <= (1 << 20) && N % 16 == 0);
+    CHECK(M >= 0 && N >= 0 && K > 0 && K % 16 == 0 && K <= kMaxIntK && N % 16 == 0);
     CHECK(M <= INT32_MAX && N <= INT32_MAX);
     CHECK(M == 0 || N == 0 ||
           (xq && scale_x && Wq && scale_w && y && aligned16(xq) && aligned16(Wq) && aligned16(y) &&
@@ -200,7 +203,7 @@ int convrot_widen_codes(const int8_t *q, int64_t count, uint16_t *out16, convrot
 int convrot_gemm_dequant_w16(const uint16_t *xq, const float *scale_x, int64_t M, int64_t K, const uint16_t *Wq16,
                              const float *scale_w, int64_t N, const uint16_t *bias, uint16_t *y,
                              convrot_stream_t stream) {
-    CHECK(M >= 0 && N >= 0 && K > 0 && K % 16 == 0 && K <= (1 << 20) && N % 16 == 0);
+    CHECK(M >= 0 && N >= 0 && K > 0 && K % 16 == 0 && K <= kMaxIntK && N % 16 == 0);
     CHECK(M <= INT32_MAX && N <= INT32_MAX);
     CHECK(M == 0 || N == 0 ||
           (xq && scale_x && Wq16 && scale_w && y && aligned16(xq) && aligned16(Wq16) && aligned16(y) &&
@@ -409,7 +412,7 @@ size_t convrot_gemm_s32_workspace_bytes(int64_t M, int64_t K) {
 
 int convrot_gemm_s32(const int8_t *A, const int8_t *B, int64_t M, int64_t N, int64_t K, int32_t *C, void *workspace,
                      size_t ws_bytes, convrot_stream_t stream) {
-    CHECK(M >= 0 && N >= 0 && K > 0 && K % 16 == 0 && K <= (1 << 17) && N % 16 == 0);
+    CHECK(M >= 0 && N >= 0 && K > 0 && K % 16 == 0 && K <= kMaxIntK && N % 16 == 0);
     CHECK(M <= INT32_MAX && N <= INT32_MAX);
     CHECK(M == 0 || N == 0 ||
           (A && B && C && workspace && aligned16(A) && aligned16(B) && aligned16(C) &&
@@ -430,7 +433,7 @@ int convrot_selftest_gemm_fault(int widened, const uint16_t *xq, const float *sc
                                 int64_t skip_iteration, int producer, convrot_stream_t stream) {
     CHECK(limit_ns > 0 && limit_ns <= 10000000000ull && (producer == 0 || producer == 1));
     CHECK(skip_iteration >= 0 && skip_iteration <= INT32_MAX && (widened == 0 || widened == 1));
-    CHECK(M >= 0 && N >= 0 && K > 0 && K % 16 == 0 && K <= (1 << 20) && N % 16 == 0);
+    CHECK(M >= 0 && N >= 0 && K > 0 && K % 16 == 0 && K <= kMaxIntK && N % 16 == 0);
     CHECK(M <= INT32_MAX && N <= INT32_MAX);
     CHECK(M == 0 || N == 0 ||
           (xq && scale_x && Wq && scale_w && y && aligned16(xq) && aligned16(Wq) && aligned16(y) &&

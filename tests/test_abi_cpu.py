@@ -98,8 +98,11 @@ def test_bad_shapes_are_rejected(L):
     assert L.convrot_linear_fwd(FAKE, 8, 256, FAKE, FAKE, 32, 32, None, FAKE, FAKE, need - 1, None) == 1
     assert L.convrot_linear_fwd(FAKE, 8, 256, FAKE, FAKE, 32, 32, None, FAKE, ctypes.c_void_p((1 << 20) + 16),
                                 need, None) == 1
-    # s32 entry: K beyond the int32-safe limit
+    # integer GEMM entries: K beyond the int32-safe limit (127 * 127 * K < 2^31 for K <= 2^17)
     assert L.convrot_gemm_s32(FAKE, FAKE, 1, 16, 1 << 18, FAKE, FAKE, 1 << 30, None) == 1
+    assert L.convrot_gemm_s32(FAKE, FAKE, 1, 16, (1 << 17) + 16, FAKE, FAKE, 1 << 30, None) == 1
+    assert L.convrot_gemm_dequant(FAKE, FAKE, 8, (1 << 17) + 16, FAKE, FAKE, 32, None, FAKE, None) == 1
+    assert L.convrot_gemm_dequant_w16(FAKE, FAKE, 8, (1 << 17) + 16, FAKE, FAKE, 32, None, FAKE, None) == 1
     # bf16 backward: N not a multiple of 16, K not a multiple of the block, workspace too small
     assert L.convrot_dequant_weight_t(FAKE, FAKE, 24, 256, 32, FAKE, None) == 1
     assert L.convrot_dequant_weight_t(FAKE, FAKE, 32, 80, 32, FAKE, None) == 1
