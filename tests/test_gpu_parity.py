@@ -76,6 +76,31 @@ def test_gemm_s32_extremes_cross_the_fp32_exact_range(K):
     assert abs(int(C[0, 1])) > 1 << 24 or K <= 1040
 
 
+def test_gemm_at_the_contraction_limit():
+    """K = 2^17, the longest contraction the integer GEMM entries accept: all-+-127 operands put sums at
+    127 * 127 * 2^17 = 2,114,060,288 in magnitude, still exact in int32. Checked on the int32 path and on the
+    widened-weight GEMM of the training step (2048 K blocks, 128 exact fp32 chunks per tile)."""
+    K = 1 << 17
+    M, N = 3, 32
+    A = np.full((M, K), 127, dtype=np.int8)
+    A[1] = -127
+    A[2, ::2] = -127
+    B = np.full((N, K), 127, dtype=np.int8)
+    B[1::2] = -127
+    B[2, 1::3] = -127
+    ref = oracle.gemm_s32(A, B)
+    assert int(np.abs(ref).max()) == 127 * 127 * K
+    np.testing.assert_array_equal(cr.convrot_gemm_s32(_i8(A), _i8(B)).cpu().numpy(), ref)
+    sx = np.full(M, 2.0 ** -24, dtype=np.float32)
+    sw = np.linspace(0.5, 2.0, N).astype(np.float32) * np.float32(2.0 ** -8)
+    y_ref = oracle.dequant(ref, sx, sw, None)
+    w16 = cr.convrot_widen_codes(_i8(B))
+    y = bits_of(cr.convrot_gemm_dequant_w16(torch.from_numpy(A.astype(np.float16)).cuda(), _f32(sx), w16, _f32(sw)))
+    ulps = np.abs(y.astype(np.int32) - y_ref.astype(np.int32))
+    assert np.all(ulps[(y >> 15) == (y_ref >> 15)] <= 1) and np.mean(y == y_ref) > 0.9
+    assert cr.convrot_get_error() == cr.OK
+
+
 def test_gemm_s32_random_signs_long_k():
     rng = np.random.default_rng(5)
     M, N, K = 140, 260 - 4, 16384 + 64
