@@ -323,13 +323,14 @@ def test_widened_gemm_row_slices_agree():
                                                    (513, 4096, 400, 16, True), (65, 256, 128, 8, False),
                                                    (40, 1056, 96, 16, True), (5, 256, 4096, 16, True),
                                                    (1, 512, 2064, 3, False), (33, 32, 48, 1, True),
-                                                   (70, 96, 272, 7, False)])
+                                                   (70, 96, 272, 7, False), (17, 32768, 272, 16, True)])
 def test_linear_fwd_lora_bypass_parity(M, K, N, rank, with_bias):
     """Shapes cover one column span (K = 256), 2, 4 and 8 spans (the clusters of the
     down-projection), spans that do not divide K (K = 1056: the last span is empty),
     few rows with many weight rows (the row tiles past M that only write B's
-    parts), and K = 32 and 96 (a K block only half filled: zeros from the copies of x
-    and A), rank 1 and 7."""
+    parts), K = 32 and 96 (a K block only half filled: zeros from the copies of x
+    and A), rank 1 and 7, and K = 32768, the longest row (spans of 4096, 32 integer
+    chunks per tile before the bypass block)."""
     b = 128 if K % 128 == 0 else 32
     x = synth.activations_bf16(21, M, K, 8, 30.0)
     W = synth.normal_bf16(21, synth.STREAM_W, N, K, 0.02)
@@ -342,9 +343,23 @@ def test_linear_fwd_lora_bypass_parity(M, K, N, rank, with_bias):
     ref = oracle.linear_fwd_lora(x, wq, sw, b, A, B, 16.0, 1.0, bias)
     yb = bits_of(y)
     assert rel_fro(f64(yb), f64(ref)) <= REL_FRO_ORACLE
-    ulps = np.abs(yb.astype(np.int32) - ref.astype(np.int32))
-    same_sign = (yb >> 15) == (ref >> 15)
-    assert np.mean(ulps[same_sign] <= 1) > 0.999 and np.mean(yb == ref) > 0.9
+    assert np.mean(yb == ref) > 0.9
+    # Every output within one bf16 step of the oracle's, plus what fp32 arithmetic leaves where the terms of
+    # y = acc * s_x * s_w + bias + L cancel: 2^-19 of the plain terms (as for the plain forward) and 2^-12 of the
+    # branch L, whose down-projection the GPU accumulates in fp32 over K (up to 32768 terms).
+    g, r = f64(yb), f64(ref)
+    step = np.exp2(np.floor(np.log2(np.maximum(np.maximum(np.abs(g), np.abs(r)), 2.0 ** -126))) - 7)
+    plain = f64(oracle.linear_fwd(x, wq, sw, b)[0])
+    branch = (16.0 / rank) * ((f64(x) @ A.T.astype(np.float64)) @ B.T.astype(np.float64))
+    cb = np.zeros(N) if bias is None else np.abs(f64(bias))
+    tol = step + 2.0 ** -19 * (np.abs(plain) + cb) + 2.0 ** -12 * np.abs(branch)
+    # on the token rows whose codes the GPU and the oracle agree on (they may differ by one at near-ties)
+    xq_gpu, _ = cr.convrot_quantize_activation(torch_bf16(x), b)
+    rows = np.all(xq_gpu.cpu().numpy().astype(np.int64) == oracle.quantize_rows_bf16(x, b)[0].astype(np.int64),
+                  axis=1)
+    assert rows.mean() > 0.9
+    bad = (np.abs(g - r) > tol) & rows[:, None]
+    assert not bad.any(), np.argwhere(bad)[:4]
     # scale 0: exactly the plain forward
     y0 = cr.convrot_linear_fwd_lora(torch_bf16(x), _i8(wq), _f32(sw), b, _f32(A), _f32(B), 16.0, 0.0,
                                     bias=None if bias is None else torch_bf16(bias))
@@ -692,7 +707,7 @@ def test_quantize_16_byte_aligned_input_takes_the_narrow_path():
     check_scales(sw.cpu().numpy(), s_ref)
 
 
-@pytest.mark.parametrize("D,block", [(48, 16), (4096, 128), (512, 256)])
+@pytest.mark.parametrize("D,block", [(48, 16), (4096, 128), (512, 256), (32768, 128)])
 def test_embedding_lookup_layouts(D, block):
     V = 300
     table = synth.normal_bf16(33, synth.STREAM_TABLE, V, D, 0.02)
