@@ -498,9 +498,10 @@ def test_linear_fwd_ragged_multi_tile():
 
 
 @pytest.mark.parametrize("block,K,N", [(32, 256, 768), (128, 256, 768), (16, 48, 400), (8, 80, 272), (64, 192, 320),
-                                       (256, 512, 512)])
+                                       (256, 512, 512), (128, 256, 32768)])
 def test_bwd_prep_and_grad_x_parity(block, K, N):
-    """Tiles of 128 (or b) weight rows and columns, ragged in both, every block size."""
+    """Tiles of 128 (or b) weight rows and columns, ragged in both, every block size, and N = 32768 (the longest
+    row of the backward weight and the longest contraction of grad_x)."""
     M = 150
     W = synth.normal_bf16(9, synth.STREAM_W, N, K, 0.02)
     wq, sw = oracle.quantize_weight(W, block)
@@ -533,7 +534,8 @@ def _check_bf16_sums(got_bits, ref_bits, K):
     assert rel_fro(g, r) <= REL_FRO_ORACLE
 
 
-@pytest.mark.parametrize("N,K,block", [(80, 256, 32), (192, 1024, 128), (16, 512, 256), (64, 64, 8), (48, 48, 16)])
+@pytest.mark.parametrize("N,K,block", [(80, 256, 32), (192, 1024, 128), (16, 512, 256), (64, 64, 8), (48, 48, 16),
+                                       (64, 32768, 128)])
 def test_dequant_weight_t_parity(N, K, block):
     W = synth.normal_bf16(15, synth.STREAM_W, N, K, 0.02)
     wq, sw = oracle.quantize_weight(W, block)
