@@ -176,7 +176,8 @@ def test_quantize_weight_with_row_stride(N, K, ld, block):
 # row kernel it falls back to (rank 24; K = 96).
 @pytest.mark.parametrize("N,K,rank,block", [(96, 512, 16, 128), (50, 4096, 16, 128), (33, 1024, 3, 128),
                                             (41, 3072, 16, 128), (23, 2560, 7, 64), (9, 12288, 16, 256),
-                                            (20, 384, 5, 128), (30, 256, 24, 32), (17, 96, 4, 32)])
+                                            (20, 384, 5, 128), (30, 256, 24, 32), (17, 96, 4, 32),
+                                            (20, 32768, 16, 128)])
 def test_quantize_weight_lora_merge_parity(N, K, rank, block):
     W = synth.normal_bf16(6, synth.STREAM_W, N, K, 0.02)
     A, B = synth.lora_pair(6, N, K, rank, 0.01)
@@ -605,7 +606,7 @@ def test_linear_bwd_x_bf16_parity(block):
     assert rel_fro(f64(got), f64(dY) @ f64(W)) <= REL_FRO_BF16
 
 
-@pytest.mark.parametrize("M,N,K,block", [(150, 768, 256, 32), (300, 512, 384, 128), (37, 1024, 256, 256)])
+@pytest.mark.parametrize("M,N,K,block", [(150, 768, 256, 32), (300, 512, 384, 128), (37, 1024, 256, 256), (40, 32768, 256, 128)])
 def test_linear_bwd_x_second_reading_parity(M, N, K, block):
     W = synth.normal_bf16(23, synth.STREAM_W, N, K, 0.02)
     wq, sw = oracle.quantize_weight(W, block)
