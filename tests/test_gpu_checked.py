@@ -123,7 +123,7 @@ def test_checked_quantize_weight_row_stride(N, K, ld, block):
 
 
 @pytest.mark.parametrize("N,K,rank,block", [(50, 4096, 16, 128), (33, 1024, 3, 128), (23, 2560, 7, 64),
-                                            (30, 256, 24, 32), (17, 96, 4, 32)])
+                                            (30, 256, 24, 32), (17, 96, 4, 32), (20, 32768, 16, 128)])
 def test_checked_quantize_weight_lora_merge(N, K, rank, block):
     W = torch_bf16(synth.normal_bf16(6, synth.STREAM_W, N, K, 0.02))
     A, B = synth.lora_pair(6, N, K, rank, 0.01)
@@ -132,7 +132,8 @@ def test_checked_quantize_weight_lora_merge(N, K, rank, block):
 
 
 @pytest.mark.parametrize("M,K,N,block,bias", [(300, 1024, 400, 128, True), (513, 4096, 272, 128, False),
-                                              (1, 48, 16, 16, True), (129, 1040, 272, 16, False)])
+                                              (1, 48, 16, 16, True), (129, 1040, 272, 16, False),
+                                              (17, 32768, 272, 128, True)])
 def test_checked_linear_fwd(M, K, N, block, bias):
     W = synth.normal_bf16(8, synth.STREAM_W, N, K, 0.02)
     wq, sw = oracle.quantize_weight(W, block)
@@ -143,7 +144,8 @@ def test_checked_linear_fwd(M, K, N, block, bias):
     _both(lambda: cr.convrot_linear_fwd_noalloc(x, Wq, s, block, bias=b))
 
 
-@pytest.mark.parametrize("M,K,N,rank", [(300, 1024, 272, 16), (65, 512, 128, 5), (5, 256, 4096, 16)])
+@pytest.mark.parametrize("M,K,N,rank", [(300, 1024, 272, 16), (65, 512, 128, 5), (5, 256, 4096, 16),
+                                        (17, 32768, 272, 16)])
 def test_checked_linear_fwd_lora(M, K, N, rank):
     block = 128
     W = synth.normal_bf16(12, synth.STREAM_W, N, K, 0.02)
@@ -155,7 +157,7 @@ def test_checked_linear_fwd_lora(M, K, N, rank):
 
 
 @pytest.mark.parametrize("block,K,N", [(32, 256, 768), (128, 256, 768), (16, 48, 400), (8, 80, 272),
-                                       (64, 192, 320), (256, 512, 512)])
+                                       (64, 192, 320), (256, 512, 512), (128, 256, 32768)])
 def test_checked_bwd_weight_and_grad_x(block, K, N):
     M = 150
     W = synth.normal_bf16(9, synth.STREAM_W, N, K, 0.02)
@@ -167,7 +169,8 @@ def test_checked_bwd_weight_and_grad_x(block, K, N):
     _both(lambda: cr.convrot_linear_bwd_x(dY, WtQ, swt, block))
 
 
-@pytest.mark.parametrize("N,K,block", [(80, 256, 32), (192, 1024, 128), (16, 512, 256), (64, 64, 8), (48, 48, 16)])
+@pytest.mark.parametrize("N,K,block", [(80, 256, 32), (192, 1024, 128), (16, 512, 256), (64, 64, 8), (48, 48, 16),
+                                       (64, 32768, 128)])
 def test_checked_dequant_weight_t(N, K, block):
     W = synth.normal_bf16(14, synth.STREAM_W, N, K, 0.02)
     wq, sw = oracle.quantize_weight(W, block)
@@ -175,7 +178,7 @@ def test_checked_dequant_weight_t(N, K, block):
     _both(lambda: cr.convrot_dequant_weight_t(Wq, s, block))
 
 
-@pytest.mark.parametrize("M,N,K,block", [(300, 544, 384, 32), (37, 1024, 256, 256)])
+@pytest.mark.parametrize("M,N,K,block", [(300, 544, 384, 32), (37, 1024, 256, 256), (40, 32768, 256, 128)])
 def test_checked_grad_x_bf16_and_second_reading(M, N, K, block):
     W = synth.normal_bf16(17, synth.STREAM_W, N, K, 0.02)
     wq, sw = oracle.quantize_weight(W, block)
@@ -185,7 +188,8 @@ def test_checked_grad_x_bf16_and_second_reading(M, N, K, block):
     _both(lambda: cr.convrot_linear_bwd_x_r2(dY, Wq, s, block))
 
 
-@pytest.mark.parametrize("V,D,block,n", [(1000, 512, 128, 300), (97, 48, 16, 130), (64, 4096, 128, 33)])
+@pytest.mark.parametrize("V,D,block,n", [(1000, 512, 128, 300), (97, 48, 16, 130), (64, 4096, 128, 33),
+                                         (64, 32768, 128, 40)])
 def test_checked_embedding_lookup(V, D, block, n):
     table = synth.normal_bf16(10, synth.STREAM_TABLE, V, D, 0.02)
     eq, se = oracle.quantize_rows_bf16(table, block)
