@@ -55,3 +55,35 @@ def test_step_replays_from_a_cuda_graph():
         torch.cuda.synchronize()
         assert torch.equal(y, y_eager) and torch.equal(dX, dx_eager)
     assert cr.convrot_get_error() == cr.OK
+
+
+def test_lora_bypass_forward_replays_from_a_cuda_graph():
+    """The forward with an unmerged adapter launches four kernels (activation quantizer, bypass operands,
+    weight widening, GEMM) on the caller's stream with a caller workspace: capturable, and the replay gives the
+    eager bits."""
+    M, K, N, b, r = 300, 1024, 272, 128, 16
+    x = torch_bf16(synth.activations_bf16(37, M, K, 4, 20.0))
+    W = torch_bf16(synth.normal_bf16(37, synth.STREAM_W, N, K, 0.02))
+    A, B = synth.lora_pair(37, N, K, r, 0.05)
+    A, B = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
+    bias = torch_bf16(synth.normal_bf16(37, 9, 1, N, 0.5)[0])
+    Wq, sw = cr.convrot_quantize_weight(W, b)
+    ws = torch.empty(cr.convrot_linear_lora_workspace_bytes(M, K, N), dtype=torch.uint8, device="cuda")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # eager call first: launch parameters are cached before capture
+        cr.convrot_linear_fwd_lora(x, Wq, sw, b, A, B, 16.0, 1.0, bias=bias, y=y, workspace=ws, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    y_eager = y.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cr.convrot_linear_fwd_lora(x, Wq, sw, b, A, B, 16.0, 1.0, bias=bias, y=y, workspace=ws,
+                                   stream=torch.cuda.current_stream())
+    for _ in range(2):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_eager)
+    assert cr.convrot_get_error() == cr.OK
