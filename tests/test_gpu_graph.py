@@ -87,3 +87,36 @@ def test_lora_bypass_forward_replays_from_a_cuda_graph():
         torch.cuda.synchronize()
         assert torch.equal(y, y_eager)
     assert cr.convrot_get_error() == cr.OK
+
+
+def test_bf16_and_second_reading_backward_replay_from_a_cuda_graph():
+    """The two other backward calls (the bf16 mode: transient weight + bf16 GEMM; the second reading of the int8
+    backward: four kernels) with caller workspaces: capturable, and the replays give the eager bits."""
+    M, N, K, b = 150, 512, 384, 128
+    W = torch_bf16(synth.normal_bf16(41, synth.STREAM_W, N, K, 0.02))
+    dY = torch_bf16(synth.normal_bf16(41, synth.STREAM_DY, M, N, 1e-3))
+    Wq, sw = cr.convrot_quantize_weight(W, b)
+    ws1 = torch.empty(cr.convrot_bwd_x_bf16_workspace_bytes(N, K), dtype=torch.uint8, device="cuda")
+    ws2 = torch.empty(cr.convrot_bwd_x_r2_workspace_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    d1 = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    d2 = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        cr.convrot_linear_bwd_x_bf16(dY, Wq, sw, b, dX=d1, workspace=ws1, stream=s)
+        cr.convrot_linear_bwd_x_r2(dY, Wq, sw, b, dX=d2, workspace=ws2, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    e1, e2 = d1.clone(), d2.clone()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st = torch.cuda.current_stream()
+        cr.convrot_linear_bwd_x_bf16(dY, Wq, sw, b, dX=d1, workspace=ws1, stream=st)
+        cr.convrot_linear_bwd_x_r2(dY, Wq, sw, b, dX=d2, workspace=ws2, stream=st)
+    for _ in range(2):
+        d1.zero_()
+        d2.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(d1, e1) and torch.equal(d2, e2)
+    assert cr.convrot_get_error() == cr.OK
