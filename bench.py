@@ -44,8 +44,8 @@ L2_FLUSH_BYTES = 256 << 20
 #   python -m int8_rotated_quantized_gb300.profile_case gemm_bf16 --M 20480 --N 4096 --K 16384 --reps 3  (bf16 grad_x)
 # keyed by the hash of the kernel source they were taken on; reported as null
 # once the kernel source differs (or where no capture was taken on it).
-GEMM_TRAFFIC = {"source_sha256_16": "3d784c87a8962024", "fwd": 1062780928 + 654667008, "bwd": 2915444736 + 162504192,
-                "bf16_bwd": 2854214656 + 162547968}
+GEMM_TRAFFIC = {"source_sha256_16": "5d91db25bf865fff", "fwd": 1072621056 + 654961152, "bwd": 3197371136 + 162885120,
+                "bf16_bwd": 3196183808 + 162829824}
 
 
 def _gemm_source_current():

@@ -955,17 +955,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 // if `group` of them (plus the streaming tiles of one wave) stay in L2; the
 // swept operand is then read once per group.  Measured on GB300, groups whose
 // tiles total more than about 32 MB no longer stay resident, so the group is
-// the largest count of tiles within that budget, but at least 8 (for 8 MB
-// tiles, K = 16384, 8 tiles measured 0.8% faster than the 4 of the budget on
-// the 20480-token grad_x shape; 2 MB tiles are unaffected), and the
-// orientation with the smaller estimated DRAM read volume wins.
+// the largest count of tiles within that budget, and the orientation with the
+// smaller estimated DRAM read volume wins.
 constexpr int64_t kRasterBudget = 32ll << 20;
-constexpr int64_t kRasterMinGroup = 8;
 
 void choose_raster(int64_t num_t, int64_t num_w, int64_t K, int64_t w_elem, int &group, int &group_weight) {
     const int64_t t_tile = (int64_t)TT * K * 2, w_tile = (int64_t)TW * K * w_elem;  // fp16/bf16 codes, int8 or bf16
-    const int64_t gt = std::max<int64_t>(1, std::min<int64_t>(num_t, std::max(kRasterMinGroup, kRasterBudget / t_tile)));
-    const int64_t gw = std::max<int64_t>(1, std::min<int64_t>(num_w, std::max(kRasterMinGroup, kRasterBudget / w_tile)));
+    const int64_t gt = std::max<int64_t>(1, std::min<int64_t>(num_t, kRasterBudget / t_tile));
+    const int64_t gw = std::max<int64_t>(1, std::min<int64_t>(num_w, kRasterBudget / w_tile));
     const int64_t reads_t = num_t * t_tile + num_w * w_tile * ((num_t + gt - 1) / gt);
     const int64_t reads_w = num_w * w_tile + num_t * t_tile * ((num_w + gw - 1) / gw);
     group_weight = reads_w < reads_t ? 1 : 0;
